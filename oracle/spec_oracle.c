@@ -1,0 +1,428 @@
+/*
+ * spec_oracle.c -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, fp64 CPU restatement of batched speculative-sampling verification.
+ * It exists to check the CUDA path; nothing in the product links, loads or calls it.
+ * Only the test suite, the smoke check and the CPU-baseline leg of the benchmark use it.
+ * It shares no source, header, table or constant with the CUDA path.
+ *
+ * Sources (web pages, cited by title and section):
+ *  [SpS]  "Speculative Decoding 为什么是 Lossless 的 — 详细证明教程" (speculative decoding lossless
+ *         proof tutorial): §2.2 notation (p = target, q = draft, a(x), (p-q)+, Z, p'), §5.1 algorithm
+ *         SpecSampleOne, §6.2-§6.4 proof steps, §7 worked examples, §8 Q1/Q2/Q4 pitfalls,
+ *         §9.1 gamma-step chain.
+ *  [Hedge] "Not-a-Bandit: Provably No-Regret Drafter Selection in Speculative Decoding for LLMs"
+ *         (HedgeSpec notes): Key design 1, counterfactual acceptance gamma_{j,i} = 1 - TV(p, q_i);
+ *         Key design 3, loss f_t[i] = 1 - gamma_t[i].
+ *  [Cactus] "Cactus: Accelerating Auto-Regressive Decoding with Constrained Acceptance Speculative
+ *         Sampling" (Cactus notes): Key design 1 (objective min{h_n/p(n),1}), Key design 2 (closed-form
+ *         h), Key design 3 (gamma* Taylor closed form). NOTE: that page writes q for the verifier
+ *         (target) and p for the draft -- the opposite of [SpS]. This file always says target/draft.
+ *  Philox4x32-10: Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3" (SC'11),
+ *         the counter-based generator; the pages do not fix a uniform source.
+ *
+ * Readings where the pages are silent (each also listed in the design notes):
+ *  - accept iff r * p_draft(t) < p_target(t)  (strict, no division; [SpS] §5.1 gives both forms);
+ *  - uniforms: Philox4x32-10, counter (pos, seq, stream, 0), key (seed lo, seed hi), word 0 mapped to
+ *    ((w >> 8) + 0.5) * 2^-24; stream 0 = accept r, stream 1 = resample / bonus u;
+ *  - inverse CDF in ascending token id: the smallest x whose running sum exceeds u * (total mass);
+ *  - a reject with Z <= 0 (possible only through rounding) resamples from the target row itself;
+ *  - bonus token (all K drafts accepted) is drawn from target row K with u = U(seed, b, K, stream 1);
+ *  - Cactus residual g = (h - p_draft)+ / sum (h - p_draft)+ (the page only says phi and g are
+ *    "derived back"); Cactus bonus row is the plain target row; p_target(n) = 1 gives gamma* = 1, s = 0.
+ *
+ * Build: gcc -O2 -std=c11 -fPIC -shared -fopenmp spec_oracle.c -o libspec_oracle.so -lm
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------------------------------ */
+/* Philox4x32-10 (SC'11 paper above): 10 rounds of the 4x32 S-box; the key is bumped by the   */
+/* Weyl constants between rounds.                                                             */
+/* ------------------------------------------------------------------------------------------ */
+#define PHILOX_M0 0xD2511F53u
+#define PHILOX_M1 0xCD9E8D57u
+#define PHILOX_W0 0x9E3779B9u
+#define PHILOX_W1 0xBB67AE85u
+
+void spec_oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4])
+{
+    uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+    uint32_t k0 = key[0], k1 = key[1];
+    for (int round = 0; round < 10; round++) {
+        if (round > 0) {
+            k0 += PHILOX_W0;
+            k1 += PHILOX_W1;
+        }
+        uint64_t prod0 = (uint64_t)PHILOX_M0 * (uint64_t)c0;
+        uint64_t prod1 = (uint64_t)PHILOX_M1 * (uint64_t)c2;
+        uint32_t hi0 = (uint32_t)(prod0 >> 32), lo0 = (uint32_t)prod0;
+        uint32_t hi1 = (uint32_t)(prod1 >> 32), lo1 = (uint32_t)prod1;
+        uint32_t n0 = hi1 ^ c1 ^ k0;
+        uint32_t n1 = lo1;
+        uint32_t n2 = hi0 ^ c3 ^ k1;
+        uint32_t n3 = lo0;
+        c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* Uniform on the 2^-24 grid strictly inside (0,1); exact in fp32 and fp64. */
+double spec_oracle_uniform(uint64_t seed, uint32_t seq, uint32_t pos, uint32_t stream)
+{
+    uint32_t ctr[4] = {pos, seq, stream, 0u};
+    uint32_t key[2] = {(uint32_t)(seed & 0xFFFFFFFFu), (uint32_t)(seed >> 32)};
+    uint32_t out[4];
+    spec_oracle_philox4x32_10(ctr, key, out);
+    return ((double)(out[0] >> 8) + 0.5) * (1.0 / 16777216.0);
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* Row access: bf16 (stored as uint16 bit patterns) or fp32 logits, converted exactly to double. */
+/* ------------------------------------------------------------------------------------------ */
+enum { ORACLE_BF16 = 0, ORACLE_FP32 = 1 };
+
+static void load_row(int dtype, const void* base, size_t row, int V, double* x)
+{
+    if (dtype == ORACLE_BF16) {
+        const uint16_t* h = (const uint16_t*)base + row * (size_t)V;
+        for (int v = 0; v < V; v++) {
+            uint32_t bits = (uint32_t)h[v] << 16;
+            float f;
+            memcpy(&f, &bits, sizeof f);
+            x[v] = (double)f;
+        }
+    } else {
+        const float* f = (const float*)base + row * (size_t)V;
+        for (int v = 0; v < V; v++) x[v] = (double)f[v];
+    }
+}
+
+/* Temperature softmax, max-subtracted: p = softmax(x / T). One T for target and draft is the
+ * "standardized sampling" rule of [SpS] §8 Q4 (otherwise the ratio compares two different
+ * distributions and losslessness is lost). Logits of -inf get probability 0. */
+void spec_oracle_softmax(const double* x, int V, double T, double* p)
+{
+    double M = -INFINITY;
+    for (int v = 0; v < V; v++) {
+        double z = x[v] / T;
+        if (z > M) M = z;
+    }
+    double S = 0.0;
+    for (int v = 0; v < V; v++) {
+        p[v] = exp(x[v] / T - M);
+        S += p[v];
+    }
+    for (int v = 0; v < V; v++) p[v] /= S;
+}
+
+/* Inverse CDF over a non-negative weight vector in ascending index order: the smallest x with
+ * w[0] + ... + w[x] > target. If rounding leaves no such x, the last index with w > 0.
+ * *margin = distance (in the same mass units) from target to the nearer of the chosen index's
+ * two CDF boundaries. */
+int spec_oracle_inverse_cdf(const double* w, int V, double target, double* margin)
+{
+    double cum = 0.0;
+    int last_pos = -1;
+    for (int x = 0; x < V; x++) {
+        if (w[x] > 0.0) last_pos = x;
+        double before = cum;
+        cum += w[x];
+        if (w[x] > 0.0 && cum > target) {
+            if (margin) {
+                double a = target - before, b = cum - target;
+                *margin = a < b ? a : b;
+            }
+            return x;
+        }
+    }
+    if (margin) *margin = 0.0;
+    return last_pos;
+}
+
+/* One verification step, [SpS] §5.1 SpecSampleOne, generalised to any target distribution h
+ * (h = p_target for standard speculative sampling; h = the Cactus target for the constrained
+ * variant, [Cactus] Key design 1: accept with min{h_n / p_draft(n), 1}).
+ *  1. the draft token t was drawn from the draft distribution (an input here);
+ *  2. accept iff r * p_draft(t) < h(t), i.e. r < min(1, h(t)/p_draft(t));
+ *  3. otherwise draw from p'(x) = (h(x) - p_draft(x))+ / Z with Z = sum_x (h(x) - p_draft(x))+.
+ * mutation (tests only, plants the pitfalls of [SpS] §8): 1 = resample from h itself on reject (Q1),
+ * 2 = resample from |h - p_draft| (Q2). 0 = the algorithm as written.
+ * Outputs: *accepted, *Z (always computed), *accept_margin = |r - h(t)/p_draft(t)|,
+ * *cdf_margin (only meaningful when rejected). Returns the emitted token. */
+int spec_oracle_sample_one(const double* h, const double* pd, int V, int t, double r, double u,
+                           int mutation, int* accepted, double* Z, double* accept_margin,
+                           double* cdf_margin, double* scratch)
+{
+    double z = 0.0;
+    for (int x = 0; x < V; x++) {
+        double d = h[x] - pd[x];
+        z += d > 0.0 ? d : 0.0;
+    }
+    if (Z) *Z = z;
+    if (accept_margin) *accept_margin = pd[t] > 0.0 ? fabs(r - h[t] / pd[t]) : INFINITY;
+    if (r * pd[t] < h[t]) {
+        *accepted = 1;
+        if (cdf_margin) *cdf_margin = INFINITY;
+        return t;
+    }
+    *accepted = 0;
+    double* w = scratch;
+    double total = 0.0;
+    for (int x = 0; x < V; x++) {
+        double d = h[x] - pd[x];
+        if (mutation == 1) w[x] = h[x];
+        else if (mutation == 2) w[x] = fabs(d);
+        else w[x] = d > 0.0 ? d : 0.0;
+        total += w[x];
+    }
+    if (!(total > 0.0)) { /* rounding-only reject: fall back to the target row */
+        total = 0.0;
+        for (int x = 0; x < V; x++) { w[x] = h[x]; total += w[x]; }
+    }
+    return spec_oracle_inverse_cdf(w, V, u * total, cdf_margin);
+}
+
+/* Cactus target distribution, [Cactus] Key design 2 and 3 (translated: the page's q is the target,
+ * its p is the draft). With q = p_target(n) for the candidate n:
+ *   gamma* = min(q + sqrt(2 delta q (1 - q)), 1),
+ *   h_n = gamma*,  h_i = (1 - gamma*) / (1 - q) * p_target(i) for i != n.
+ * q = 1 gives gamma* = 1 and the other entries 0. Returns gamma*. */
+double spec_oracle_cactus_h(const double* pt, int V, int n, double delta, double* h)
+{
+    double q = pt[n];
+    double g = q + sqrt(2.0 * delta * q * (1.0 - q));
+    if (g > 1.0) g = 1.0;
+    double s = (q < 1.0) ? (1.0 - g) / (1.0 - q) : 0.0;
+    for (int i = 0; i < V; i++) h[i] = s * pt[i];
+    h[n] = g;
+    return g;
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* Batched calls.                                                                             */
+/* ------------------------------------------------------------------------------------------ */
+/* The chain keeps per-position row pointers on the stack. */
+#define ORACLE_MAX_K 64
+
+/* The gamma-step chain of [SpS] §9.1 for one sequence: verify draft positions left to right, stop at
+ * the first reject and emit the residual draw there; if every draft is accepted, emit one token from
+ * target row K. The per-position quantities (diag, margins) are computed for every j, also after the
+ * chain stopped, because the batched output reports them for all positions.
+ *   hrows[j] : the target distribution used at position j (p_target, or the Cactus h)
+ *   drows[j] : the draft distribution at position j
+ *   bonus    : target row K (plain softmax). */
+static void chain_one(double** hrows, double** drows, const double* bonus, int K, int V,
+                      const int32_t* tok, uint64_t seed, uint32_t seq, int mutation,
+                      int32_t* accept_len, int32_t* out, double* diag, double* acc_margin,
+                      double* cdf_margin, double* scratch)
+{
+    int L = K, emitted = -1;
+    double cm = INFINITY;
+    for (int j = 0; j < K; j++) {
+        double r = spec_oracle_uniform(seed, seq, (uint32_t)j, 0u);
+        double u = spec_oracle_uniform(seed, seq, (uint32_t)j, 1u);
+        int acc = 0;
+        double Z = 0.0, am = 0.0, c = INFINITY;
+        int e = spec_oracle_sample_one(hrows[j], drows[j], V, tok[j], r, u,
+                                       (L == K) ? mutation : 0, &acc, &Z, &am, &c, scratch);
+        if (diag) {
+            diag[4 * j + 0] = hrows[j][tok[j]];
+            diag[4 * j + 1] = drows[j][tok[j]];
+            diag[4 * j + 2] = Z;
+            diag[4 * j + 3] = r;
+        }
+        if (acc_margin) acc_margin[j] = am;
+        if (L == K) {
+            if (acc) {
+                out[j] = tok[j];
+            } else {
+                L = j;
+                emitted = e;
+                cm = c;
+            }
+        }
+    }
+    if (L == K) {
+        double u = spec_oracle_uniform(seed, seq, (uint32_t)K, 1u);
+        double total = 0.0;
+        for (int x = 0; x < V; x++) total += bonus[x];
+        emitted = spec_oracle_inverse_cdf(bonus, V, u * total, &cm);
+    }
+    out[L] = emitted;
+    for (int j = L + 1; j <= K; j++) out[j] = -1;
+    *accept_len = L;
+    if (cdf_margin) *cdf_margin = cm;
+}
+
+static int nthreads_or_default(int n)
+{
+#ifdef _OPENMP
+    return n > 0 ? n : omp_get_max_threads();
+#else
+    (void)n;
+    return 1;
+#endif
+}
+
+/* Standard speculative sampling over a batch ([SpS] §5.1 + §9.1).
+ * target [B, K+1, V], draft [B, K, V] (dtype: 0 = bf16 bit patterns, 1 = fp32), tokens [B, K],
+ * seeds [B]; seq_index [B] (nullable) gives the sequence number used in the Philox counter
+ * (identity when NULL). Returns -1 (and computes nothing) unless 1 <= K <= 64 and V >= 1. Outputs: accept_len [B], out_tokens [B, K+1] (-1 padded),
+ * diag [B, K, 4] = (p_target(t), p_draft(t), Z, r) (nullable), accept_margin [B, K] (nullable),
+ * cdf_margin [B] (nullable). mutation: see spec_oracle_sample_one. Returns 0. */
+int spec_oracle_verify(int dtype, const void* target, const void* draft, const int32_t* tokens,
+                       const uint64_t* seeds, const int32_t* seq_index, int B, int K, int V,
+                       double T, int mutation, int32_t* accept_len, int32_t* out_tokens,
+                       double* diag, double* accept_margin, double* cdf_margin, int nthreads)
+{
+    if (K < 1 || K > ORACLE_MAX_K || V < 1 || B < 0) return -1;
+    int nt = nthreads_or_default(nthreads);
+#pragma omp parallel for schedule(dynamic) num_threads(nt)
+    for (int b = 0; b < B; b++) {
+        double* x = (double*)malloc(sizeof(double) * (size_t)V);
+        double* scratch = (double*)malloc(sizeof(double) * (size_t)V);
+        double* store = (double*)malloc(sizeof(double) * (size_t)V * (size_t)(2 * K + 1));
+        double* hrows[ORACLE_MAX_K];
+        double* drows[ORACLE_MAX_K];
+        for (int j = 0; j < K; j++) {
+            hrows[j] = store + (size_t)j * V;
+            drows[j] = store + (size_t)(K + j) * V;
+            load_row(dtype, target, (size_t)b * (K + 1) + j, V, x);
+            spec_oracle_softmax(x, V, T, hrows[j]);
+            load_row(dtype, draft, (size_t)b * K + j, V, x);
+            spec_oracle_softmax(x, V, T, drows[j]);
+        }
+        double* bonus = store + (size_t)(2 * K) * V;
+        load_row(dtype, target, (size_t)b * (K + 1) + K, V, x);
+        spec_oracle_softmax(x, V, T, bonus);
+        uint32_t seq = seq_index ? (uint32_t)seq_index[b] : (uint32_t)b;
+        chain_one(hrows, drows, bonus, K, V, tokens + (size_t)b * K, seeds[b], seq, mutation,
+                  accept_len + b, out_tokens + (size_t)b * (K + 1),
+                  diag ? diag + (size_t)b * K * 4 : NULL,
+                  accept_margin ? accept_margin + (size_t)b * K : NULL,
+                  cdf_margin ? cdf_margin + b : NULL, scratch);
+        free(store);
+        free(scratch);
+        free(x);
+    }
+    return 0;
+}
+
+/* Cactus constrained acceptance over a batch ([Cactus] Key design 1-3 inside the [SpS] §9.1 chain).
+ * Same layout as spec_oracle_verify plus delta >= 0 and gamma_star [B, K] (nullable). At each
+ * position the target distribution of the chain is h built from the target row and the draft token;
+ * the bonus row is the plain target row. diag's first entry is h(t) = gamma*. */
+int spec_oracle_cactus(int dtype, const void* target, const void* draft, const int32_t* tokens,
+                       const uint64_t* seeds, const int32_t* seq_index, int B, int K, int V,
+                       double T, double delta, int32_t* accept_len, int32_t* out_tokens,
+                       double* diag, double* gamma_star, double* accept_margin,
+                       double* cdf_margin, int nthreads)
+{
+    if (K < 1 || K > ORACLE_MAX_K || V < 1 || B < 0) return -1;
+    int nt = nthreads_or_default(nthreads);
+#pragma omp parallel for schedule(dynamic) num_threads(nt)
+    for (int b = 0; b < B; b++) {
+        double* x = (double*)malloc(sizeof(double) * (size_t)V);
+        double* pt = (double*)malloc(sizeof(double) * (size_t)V);
+        double* scratch = (double*)malloc(sizeof(double) * (size_t)V);
+        double* store = (double*)malloc(sizeof(double) * (size_t)V * (size_t)(2 * K + 1));
+        double* hrows[ORACLE_MAX_K];
+        double* drows[ORACLE_MAX_K];
+        for (int j = 0; j < K; j++) {
+            hrows[j] = store + (size_t)j * V;
+            drows[j] = store + (size_t)(K + j) * V;
+            load_row(dtype, target, (size_t)b * (K + 1) + j, V, x);
+            spec_oracle_softmax(x, V, T, pt);
+            double g = spec_oracle_cactus_h(pt, V, tokens[(size_t)b * K + j], delta, hrows[j]);
+            if (gamma_star) gamma_star[(size_t)b * K + j] = g;
+            load_row(dtype, draft, (size_t)b * K + j, V, x);
+            spec_oracle_softmax(x, V, T, drows[j]);
+        }
+        double* bonus = store + (size_t)(2 * K) * V;
+        load_row(dtype, target, (size_t)b * (K + 1) + K, V, x);
+        spec_oracle_softmax(x, V, T, bonus);
+        uint32_t seq = seq_index ? (uint32_t)seq_index[b] : (uint32_t)b;
+        chain_one(hrows, drows, bonus, K, V, tokens + (size_t)b * K, seeds[b], seq, 0,
+                  accept_len + b, out_tokens + (size_t)b * (K + 1),
+                  diag ? diag + (size_t)b * K * 4 : NULL,
+                  accept_margin ? accept_margin + (size_t)b * K : NULL,
+                  cdf_margin ? cdf_margin + b : NULL, scratch);
+        free(store);
+        free(scratch);
+        free(pt);
+        free(x);
+    }
+    return 0;
+}
+
+/* HedgeSpec counterfactual evaluation ([Hedge] Key design 1): for every drafter i, sequence b and
+ * level j < K, gamma[i,b,j] = sum_x min(p_target(x), q_i(x)), the acceptance probability of
+ * drafter i at that level ([SpS] §6.3: P(accept) = sum_x min(p, q) = 1 - TV). tv[i,b,j] =
+ * 1/2 sum_x |p_target(x) - q_i(x)| is computed separately so that a test can check the identity.
+ * The loss for the acceptance-probability objective is 1 - gamma ([Hedge] Key design 3); callers
+ * form it from gamma.
+ * target [B, K+1, V], drafters [N, B, K, V]. If selected >= 0, the chain of drafter `selected` is also
+ * verified exactly as spec_oracle_verify would with draft = drafters[selected]; the verify outputs
+ * may then not be NULL. */
+int spec_oracle_counterfactual(int dtype, const void* target, const void* drafters, int N, int B,
+                               int K, int V, double T, double* gamma, double* tv, int selected,
+                               const int32_t* tokens, const uint64_t* seeds,
+                               const int32_t* seq_index, int32_t* accept_len, int32_t* out_tokens,
+                               double* diag, double* accept_margin, double* cdf_margin,
+                               int nthreads)
+{
+    if (K < 1 || K > ORACLE_MAX_K || V < 1 || B < 0) return -1;
+    int nt = nthreads_or_default(nthreads);
+#pragma omp parallel for schedule(dynamic) num_threads(nt)
+    for (int b = 0; b < B; b++) {
+        double* x = (double*)malloc(sizeof(double) * (size_t)V);
+        double* q = (double*)malloc(sizeof(double) * (size_t)V);
+        double* scratch = (double*)malloc(sizeof(double) * (size_t)V);
+        double* store = (double*)malloc(sizeof(double) * (size_t)V * (size_t)(2 * K + 1));
+        double* hrows[ORACLE_MAX_K];
+        double* drows[ORACLE_MAX_K];
+        for (int j = 0; j < K; j++) {
+            hrows[j] = store + (size_t)j * V;
+            drows[j] = store + (size_t)(K + j) * V;
+            load_row(dtype, target, (size_t)b * (K + 1) + j, V, x);
+            spec_oracle_softmax(x, V, T, hrows[j]);
+            for (int i = 0; i < N; i++) {
+                size_t row = ((size_t)i * B + b) * K + j;
+                load_row(dtype, drafters, row, V, x);
+                spec_oracle_softmax(x, V, T, q);
+                double overlap = 0.0, dist = 0.0;
+                for (int v = 0; v < V; v++) {
+                    double pv = hrows[j][v], qv = q[v];
+                    overlap += pv < qv ? pv : qv;
+                    dist += fabs(pv - qv);
+                }
+                size_t o = ((size_t)i * B + b) * K + j;
+                if (gamma) gamma[o] = overlap;
+                if (tv) tv[o] = 0.5 * dist;
+                if (i == selected) memcpy(drows[j], q, sizeof(double) * (size_t)V);
+            }
+        }
+        if (selected >= 0 && selected < N) {
+            double* bonus = store + (size_t)(2 * K) * V;
+            load_row(dtype, target, (size_t)b * (K + 1) + K, V, x);
+            spec_oracle_softmax(x, V, T, bonus);
+            uint32_t seq = seq_index ? (uint32_t)seq_index[b] : (uint32_t)b;
+            chain_one(hrows, drows, bonus, K, V, tokens + (size_t)b * K, seeds[b], seq, 0,
+                      accept_len + b, out_tokens + (size_t)b * (K + 1),
+                      diag ? diag + (size_t)b * K * 4 : NULL,
+                      accept_margin ? accept_margin + (size_t)b * K : NULL,
+                      cdf_margin ? cdf_margin + b : NULL, scratch);
+        }
+        free(store);
+        free(scratch);
+        free(q);
+        free(x);
+    }
+    return 0;
+}

@@ -1,0 +1,492 @@
+"""Pins of the fp64 oracle to facts fixed outside itself (CPU only).
+
+Sources: the lossless-proof tutorial "Speculative Decoding 为什么是 Lossless 的 — 详细证明教程" (the
+worked cat/dog/fish example of §2.3/§6/§7.1, the special cases of §7.2/§7.3, the pitfalls of §8 Q1/Q2,
+the chain of §9.1); the HedgeSpec notes "Not-a-Bandit: Provably No-Regret Drafter Selection in
+Speculative Decoding for LLMs" (Key design 1: gamma = 1 - TV); the Cactus notes "Cactus: Accelerating
+Auto-Regressive Decoding with Constrained Acceptance Speculative Sampling" (Key design 1-3: gamma*,
+closed-form h, delta = 0 is standard speculative sampling, the KL bound when gamma* <= 0.5, and the
+Theorem 3 bound KL(h_alg || target) <= KL(draft || target)); and the Philox4x32-10 known answers.
+
+Exact laws are obtained by enumerating the oracle's own decisions over the whole 2^-24 grid of
+uniforms (bisection on the monotone accept and inverse-CDF decisions), so a wrong sign, index or term
+anywhere in the accept test, the residual or the inverse CDF changes an enumerated probability.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+from scipy import special, stats
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+GRID = 1 << 24
+
+
+def _golden_kv(name):
+    d = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            k, *vals = line.split()
+            d[k] = np.array([float(v) for v in vals])
+    return d
+
+
+# ----------------------------------------------------------------------------------------------
+# enumeration helpers (drive the oracle's decisions; no re-implementation of the rule)
+# ----------------------------------------------------------------------------------------------
+def accept_fraction(h, pd, t):
+    """Fraction of the 2^24 grid uniforms r that the oracle accepts for candidate t."""
+    lo, hi = 0, GRID
+    while lo < hi:
+        mid = (lo + hi) // 2
+        _, acc, *_ = oracle.sample_one(h, pd, t, (mid + 0.5) / GRID, 0.5)
+        if acc:
+            lo = mid + 1
+        else:
+            hi = mid
+    return lo / GRID
+
+
+def resample_law(h, pd, t, mutation=0):
+    """Law of the token the oracle emits after a reject at candidate t, over the u grid."""
+    V = len(h)
+    r_rej = (GRID - 0.5) / GRID
+    _, acc, *_ = oracle.sample_one(h, pd, t, r_rej, 0.5, mutation)
+    if acc:
+        return None
+
+    def tok(k):
+        return oracle.sample_one(h, pd, t, r_rej, (k + 0.5) / GRID, mutation)[0]
+
+    law = np.zeros(V)
+    start = 0
+    while start < GRID:
+        x = tok(start)
+        lo, hi = start, GRID          # first k with tok(k) > x
+        while lo < hi:
+            mid = (lo + hi) // 2
+            if tok(mid) > x:
+                hi = mid
+            else:
+                lo = mid + 1
+        law[x] += (lo - start) / GRID
+        start = lo
+    return law
+
+
+def output_law(h, pd, mutation=0, h_of=None):
+    """P(output = x) of one verification step with the draft token t ~ pd, enumerated exactly.
+    h_of(t) gives the target distribution used for candidate t (Cactus); default h."""
+    V = len(pd)
+    law = np.zeros(V)
+    for t in range(V):
+        if pd[t] == 0.0:
+            continue
+        ht = h if h_of is None else h_of(t)
+        a = accept_fraction(ht, pd, t)
+        law[t] += pd[t] * a
+        if a < 1.0:
+            law += pd[t] * (1.0 - a) * resample_law(ht, pd, t, mutation)
+    return law
+
+
+# ----------------------------------------------------------------------------------------------
+# Philox
+# ----------------------------------------------------------------------------------------------
+def test_philox_known_answers():
+    n = 0
+    with open(os.path.join(GOLDEN, "philox4x32_10_kat.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            left, right = line.split("|")
+            vals = [int(v, 16) for v in left.split()]
+            want = [int(v, 16) for v in right.split()]
+            got = oracle.philox4x32_10(vals[:4], vals[4:6])
+            assert [int(g) for g in got] == want
+            n += 1
+    assert n == 3
+
+
+def test_uniform_grid_and_streams():
+    us = [oracle.uniform(s, b, j, st) for s in (0, 1, 2**40 + 3) for b in range(4) for j in range(6) for st in (0, 1)]
+    for u in us:
+        assert 0.0 < u < 1.0
+        k = u * GRID - 0.5
+        assert k == int(k)                      # on the 2^-24 grid
+    assert len(set(us)) == len(us)              # counter and key both reach the output
+    w0 = oracle.philox4x32_10([3, 2, 1, 0], [7, 0])[0]
+    assert oracle.uniform(7, 2, 3, 1) == ((int(w0) >> 8) + 0.5) / GRID
+
+
+def test_uniform_is_uniform():
+    us = np.array([oracle.uniform(11, b, j, 0) for b in range(200) for j in range(50)])
+    assert stats.kstest(us, "uniform").pvalue > 1e-4
+
+
+# ----------------------------------------------------------------------------------------------
+# softmax / inverse CDF against library routines
+# ----------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("T", [1.0, 0.7, 2.5])
+def test_softmax_matches_scipy(T):
+    rng = np.random.default_rng(5)
+    x = rng.normal(0, 3, 4099)
+    assert np.allclose(oracle.softmax(x, T), special.softmax(x / T), rtol=1e-13, atol=1e-300)
+    assert np.allclose(oracle.softmax(x + 123.0, T), oracle.softmax(x, T), rtol=1e-12, atol=0)
+
+
+def test_softmax_masked_logits():
+    x = np.array([-np.inf, math.log(0.75), -np.inf, math.log(0.25)])
+    p = oracle.softmax(x, 1.0)
+    assert p[0] == 0.0 and p[2] == 0.0
+    assert np.allclose(p, [0, 0.75, 0, 0.25], atol=1e-15)
+
+
+def test_inverse_cdf_matches_searchsorted():
+    rng = np.random.default_rng(9)
+    for _ in range(200):
+        w = rng.random(37) * (rng.random(37) > 0.3)
+        if w.sum() == 0:
+            continue
+        target = rng.random() * w.sum()
+        x, margin = oracle.inverse_cdf(w, target)
+        c = np.cumsum(w)
+        assert x == int(np.searchsorted(c, target, side="right"))
+        assert w[x] > 0
+        assert margin == pytest.approx(min(target - (c[x] - w[x]), c[x] - target), abs=1e-12)
+
+
+def test_inverse_cdf_never_picks_zero_mass():
+    w = np.array([0.0, 0.5, 0.0, 0.5, 0.0])
+    for target in [0.0, 0.25, 0.5, 0.75, 0.9999999, 1.0, 1.5]:
+        x, _ = oracle.inverse_cdf(w, target)
+        assert x in (1, 3)
+
+
+# ----------------------------------------------------------------------------------------------
+# the worked example of the lossless tutorial
+# ----------------------------------------------------------------------------------------------
+def test_worked_example_quantities():
+    g = _golden_kv("sps_worked_example.txt")
+    p, q = g["p"], g["q"]
+    for t in range(3):
+        assert accept_fraction(p, q, t) == pytest.approx(g["a"][t], abs=2.0 / GRID)
+        _, _, Z, _, _ = oracle.sample_one(p, q, t, 0.5, 0.5)
+        assert Z == pytest.approx(g["Z"][0], abs=1e-15)
+    # acceptance path: P(x and accept) = q(x) a(x) = min(p, q)(x)
+    for t in range(3):
+        assert q[t] * accept_fraction(p, q, t) == pytest.approx(g["p_x_accept"][t], abs=1e-6)
+    # reject path only ever emits cat (p' = (1, 0, 0)); dog is the only candidate that can be rejected
+    assert resample_law(p, q, 1) == pytest.approx(g["p_prime"], abs=0)
+    assert resample_law(p, q, 0) is None and resample_law(p, q, 2) is None
+    law = output_law(p, q)
+    assert law == pytest.approx(g["p_out"], abs=1e-6)
+    # P(x and reject) = (p - q)+
+    acc_part = np.array([q[t] * accept_fraction(p, q, t) for t in range(3)])
+    assert law - acc_part == pytest.approx(g["p_x_reject"], abs=1e-6)
+
+
+def test_worked_example_batched_counterfactual():
+    g = _golden_kv("sps_worked_example.txt")
+    tgt = np.log(np.array([[g["p"], g["p"]]], dtype=np.float64)).astype(np.float32)
+    drf = np.log(np.array([[[g["q"]]]], dtype=np.float64)).astype(np.float32)
+    out = oracle.counterfactual(tgt, drf)
+    assert out["gamma"][0, 0, 0] == pytest.approx(g["p_accept"][0], abs=1e-7)
+    assert out["tv"][0, 0, 0] == pytest.approx(1 - g["p_accept"][0], abs=1e-7)
+    assert out["loss"][0, 0, 0] == pytest.approx(g["Z"][0], abs=1e-7)
+
+
+def test_pitfall_q1_resample_from_target_is_biased():
+    g = _golden_kv("sps_worked_example.txt")
+    law = output_law(g["p"], g["q"], mutation=1)
+    assert law[0] == pytest.approx(g["q1_p_cat"][0], abs=1e-6)
+    assert abs(law[0] - g["p"][0]) > 0.05
+
+
+def test_pitfall_q2_absolute_difference_is_biased():
+    g = _golden_kv("sps_worked_example.txt")
+    law = output_law(g["p"], g["q"], mutation=2)
+    assert law[1] > g["p"][1] + 0.05           # dog pushed above 0.3
+    assert law.sum() == pytest.approx(1.0, abs=1e-6)
+
+
+def test_perfect_draft_never_rejects():
+    rng = np.random.default_rng(1)
+    p = special.softmax(rng.normal(0, 2, 6))
+    for t in range(6):
+        assert accept_fraction(p, p, t) == 1.0
+        _, _, Z, _, _ = oracle.sample_one(p, p, t, 0.5, 0.5)
+        assert Z == 0.0
+    assert output_law(p, p) == pytest.approx(p, abs=1e-6)
+
+
+def test_disjoint_support_always_rejects_and_resamples_target():
+    p = np.array([0.0, 0.75, 0.25])
+    q = np.array([1.0, 0.0, 0.0])
+    assert accept_fraction(p, q, 0) == 0.0
+    _, _, Z, _, _ = oracle.sample_one(p, q, 0, 0.5, 0.5)
+    assert Z == pytest.approx(1.0, abs=1e-15)
+    assert resample_law(p, q, 0) == pytest.approx(p, abs=1e-6)
+    assert output_law(p, q) == pytest.approx(p, abs=1e-6)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2, 3])
+def test_lossless_exact_enumeration_random(seed):
+    rng = np.random.default_rng(100 + seed)
+    V = 5
+    p = special.softmax(rng.normal(0, 2, V))
+    q = special.softmax(rng.normal(0, 2, V))
+    if seed == 3:
+        p[2] = 0.0
+        p /= p.sum()
+    assert output_law(p, q) == pytest.approx(p, abs=2e-6)
+
+
+def test_money_identity_and_one_minus_tv():
+    rng = np.random.default_rng(3)
+    B, K, V, N = 3, 2, 257, 4
+    tgt = rng.normal(0, 3, (B, K + 1, V)).astype(np.float32)
+    drf = (tgt[None, :, :K] + rng.normal(0, 1.5, (N, B, K, V))).astype(np.float32)
+    out = oracle.counterfactual(tgt, drf, temperature=0.8)
+    assert np.all(np.abs(out["gamma"] + out["tv"] - 1.0) < 1e-12)
+    assert np.all((out["gamma"] > 0) & (out["gamma"] < 1))
+    # Z of the verify path equals 1 - gamma (P(reject) = Z, tutorial §6.4 Step 3a)
+    tok = rng.integers(0, V, (B, K)).astype(np.int32)
+    v = oracle.verify(tgt, drf[1], tok, np.arange(B, dtype=np.uint64), temperature=0.8)
+    assert np.allclose(v["diag"][:, :, 2], 1.0 - out["gamma"][1], atol=1e-12)
+
+
+def test_gamma_special_cases():
+    rng = np.random.default_rng(4)
+    x = rng.normal(0, 2, (1, 2, 16)).astype(np.float32)
+    out = oracle.counterfactual(x, x[None, :, :1].copy())
+    assert out["gamma"][0, 0, 0] == pytest.approx(1.0, abs=1e-14)
+    tgt = np.full((1, 2, 4), -np.inf, np.float32)
+    tgt[0, :, 2:] = 0.0
+    drf = np.full((1, 1, 1, 4), -np.inf, np.float32)
+    drf[0, 0, 0, :2] = 0.0
+    out = oracle.counterfactual(tgt, drf)
+    assert out["gamma"][0, 0, 0] == 0.0
+
+
+# ----------------------------------------------------------------------------------------------
+# batched sampling: chi-square losslessness, mutations, chain
+# ----------------------------------------------------------------------------------------------
+def _batch_same_rows(p_rows, q_rows, bonus, n, rng):
+    """n sequences sharing the same rows; draft tokens drawn from q with numpy's generator."""
+    K = len(q_rows)
+    V = len(bonus)
+    tgt = np.log(np.array([list(p_rows) + [bonus]] * n)).astype(np.float32)
+    drf = np.log(np.array([list(q_rows)] * n)).astype(np.float32)
+    tok = np.stack([rng.choice(V, size=n, p=q_rows[j] / q_rows[j].sum()) for j in range(K)], 1).astype(np.int32)
+    return tgt, drf, tok
+
+
+def _chi2_p(counts, probs):
+    m = probs > 0
+    assert counts[~m].sum() == 0
+    exp = probs[m] / probs[m].sum() * counts.sum()
+    return stats.chisquare(counts[m], exp).pvalue
+
+
+def test_chi2_lossless_worked_example_and_mutations():
+    g = _golden_kv("sps_worked_example.txt")
+    rng = np.random.default_rng(7)
+    n = 60000
+    tgt, drf, tok = _batch_same_rows([g["p"]], [g["q"]], g["p"], n, rng)
+    seeds = np.arange(n, dtype=np.uint64) * 7919 + 5
+    p_true = g["p"] / g["p"].sum()
+    with np.errstate(divide="ignore"):
+        pass
+    good = oracle.verify(tgt, drf, tok, seeds)
+    c = np.bincount(good["out_tokens"][:, 0], minlength=3)
+    assert _chi2_p(c, p_true) > 1e-6
+    assert abs(good["accept_len"].mean() - g["p_accept"][0]) < 0.01
+    for mut in (1, 2):
+        bad = oracle.verify(tgt, drf, tok, seeds, mutation=mut)
+        c = np.bincount(bad["out_tokens"][:, 0], minlength=3)
+        assert _chi2_p(c, p_true) < 1e-6
+
+
+def test_chi2_chain_levels():
+    rng = np.random.default_rng(8)
+    V, K, n = 8, 3, 40000
+    P = [special.softmax(rng.normal(0, 1.5, V)) for _ in range(K + 1)]
+    Q = [special.softmax(np.log(P[j]) + rng.normal(0, 1.0, V)) for j in range(K)]
+    tgt, drf, tok = _batch_same_rows(P[:K], Q, P[K], n, rng)
+    seeds = np.full(n, 42, dtype=np.uint64)      # one key; the sequence number in the counter separates them
+    out = oracle.verify(tgt, drf, tok, seeds)
+    L = out["accept_len"]
+    for j in range(K + 1):
+        reach = L >= j
+        c = np.bincount(out["out_tokens"][reach, j], minlength=V)
+        assert reach.sum() > 1000
+        assert _chi2_p(c, P[j]) > 1e-6, j
+    gam = [np.minimum(P[j], Q[j]).sum() for j in range(K)]
+    for j in range(K):
+        reach = L >= j
+        assert abs((L[reach] > j).mean() - gam[j]) < 4 * math.sqrt(gam[j] * (1 - gam[j]) / reach.sum()) + 1e-3
+    assert np.all(out["out_tokens"][np.arange(n), L] >= 0)
+    assert all(np.all(out["out_tokens"][L == l, l + 1:] == -1) for l in range(K))
+
+
+def test_counterfactual_gamma_matches_monte_carlo_acceptance():
+    rng = np.random.default_rng(12)
+    V, n, N = 16, 30000, 3
+    p = special.softmax(rng.normal(0, 2, V))
+    qs = [special.softmax(np.log(p) + rng.normal(0, s, V)) for s in (0.5, 1.5, 3.0)]
+    tgt = np.log(np.array([[p, p]])).astype(np.float32)
+    drf = np.log(np.array(qs))[:, None, None, :].astype(np.float32)
+    gam = oracle.counterfactual(tgt, drf)["gamma"][:, 0, 0]
+    for i in range(N):
+        t2, d2, tok = _batch_same_rows([p], [qs[i]], p, n, rng)
+        out = oracle.verify(t2, d2, tok, np.arange(n, dtype=np.uint64))
+        rate = out["accept_len"].mean()
+        sd = math.sqrt(gam[i] * (1 - gam[i]) / n)
+        assert abs(rate - gam[i]) < 4 * sd + 1e-3
+
+
+def test_seq_index_selects_counter():
+    rng = np.random.default_rng(13)
+    B, K, V = 6, 3, 50
+    tgt = rng.normal(0, 2, (B, K + 1, V)).astype(np.float32)
+    drf = (tgt[:, :K] + rng.normal(0, 2, (B, K, V))).astype(np.float32)
+    tok = rng.integers(0, V, (B, K)).astype(np.int32)
+    seeds = np.arange(B, dtype=np.uint64) + 9
+    full = oracle.verify(tgt, drf, tok, seeds)
+    sub = [1, 4]
+    part = oracle.verify(tgt[sub], drf[sub], tok[sub], seeds[sub], seq_index=np.array(sub))
+    assert np.array_equal(part["out_tokens"], full["out_tokens"][sub])
+    assert np.array_equal(part["diag"], full["diag"][sub])
+
+
+def test_bf16_input_is_exact_conversion():
+    rng = np.random.default_rng(14)
+    x32 = rng.normal(0, 3, (2, 3, 64)).astype(np.float32)
+    bits = (x32.view(np.uint32) >> 16).astype(np.uint16)          # truncate to bf16
+    back = (bits.astype(np.uint32) << 16).view(np.float32)
+    d32 = (back[:, :2] + 0.5).astype(np.float32)
+    dbits = (d32.view(np.uint32) >> 16).astype(np.uint16)
+    dback = (dbits.astype(np.uint32) << 16).view(np.float32)
+    tok = np.zeros((2, 2), np.int32)
+    a = oracle.verify(bits, dbits, tok, np.arange(2, dtype=np.uint64))
+    b = oracle.verify(back, dback, tok, np.arange(2, dtype=np.uint64))
+    assert np.array_equal(a["diag"], b["diag"]) and np.array_equal(a["out_tokens"], b["out_tokens"])
+
+
+# ----------------------------------------------------------------------------------------------
+# Cactus
+# ----------------------------------------------------------------------------------------------
+def _kl(a, b):
+    m = a > 0
+    return float(np.sum(a[m] * np.log(a[m] / b[m])))
+
+
+def test_cactus_closed_form_invariants():
+    rng = np.random.default_rng(20)
+    for _ in range(300):
+        V = int(rng.integers(2, 12))
+        pt = special.softmax(rng.normal(0, rng.uniform(0.2, 4), V))
+        n = int(rng.integers(0, V))
+        delta = float(rng.choice([0.0, 1e-3, 0.05, 0.3, 0.75, 1.0, 3.0]))
+        h, gs = oracle.cactus_h(pt, n, delta)
+        assert gs >= pt[n] - 1e-15 and gs <= 1.0
+        assert h[n] == gs
+        assert np.all(h >= 0) and h.sum() == pytest.approx(1.0, abs=1e-12)
+        others = np.arange(V) != n
+        if pt[n] < 1:
+            assert np.allclose(h[others], pt[others] * (1 - gs) / (1 - pt[n]), rtol=1e-13, atol=0)
+        if gs <= 0.5:
+            assert _kl(h, pt) <= delta + 1e-12
+        if delta == 0.0:
+            assert gs == pt[n] and np.array_equal(h, pt)
+
+
+def test_cactus_bonus_largest_at_half():
+    qs = np.linspace(0.01, 0.99, 99)
+    bonus = []
+    for qv in qs:
+        _, gs = oracle.cactus_h(np.array([qv, 1 - qv]), 0, 0.02)
+        bonus.append(gs - qv)
+    assert qs[int(np.argmax(bonus))] == pytest.approx(0.5, abs=0.011)
+
+
+def test_cactus_delta_zero_is_standard_sps():
+    rng = np.random.default_rng(21)
+    B, K, V = 16, 4, 300
+    tgt = rng.normal(0, 3, (B, K + 1, V)).astype(np.float32)
+    drf = (tgt[:, :K] + rng.normal(0, 2, (B, K, V))).astype(np.float32)
+    tok = rng.integers(0, V, (B, K)).astype(np.int32)
+    seeds = np.arange(B, dtype=np.uint64) * 3 + 1
+    a = oracle.verify(tgt, drf, tok, seeds, temperature=0.9)
+    c = oracle.cactus(tgt, drf, tok, seeds, 0.0, temperature=0.9)
+    for k in ("accept_len", "out_tokens", "diag", "accept_margin", "cdf_margin"):
+        assert np.array_equal(a[k], c[k]), k
+    assert np.array_equal(c["gamma_star"], c["diag"][:, :, 0])
+
+
+def test_cactus_raises_acceptance():
+    rng = np.random.default_rng(22)
+    B, K, V = 64, 5, 200
+    tgt = rng.normal(0, 3, (B, K + 1, V)).astype(np.float32)
+    drf = (tgt[:, :K] + rng.normal(0, 2, (B, K, V))).astype(np.float32)
+    tok = np.stack([[rng.choice(V, p=special.softmax(drf[b, j])) for j in range(K)] for b in range(B)]).astype(np.int32)
+    seeds = np.arange(B, dtype=np.uint64)
+    L0 = oracle.cactus(tgt, drf, tok, seeds, 0.0)["accept_len"]
+    L1 = oracle.cactus(tgt, drf, tok, seeds, 1.0)["accept_len"]
+    assert np.all(L1 >= L0)          # same uniforms, gamma* >= p_target(n): acceptance is monotone in delta
+    assert L1.mean() > L0.mean()
+
+
+@pytest.mark.parametrize("delta", [0.0, 0.2, 1.0])
+def test_cactus_exact_law_and_theorem3(delta):
+    rng = np.random.default_rng(30 + int(10 * delta))
+    V = 5
+    pt = special.softmax(rng.normal(0, 1.5, V))
+    pd = special.softmax(np.log(pt) + rng.normal(0, 1.0, V))
+    hs = [oracle.cactus_h(pt, n, delta)[0] for n in range(V)]
+    law = output_law(None, pd, h_of=lambda t: hs[t])
+    # law of the algorithm, stated directly: accept n w.p. min(1, h_n(n)/pd(n)); else (h_n - pd)+ / Z
+    direct = np.zeros(V)
+    for n in range(V):
+        h = hs[n]
+        a = min(1.0, h[n] / pd[n])
+        direct[n] += pd[n] * a
+        res = np.maximum(h - pd, 0.0)
+        if a < 1.0:
+            direct += pd[n] * (1 - a) * res / res.sum()
+    assert law == pytest.approx(direct, abs=2e-6)
+    if delta == 0.0:
+        assert law == pytest.approx(pt, abs=2e-6)
+    else:
+        # Cactus Theorem 3 (translated): D(h_alg || target) <= D(draft || target)
+        assert _kl(law, pt) <= _kl(pd, pt) + 1e-6
+        # every candidate's own acceptance rises: gamma* >= p_target(n)
+        assert law.sum() == pytest.approx(1.0, abs=1e-6)
+
+
+def test_cactus_batched_chi2():
+    rng = np.random.default_rng(40)
+    V, n, delta = 6, 50000, 0.5
+    pt = special.softmax(rng.normal(0, 1.5, V))
+    pd = special.softmax(np.log(pt) + rng.normal(0, 1.2, V))
+    hs = [oracle.cactus_h(pt, k, delta)[0] for k in range(V)]
+    direct = np.zeros(V)
+    for k in range(V):
+        h = hs[k]
+        a = min(1.0, h[k] / pd[k])
+        res = np.maximum(h - pd, 0.0)
+        direct[k] += pd[k] * a
+        if a < 1.0:
+            direct += pd[k] * (1 - a) * res / res.sum()
+    tgt, drf, tok = _batch_same_rows([pt], [pd], pt, n, rng)
+    out = oracle.cactus(tgt, drf, tok, np.arange(n, dtype=np.uint64) + 77, delta)
+    c = np.bincount(out["out_tokens"][:, 0], minlength=V)
+    assert _chi2_p(c, direct) > 1e-6
+    assert _chi2_p(c, pt) < 1e-6        # lossy by design for delta > 0
