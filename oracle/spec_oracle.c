@@ -24,7 +24,8 @@
  * Readings where the pages are silent (each also listed in the design notes):
  *  - accept iff r * p_draft(t) < p_target(t)  (strict, no division; [SpS] §5.1 gives both forms);
  *  - uniforms: Philox4x32-10, counter (pos, seq, stream, 0), key (seed lo, seed hi), word 0 mapped to
- *    ((w >> 8) + 0.5) * 2^-24; stream 0 = accept r, stream 1 = resample / bonus u;
+ *    ((w >> 9) + 0.5) * 2^-23, i.e. an odd multiple of 2^-24 below 1 (exact in fp32 and fp64);
+ *    stream 0 = accept r, stream 1 = resample / bonus u;
  *  - inverse CDF in ascending token id: the smallest x whose running sum exceeds u * (total mass);
  *  - a reject with Z <= 0 (possible only through rounding) resamples from the target row itself;
  *  - bonus token (all K drafts accepted) is drawn from target row K with u = U(seed, b, K, stream 1);
@@ -72,14 +73,14 @@ void spec_oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uin
     out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
 }
 
-/* Uniform on the 2^-24 grid strictly inside (0,1); exact in fp32 and fp64. */
+/* Uniform on the grid (k + 1/2) 2^-23, k in [0, 2^23): strictly inside (0,1), exact in fp32 and fp64. */
 double spec_oracle_uniform(uint64_t seed, uint32_t seq, uint32_t pos, uint32_t stream)
 {
     uint32_t ctr[4] = {pos, seq, stream, 0u};
     uint32_t key[2] = {(uint32_t)(seed & 0xFFFFFFFFu), (uint32_t)(seed >> 32)};
     uint32_t out[4];
     spec_oracle_philox4x32_10(ctr, key, out);
-    return ((double)(out[0] >> 8) + 0.5) * (1.0 / 16777216.0);
+    return ((double)(out[0] >> 9) + 0.5) * (1.0 / 8388608.0);
 }
 
 /* ------------------------------------------------------------------------------------------ */

@@ -8,7 +8,7 @@ Auto-Regressive Decoding with Constrained Acceptance Speculative Sampling" (Key 
 closed-form h, delta = 0 is standard speculative sampling, the KL bound when gamma* <= 0.5, and the
 Theorem 3 bound KL(h_alg || target) <= KL(draft || target)); and the Philox4x32-10 known answers.
 
-Exact laws are obtained by enumerating the oracle's own decisions over the whole 2^-24 grid of
+Exact laws are obtained by enumerating the oracle's own decisions over the whole grid of
 uniforms (bisection on the monotone accept and inverse-CDF decisions), so a wrong sign, index or term
 anywhere in the accept test, the residual or the inverse CDF changes an enumerated probability.
 """
@@ -22,7 +22,7 @@ from scipy import special, stats
 import oracle
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
-GRID = 1 << 24
+GRID = 1 << 23          # the oracle's uniforms are (k + 1/2) / 2^23
 
 
 def _golden_kv(name):
@@ -41,7 +41,7 @@ def _golden_kv(name):
 # enumeration helpers (drive the oracle's decisions; no re-implementation of the rule)
 # ----------------------------------------------------------------------------------------------
 def accept_fraction(h, pd, t):
-    """Fraction of the 2^24 grid uniforms r that the oracle accepts for candidate t."""
+    """Fraction of the grid uniforms r that the oracle accepts for candidate t."""
     lo, hi = 0, GRID
     while lo < hi:
         mid = (lo + hi) // 2
@@ -119,10 +119,11 @@ def test_uniform_grid_and_streams():
     for u in us:
         assert 0.0 < u < 1.0
         k = u * GRID - 0.5
-        assert k == int(k)                      # on the 2^-24 grid
+        assert k == int(k)                      # on the (k + 1/2) 2^-23 grid
+        assert float(np.float32(u)) == u        # exact in fp32
     assert len(set(us)) == len(us)              # counter and key both reach the output
     w0 = oracle.philox4x32_10([3, 2, 1, 0], [7, 0])[0]
-    assert oracle.uniform(7, 2, 3, 1) == ((int(w0) >> 8) + 0.5) / GRID
+    assert oracle.uniform(7, 2, 3, 1) == ((int(w0) >> 9) + 0.5) / GRID
 
 
 def test_uniform_is_uniform():
