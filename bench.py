@@ -1,0 +1,324 @@
+"""Benchmark: verified draft positions per second on GB300.
+
+One step = one spec_verify call (all of the standard path: temperature softmax of both rows, accept test,
+chain length, residual or bonus draw) over one batch of the standard-verification workload at the Llama-3
+vocabulary (B = 64 sequences, K = 5 draft positions, V = 128256, bf16 logits). Steps cycle through a ring of
+distinct input batches whose total size is several times the 129 MB L2, so no step reads the previous
+step's logits from L2.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+Multi-GPU (torchrun): sequences are independent, so every rank verifies its own batches (weak scaling) with
+no collective on the data path; rank 0 reports total positions / max-over-ranks time.
+
+--impl reference times the fp64 CPU oracle (the only other implementation) on the host cores, on a bounded
+sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "verified draft positions/sec"
+UNIT = "positions/s"
+DEFAULT_WORKLOAD = "sps_llama3_b64_k5"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------------------------------------
+# clocks during the timed region (NVML through ctypes: read-only queries)
+# ------------------------------------------------------------------------------------------------
+class ClockSampler:
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown", 0x4: "sw_power_cap",
+               0x80: "hw_power_brake_slowdown", 0x1: "gpu_idle", 0x2: "applications_clocks_setting"}
+
+    def __init__(self, index=0, period_s=0.002):
+        self.samples, self.reasons, self.max_mhz = [], set(), None
+        self.period = period_s
+        self._stop = threading.Event()
+        self._thr = None
+        try:
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            self.nvml.nvmlInit_v2()
+            self.dev = ctypes.c_void_p()
+            self.nvml.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.dev))
+            mx = ctypes.c_uint()
+            if self.nvml.nvmlDeviceGetMaxClockInfo(self.dev, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+        except OSError:
+            self.nvml = None
+
+    def _sample(self):
+        clk = ctypes.c_uint()
+        if self.nvml.nvmlDeviceGetClockInfo(self.dev, 1, ctypes.byref(clk)) == 0:
+            self.samples.append(clk.value)
+        r = ctypes.c_ulonglong()
+        fn = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(self.nvml, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        if fn(self.dev, ctypes.byref(r)) == 0:
+            for bit, name in self.REASONS.items():
+                if r.value & bit and name != "gpu_idle":
+                    self.reasons.add(name)
+
+    def _run(self):
+        while not self._stop.is_set():
+            self._sample()
+            time.sleep(self.period)
+
+    def start(self):
+        if self.nvml:
+            self._sample()
+            self._thr = threading.Thread(target=self._run, daemon=True)
+            self._thr.start()
+
+    def stop(self):
+        if self.nvml:
+            self._stop.set()
+            self._thr.join()
+            self._sample()
+
+    def summary(self):
+        if not self.nvml:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None, "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons), "samples": len(self.samples)}
+
+
+# ------------------------------------------------------------------------------------------------
+# distributed plumbing
+# ------------------------------------------------------------------------------------------------
+def dist_setup(n_gpus):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+        pg = dist
+    return rank, world, local, pg
+
+
+def barrier(pg, torch):
+    if pg is not None:
+        pg.barrier()
+    if torch.cuda.is_available():
+        torch.cuda.synchronize()
+
+
+def max_over_ranks(pg, torch, v, device):
+    if pg is None:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU oracle timing (reference arm and cpu_baseline)
+# ------------------------------------------------------------------------------------------------
+def time_oracle(w, inp_host, n_seq, repeats=1):
+    import oracle
+    sel = np.arange(n_seq)
+    t = workloads.to_numpy_logits(inp_host["target"][:n_seq])
+    d = workloads.to_numpy_logits(inp_host["draft"][:n_seq])
+    tok = inp_host["tokens"][:n_seq].numpy()
+    seeds = inp_host["seeds"][:n_seq].numpy().astype(np.uint64)
+    oracle.build()
+    cores = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    for _ in range(repeats):
+        oracle.verify(t, d, tok, seeds, w.temperature, seq_index=sel, nthreads=cores)
+    dt = (time.perf_counter() - t0) / repeats
+    return n_seq * w.K / dt, dt, cores
+
+
+def run_reference(args, w):
+    import torch
+    rank, world, local, pg = dist_setup(args.gpus)
+    if rank != 0:
+        return 0
+    n_seq = min(w.B, args.ref_sequences)
+    inp = workloads.make(w.scaled(B=n_seq), device="cpu")
+    for _ in range(args.warmup):
+        time_oracle(w, inp, min(n_seq, 2))
+    t0 = time.perf_counter()
+    times = []
+    for _ in range(args.steps):
+        _, dt, cores = time_oracle(w, inp, n_seq)
+        times.append(dt)
+    total = time.perf_counter() - t0
+    value = n_seq * w.K * args.steps / total
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "K": w.K, "V": w.V, "sample_sequences": n_seq},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": "%d of %d sequences of one batch per step" % (n_seq, w.B)},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    del torch
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------------------------------------
+# GPU arm
+# ------------------------------------------------------------------------------------------------
+def run_ours(args, w):
+    import torch
+    import speculative_decoding_verification_target_gb300 as sv
+
+    rank, world, local, pg = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    sv.load()
+    batch_bytes = w.algorithmic_bytes()
+    ring = max(2, -(-4 * L2_BYTES // batch_bytes))        # >= 4x L2 in flight across the ring
+    ring = min(ring, args.max_ring)
+    batches = [workloads.make(w.scaled(gen_seed=w.gen_seed + 101 * i + 7919 * rank), device=dev)
+               for i in range(ring)]
+    ws = sv.new_workspace(w.B, w.K, w.V, 1, dev)
+    acc = torch.empty(w.B, dtype=torch.int32, device=dev)
+    outt = torch.empty((w.B, w.K + 1), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        bt = batches[i % ring]
+        sv.verify(bt["target"], bt["draft"], bt["tokens"], bt["seeds"], w.temperature, accept_len=acc,
+                  out_tokens=outt, want_diag=False, workspace=ws, stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    barrier(pg, torch)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step(i)
+        ev[i][1].record(stream)
+    stop.record(stream)
+    barrier(pg, torch)
+    clocks.stop()
+    elapsed_ms = start.elapsed_time(stop)
+    call_ms = [a.elapsed_time(b) for a, b in ev]
+    elapsed_ms = max_over_ranks(pg, torch, elapsed_ms, dev)
+    status = sv.read_status(ws)
+
+    # end to end through the public call: pinned host inputs -> device, verify, results -> host
+    hb = batches[0]
+    host_in = {k: hb[k].to("cpu").pin_memory() for k in ("target", "draft", "tokens", "seeds")}
+    dev_in = {k: torch.empty_like(hb[k]) for k in host_in}
+    host_out = {"accept_len": torch.empty(w.B, dtype=torch.int32).pin_memory(),
+                "out_tokens": torch.empty((w.B, w.K + 1), dtype=torch.int32).pin_memory()}
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+
+    def e2e_step():
+        for k in host_in:
+            dev_in[k].copy_(host_in[k], non_blocking=True)
+        sv.verify(dev_in["target"], dev_in["draft"], dev_in["tokens"], dev_in["seeds"], w.temperature,
+                  accept_len=acc, out_tokens=outt, want_diag=False, workspace=ws, stream=stream)
+        host_out["accept_len"].copy_(acc, non_blocking=True)
+        host_out["out_tokens"].copy_(outt, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        e2e_step()
+    barrier(pg, torch)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier(pg, torch)
+    e2e_ms = max_over_ranks(pg, torch, e0.elapsed_time(e1), dev)
+
+    if rank != 0:
+        return 0
+    positions = w.positions * world
+    value = positions * args.steps / (elapsed_ms / 1e3)
+    e2e_value = positions * e2e_steps / (e2e_ms / 1e3)
+    peak, peak_kind = peaks()
+    avg_call_s = statistics.mean(call_ms) / 1e3
+    achieved = batch_bytes / avg_call_s / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "fp32", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "K": w.K, "V": w.V, "N": w.N, "temperature": w.temperature,
+                   "positions_per_step_per_gpu": w.positions, "bytes_per_step_per_gpu": batch_bytes,
+                   "l2": "inputs larger than L2: ring of %d distinct batches (%.0f MB) > 129 MB L2" % (
+                       ring, ring * batch_bytes / 1e6),
+                   "parallelism": "replicas over sequences" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "peak_kind": peak_kind,
+                     "kernel": "rows_kernel + chain finish (one verify call, CUDA events on its stream)",
+                     "avg_call_us": avg_call_s * 1e6, "min_call_us": min(call_ms) * 1e3,
+                     "frac_of_8tbs_nominal": achieved / 8000.0},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms / e2e_steps},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks.summary(),
+        "device_status": status,
+    }
+    if not args.no_cpu_baseline:
+        host = {k: batches[0][k].to("cpu") for k in ("target", "draft", "tokens", "seeds")}
+        n_seq = min(w.B, args.cpu_sequences)
+        pos_s, dt, cores = time_oracle(w, host, n_seq)
+        line["cpu_baseline"] = {"value": pos_s, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": "%d of %d sequences of one %s batch (%.1f s)" % (n_seq, w.B, w.name, dt)}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--max-ring", type=int, default=8)
+    ap.add_argument("--cpu-sequences", type=int, default=64)
+    ap.add_argument("--ref-sequences", type=int, default=16)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    w = workloads.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,134 @@
+/*
+ * specverify.h -- C ABI of the GB300 (sm_103a) speculative-sampling verification library.
+ *
+ * Batched verification of draft tokens against full-vocabulary target and draft logits:
+ *  - temperature softmax of both rows, with one temperature for both ("standardized sampling",
+ *    lossless-proof tutorial "Speculative Decoding 为什么是 Lossless 的 — 详细证明教程", §8 Q4);
+ *  - the accept test r < min(1, p_target(t) / p_draft(t)), evaluated as r * p_draft(t) < p_target(t)
+ *    (same tutorial, §5.1 SpecSampleOne);
+ *  - on the first reject, one draw from the residual (p_target - p_draft)+ / Z, Z = sum (p_target - p_draft)+
+ *    (§5.1, §6.4); the drafts after it are dropped; if every draft is accepted, one bonus draw from the
+ *    target row K+1 (§9.1, the gamma-step chain);
+ *  - HedgeSpec counterfactual acceptance gamma[i,b,j] = 1 - TV(p_target, q_i) = sum_x min(p_target, q_i)
+ *    for every drafter i ("Not-a-Bandit: Provably No-Regret Drafter Selection in Speculative Decoding for
+ *    LLMs", Key design 1) and its loss 1 - gamma (Key design 3);
+ *  - Cactus constrained acceptance ("Cactus: Accelerating Auto-Regressive Decoding with Constrained
+ *    Acceptance Speculative Sampling", Key design 2-3): gamma* = min(q(n) + sqrt(2 delta q(n)(1 - q(n))), 1)
+ *    with q(n) the TARGET probability of the draft token n (that page calls the target q and the draft p),
+ *    target h_n = gamma*, h_i = (1 - gamma*) / (1 - q(n)) * p_target(i), accept iff r * p_draft(n) < gamma*,
+ *    residual (h - p_draft)+ / sum (h - p_draft)+.
+ *
+ * Conventions for every call:
+ *  - Tensor pointers are DEVICE memory owned by the caller, contiguous, row-major. Logits are bf16 or fp32
+ *    (spec_dtype). The library allocates nothing; it reads the logits once and writes only the outputs and
+ *    the caller's workspace.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream). Calls are asynchronous:
+ *    they enqueue kernels and return without synchronising.
+ *  - Uniforms: Philox4x32-10 (Salmon et al., SC'11) with key = seeds[b] (low word, high word) and counter
+ *    (position j, sequence b, stream, 0); output word 0 maps to ((w >> 8) + 0.5) * 2^-24. Stream 0 gives
+ *    the accept uniform r of position j; stream 1 gives the resample uniform u of position j (or of the
+ *    bonus row at j = K).
+ *  - Inverse CDF in ascending token id: the emitted token is the smallest x whose running mass exceeds
+ *    u * (total mass). A token with zero mass is never emitted.
+ *  - Arguments are validated on the host before anything is launched; a bad argument returns
+ *    SPEC_ERR_INVALID (message in spec_last_error()) and enqueues nothing. A CUDA launch failure returns
+ *    SPEC_ERR_CUDA. Draft tokens live on the device and are checked there: a token outside [0, V) sets
+ *    bit SPEC_STATUS_BAD_TOKEN of the workspace status word (read with spec_read_status) and that position
+ *    is verified as if the draft had proposed a token of probability 0 under both models.
+ *  - Every row must hold at least one finite logit; -inf logits are allowed (probability 0). NaN or +inf
+ *    logits give unspecified results.
+ *  - Limits: 1 <= K <= 64, 1 <= V <= 262144, 1 <= N <= 64, temperature > 0 and finite (temperature 0,
+ *    greedy decoding, returns SPEC_ERR_UNSUPPORTED), delta >= 0 and finite. B = 0 is a no-op.
+ *  - Workspace: caller-provided device memory of at least spec_workspace_size(B, K, V, N) bytes, 16-byte
+ *    aligned. Its first word is the status word: zero it once before first use (spec_clear_status or a
+ *    memset); calls only OR bits into it. The rest is scratch for per-position records and holds nothing
+ *    a later call depends on. Calls that share a workspace must not overlap on the GPU.
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SPEC_OK = 0,
+    SPEC_ERR_INVALID = 1,
+    SPEC_ERR_CUDA = 2,
+    SPEC_ERR_UNSUPPORTED = 3
+} spec_status;
+
+typedef enum { SPEC_BF16 = 0, SPEC_FP32 = 1 } spec_dtype;
+
+/* Bits of the device status word. */
+#define SPEC_STATUS_BAD_TOKEN 1u /* a draft token was outside [0, V) */
+#define SPEC_STATUS_TIMEOUT 2u   /* a bounded wait for a bulk copy gave up (results invalid) */
+
+/* Bytes of workspace the three calls need for these sizes (a pure function of the sizes; the same
+ * buffer serves any call whose sizes are not larger). */
+size_t spec_workspace_size(int B, int K, int V, int N);
+
+/* Standard speculative sampling (tutorial §5.1 + §9.1).
+ *  target_logits [B, K+1, V]  row K of each sequence is the bonus row
+ *  draft_logits  [B, K, V]
+ *  draft_tokens  int32 [B, K], the draft's proposals
+ *  seeds         uint64 [B], Philox keys
+ *  temperature   applied to both rows
+ * Outputs (device):
+ *  accept_len    int32 [B], number of accepted drafts L in [0, K]
+ *  out_tokens    int32 [B, K+1]: the L accepted drafts, then the residual draw (L < K) or the bonus draw
+ *                (L = K), then -1 padding
+ *  diag          nullable float [B, K, 4]: per position (p_target(t), p_draft(t), Z, r) for every j, also
+ *                after the chain stopped */
+spec_status spec_verify(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                        const int32_t* draft_tokens, const uint64_t* seeds, int B, int K, int V,
+                        float temperature, int32_t* accept_len, int32_t* out_tokens, float* diag,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* HedgeSpec counterfactual evaluation ("Not-a-Bandit ...", Key design 1 and 3).
+ *  target_logits  [B, K+1, V]  (row K is read only when selected >= 0)
+ *  drafter_logits [N, B, K, V]
+ * Outputs: gamma float [N, B, K] = sum_x min(p_target, q_i) at every level j (all K levels; the caller
+ * applies censoring with accept_len), loss nullable float [N, B, K] = 1 - gamma.
+ * selected = -1: gamma only (draft_tokens, seeds, accept_len, out_tokens, diag may be NULL).
+ * selected in [0, N): in the same pass, the chain of drafter `selected` is verified exactly as spec_verify
+ * would with draft_logits = drafter_logits[selected]. */
+spec_status spec_counterfactual_gamma(const void* target_logits, const void* drafter_logits,
+                                      spec_dtype dtype, int N, int B, int K, int V, float temperature,
+                                      float* gamma, float* loss, int selected,
+                                      const int32_t* draft_tokens, const uint64_t* seeds,
+                                      int32_t* accept_len, int32_t* out_tokens, float* diag,
+                                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* Cactus constrained acceptance ("Cactus ...", Key design 1-3). Same layout and outputs as spec_verify,
+ * plus delta >= 0 (the divergence budget) and gamma_star nullable float [B, K]. diag's first entry is
+ * h(t) = gamma*. The bonus row is the plain target row. delta = 0 gives outputs bit-identical to
+ * spec_verify. */
+spec_status spec_cactus_verify(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                               const int32_t* draft_tokens, const uint64_t* seeds, int B, int K, int V,
+                               float temperature, float delta, int32_t* accept_len, int32_t* out_tokens,
+                               float* diag, float* gamma_star, void* workspace, size_t workspace_bytes,
+                               void* stream);
+
+/* Copies the workspace status word to *status_out (host), synchronising `stream`. */
+spec_status spec_read_status(const void* workspace, uint32_t* status_out, void* stream);
+
+/* Zeroes the workspace status word (asynchronous on `stream`). */
+spec_status spec_clear_status(void* workspace, void* stream);
+
+/* Thread-local message describing the last non-OK status returned on this thread. */
+const char* spec_last_error(void);
+
+/* Tuning and test hook: forces the number of CTAs that split one vocabulary row (1, 2, 4, 8 or 16; 0
+ * restores the automatic choice). Process-wide, not thread-safe; results do not depend on it beyond
+ * floating-point summation order. Returns 0, or -1 for an unsupported value. */
+int spec_debug_set_cluster_size(int C);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_H */

@@ -1,0 +1,452 @@
+// Host side of the C ABI declared in include/specverify.h: argument validation, launch planning
+// (cluster size, vocabulary slice, shared-memory slots, persistent grid size) and the launches.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "specverify.h"
+#include "specverify_kernels.cuh"
+
+namespace specv {
+namespace {
+
+thread_local char g_err[512] = "";
+
+spec_status fail(spec_status s, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+constexpr int MAX_K = 64;
+constexpr int MAX_V = 262144;
+constexpr int MAX_N = 64;
+constexpr size_t WS_HEADER = 256;          // status word + padding
+constexpr int SMEM_PER_SM = 233472;        // GB300: 228 KiB per SM
+constexpr int SMEM_RESERVED_PER_CTA = 1024;
+constexpr int SMEM_MAX_PER_CTA = 232448;   // opt-in maximum per CTA
+
+int g_cluster_override = 0;   // test / tuning hook (0 = automatic)
+
+struct Plan {
+    int C = 1, slice_elems = 0, P = 1, ts = 1, r = 1, slot_bytes = 0, tiles_cap = 0;
+    size_t smem = 0;
+    int tma = 0;
+};
+
+size_t fixed_smem(int C, int tiles_cap) {
+    return MAX_SLOTS * 8 + static_cast<size_t>(2 * C * 8) * 4 + static_cast<size_t>(tiles_cap) * 4 + NWARPS * 4 * 4 +
+           8 * 4 + 8 * 4;
+}
+
+int passes_for(int slice_elems) {
+    const int chunks = (slice_elems + CHUNK - 1) / CHUNK;
+    const int need = (chunks + NT - 1) / NT;
+    static const int supported[] = {1, 2, 4, 5, 8};
+    for (int p : supported)
+        if (p >= need) return p;
+    return -1;
+}
+
+// Chooses the cluster size C (vocabulary split), the per-CTA slice, the register passes P and the number
+// of shared-memory row slots. Two CTAs per SM are preferred (one computes while the other's copies
+// land); the slot counts shrink until that fits.
+bool make_plan(int V, int elem_bytes, int n_other, bool aligned, Plan& pl) {
+    const int q_tiles = (V + SLICE_Q - 1) / SLICE_Q;
+    int cands[5] = {1, 2, 4, 8, 16};
+    int start = 0;
+    if (g_cluster_override > 0) {
+        cands[0] = g_cluster_override;
+        start = 0;
+    }
+    const int ncand = g_cluster_override > 0 ? 1 : 5;
+    for (int ci = start; ci < ncand; ++ci) {
+        const int C = cands[ci];
+        // small vocabularies stay in one CTA; large ones use a cluster of 8 (16 only if 8 cannot hold)
+        if (g_cluster_override == 0) {
+            if (V > 8192 && C < 8) continue;
+        }
+        Plan p;
+        p.C = C;
+        p.slice_elems = (q_tiles + C - 1) / C * SLICE_Q;
+        p.P = passes_for(p.slice_elems);
+        if (p.P < 0) continue;
+        p.slot_bytes = p.slice_elems * elem_bytes;
+        const int ntiles = (p.slice_elems + TILE - 1) / TILE;
+        p.tiles_cap = (ntiles + 3) / 4 * 4;
+        const size_t fixed = fixed_smem(C, p.tiles_cap);
+        const size_t two_per_sm = SMEM_PER_SM / 2 - SMEM_RESERVED_PER_CTA;
+        // preferences: (ts, r)
+        const int pref_verify[][2] = {{2, 1}, {1, 1}};
+        const int pref_many[][2] = {{1, 2}, {1, 1}};
+        const auto& pref = n_other >= 2 ? pref_many : pref_verify;
+        bool ok = false;
+        for (const auto& tr : pref) {
+            const size_t need = static_cast<size_t>(tr[0] + tr[1]) * p.slot_bytes + fixed;
+            if (need <= two_per_sm) {
+                p.ts = tr[0];
+                p.r = tr[1];
+                p.smem = need;
+                ok = true;
+                break;
+            }
+        }
+        if (!ok) {
+            // one CTA per SM: more slots
+            const int pref_one[][2] = {{2, 2}, {1, 2}, {1, 1}};
+            for (const auto& tr : pref_one) {
+                const size_t need = static_cast<size_t>(tr[0] + tr[1]) * p.slot_bytes + fixed;
+                if (need <= static_cast<size_t>(SMEM_MAX_PER_CTA)) {
+                    p.ts = tr[0];
+                    p.r = tr[1];
+                    p.smem = need;
+                    ok = true;
+                    break;
+                }
+            }
+        }
+        if (!ok) continue;
+        p.tma = aligned ? 1 : 0;
+        pl = p;
+        return true;
+    }
+    return false;
+}
+
+using KernelFn = void (*)(const KParams);
+
+template <class E>
+KernelFn pick_kernel(int P) {
+    switch (P) {
+        case 1: return rows_kernel<E, 1>;
+        case 2: return rows_kernel<E, 2>;
+        case 4: return rows_kernel<E, 4>;
+        case 5: return rows_kernel<E, 5>;
+        case 8: return rows_kernel<E, 8>;
+        default: return nullptr;
+    }
+}
+
+struct OccKey {
+    KernelFn fn;
+    int C;
+    size_t smem;
+    int device;
+};
+std::mutex g_occ_mu;
+OccKey g_occ_keys[64];
+int g_occ_vals[64];
+int g_occ_n = 0;
+
+cudaError_t max_clusters(KernelFn fn, int C, size_t smem, int& out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    {
+        std::lock_guard<std::mutex> lk(g_occ_mu);
+        for (int i = 0; i < g_occ_n; ++i)
+            if (g_occ_keys[i].fn == fn && g_occ_keys[i].C == C && g_occ_keys[i].smem == smem &&
+                g_occ_keys[i].device == dev) {
+                out = g_occ_vals[i];
+                return cudaSuccess;
+            }
+    }
+    // The attribute is a per-function ceiling shared by every plan: always the opt-in maximum, so that a
+    // later plan with less shared memory never lowers it under an earlier, cached one.
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX_PER_CTA);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    cfg.gridDim = dim3(static_cast<unsigned>(C), 1, 1);
+    cfg.blockDim = dim3(NT, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = static_cast<unsigned>(C);
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n < 1) return cudaErrorInvalidConfiguration;
+    std::lock_guard<std::mutex> lk(g_occ_mu);
+    if (g_occ_n < 64) {
+        g_occ_keys[g_occ_n] = {fn, C, smem, dev};
+        g_occ_vals[g_occ_n] = n;
+        ++g_occ_n;
+    }
+    out = n;
+    return cudaSuccess;
+}
+
+struct Call {
+    const void* target;
+    const void* others;
+    spec_dtype dtype;
+    const int32_t* tokens;
+    const uint64_t* seeds;
+    int B, K, V, N, selected;
+    float temperature, delta;
+    int cactus;
+    float* gamma;
+    float* loss;
+    int32_t* accept_len;
+    int32_t* out_tokens;
+    float* diag;
+    float* gamma_star;
+    void* workspace;
+    size_t workspace_bytes;
+    cudaStream_t stream;
+};
+
+spec_status run(const Call& a) {
+    if (a.B == 0) return SPEC_OK;
+    const int eb = a.dtype == SPEC_BF16 ? 2 : 4;
+    const bool chain = a.selected >= 0;
+    const uintptr_t align_mask = 15;
+    const bool aligned = ((reinterpret_cast<uintptr_t>(a.target) | reinterpret_cast<uintptr_t>(a.others)) & align_mask) == 0 &&
+                         (static_cast<size_t>(a.V) * eb) % 16 == 0;
+    Plan pl;
+    if (!make_plan(a.V, eb, a.N, aligned, pl))
+        return fail(SPEC_ERR_UNSUPPORTED, "no launch plan fits V=%d (cluster override %d)", a.V, g_cluster_override);
+    KernelFn fn = a.dtype == SPEC_BF16 ? pick_kernel<Bf16>(pl.P) : pick_kernel<F32>(pl.P);
+    if (!fn) return fail(SPEC_ERR_UNSUPPORTED, "no kernel for %d passes", pl.P);
+    int ncl = 0;
+    cudaError_t e = max_clusters(fn, pl.C, pl.smem, ncl);
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "occupancy query failed: %s", cudaGetErrorString(e));
+
+    KParams k = {};
+    k.target = static_cast<const unsigned char*>(a.target);
+    k.others = static_cast<const unsigned char*>(a.others);
+    k.tokens = chain ? a.tokens : nullptr;
+    k.seeds = chain ? a.seeds : nullptr;
+    k.B = a.B;
+    k.K = a.K;
+    k.V = a.V;
+    k.N = a.N;
+    k.selected = a.selected;
+    k.J = chain ? a.K + 1 : a.K;
+    k.num_items = a.B * k.J;
+    k.c = static_cast<float>(1.4426950408889634 / static_cast<double>(a.temperature));
+    k.delta = a.delta;
+    k.cactus = a.cactus;
+    k.slice_elems = pl.slice_elems;
+    k.tma = pl.tma;
+    k.ts = pl.ts;
+    k.r = pl.r;
+    k.slot_bytes = pl.slot_bytes;
+    k.tiles_cap = pl.tiles_cap;
+    k.gamma = a.gamma;
+    k.loss = a.loss;
+    unsigned char* ws = static_cast<unsigned char*>(a.workspace);
+    k.status = reinterpret_cast<unsigned*>(ws);
+    k.rec = chain ? reinterpret_cast<float*>(ws + WS_HEADER) : nullptr;
+
+    const int grid_clusters = ncl < k.num_items ? ncl : k.num_items;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    cfg.gridDim = dim3(static_cast<unsigned>(grid_clusters * pl.C), 1, 1);
+    cfg.blockDim = dim3(NT, 1, 1);
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = a.stream;
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = static_cast<unsigned>(pl.C);
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, fn, k);
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "verification kernel launch failed: %s", cudaGetErrorString(e));
+
+    if (chain) {
+        FParams f = {};
+        f.rec = k.rec;
+        f.tokens = a.tokens;
+        f.seeds = a.seeds;
+        f.B = a.B;
+        f.K = a.K;
+        f.accept_len = a.accept_len;
+        f.out_tokens = a.out_tokens;
+        f.diag = a.diag;
+        f.gamma_star = a.gamma_star;
+        cudaLaunchConfig_t fc = {};
+        cudaLaunchAttribute fa[1];
+        const int per_block = 8;   // sequences (warps) per block
+        fc.gridDim = dim3(static_cast<unsigned>((a.B + per_block - 1) / per_block), 1, 1);
+        fc.blockDim = dim3(per_block * 32, 1, 1);
+        fc.dynamicSmemBytes = 0;
+        fc.stream = a.stream;
+        fa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        fa[0].val.programmaticStreamSerializationAllowed = 1;
+        fc.attrs = fa;
+        fc.numAttrs = 1;
+        e = cudaLaunchKernelEx(&fc, finish_kernel, f);
+        if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "chain kernel launch failed: %s", cudaGetErrorString(e));
+    }
+    return SPEC_OK;
+}
+
+spec_status check_common(const void* target, const void* others, spec_dtype dtype, int B, int K, int V, int N,
+                         float temperature, void* workspace, size_t workspace_bytes) {
+    if (dtype != SPEC_BF16 && dtype != SPEC_FP32) return fail(SPEC_ERR_INVALID, "unknown dtype %d", static_cast<int>(dtype));
+    if (B < 0) return fail(SPEC_ERR_INVALID, "B must be >= 0 (got %d)", B);
+    if (K < 1 || K > MAX_K) return fail(SPEC_ERR_INVALID, "K must be in [1, %d] (got %d)", MAX_K, K);
+    if (V < 1 || V > MAX_V) return fail(SPEC_ERR_INVALID, "V must be in [1, %d] (got %d)", MAX_V, V);
+    if (N < 1 || N > MAX_N) return fail(SPEC_ERR_INVALID, "N must be in [1, %d] (got %d)", MAX_N, N);
+    if (std::isnan(temperature) || std::isinf(temperature) || temperature < 0.f)
+        return fail(SPEC_ERR_INVALID, "temperature must be finite and > 0 (got %g)", static_cast<double>(temperature));
+    if (temperature == 0.f) return fail(SPEC_ERR_UNSUPPORTED, "temperature 0 (greedy) is not supported");
+    if (B == 0) return SPEC_OK;
+    if (!target || !others) return fail(SPEC_ERR_INVALID, "logits pointers must not be NULL");
+    if (!workspace) return fail(SPEC_ERR_INVALID, "workspace must not be NULL");
+    if (reinterpret_cast<uintptr_t>(workspace) % 16) return fail(SPEC_ERR_INVALID, "workspace must be 16-byte aligned");
+    const size_t need = spec_workspace_size(B, K, V, N);
+    if (workspace_bytes < need)
+        return fail(SPEC_ERR_INVALID, "workspace too small: %zu bytes, need %zu", workspace_bytes, need);
+    return SPEC_OK;
+}
+
+}  // namespace
+}  // namespace specv
+
+using namespace specv;
+
+extern "C" {
+
+size_t spec_workspace_size(int B, int K, int V, int N) {
+    (void)V;
+    (void)N;
+    if (B < 0 || K < 0) return 0;
+    return WS_HEADER + static_cast<size_t>(B) * static_cast<size_t>(K + 1) * REC * sizeof(float);
+}
+
+spec_status spec_verify(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                        const int32_t* draft_tokens, const uint64_t* seeds, int B, int K, int V,
+                        float temperature, int32_t* accept_len, int32_t* out_tokens, float* diag,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+    spec_status s = check_common(target_logits, draft_logits, dtype, B, K, V, 1, temperature, workspace, workspace_bytes);
+    if (s != SPEC_OK || B == 0) return s;
+    if (!draft_tokens || !seeds || !accept_len || !out_tokens)
+        return fail(SPEC_ERR_INVALID, "draft_tokens, seeds, accept_len and out_tokens must not be NULL");
+    Call a = {};
+    a.target = target_logits;
+    a.others = draft_logits;
+    a.dtype = dtype;
+    a.tokens = draft_tokens;
+    a.seeds = seeds;
+    a.B = B;
+    a.K = K;
+    a.V = V;
+    a.N = 1;
+    a.selected = 0;
+    a.temperature = temperature;
+    a.accept_len = accept_len;
+    a.out_tokens = out_tokens;
+    a.diag = diag;
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+    a.stream = static_cast<cudaStream_t>(stream);
+    return run(a);
+}
+
+spec_status spec_counterfactual_gamma(const void* target_logits, const void* drafter_logits, spec_dtype dtype,
+                                      int N, int B, int K, int V, float temperature, float* gamma, float* loss,
+                                      int selected, const int32_t* draft_tokens, const uint64_t* seeds,
+                                      int32_t* accept_len, int32_t* out_tokens, float* diag, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+    spec_status s = check_common(target_logits, drafter_logits, dtype, B, K, V, N, temperature, workspace, workspace_bytes);
+    if (s != SPEC_OK || B == 0) return s;
+    if (!gamma) return fail(SPEC_ERR_INVALID, "gamma must not be NULL");
+    if (selected < -1 || selected >= N) return fail(SPEC_ERR_INVALID, "selected must be -1 or in [0, N) (got %d)", selected);
+    if (selected >= 0 && (!draft_tokens || !seeds || !accept_len || !out_tokens))
+        return fail(SPEC_ERR_INVALID, "with selected >= 0, draft_tokens, seeds, accept_len and out_tokens must not be NULL");
+    Call a = {};
+    a.target = target_logits;
+    a.others = drafter_logits;
+    a.dtype = dtype;
+    a.tokens = draft_tokens;
+    a.seeds = seeds;
+    a.B = B;
+    a.K = K;
+    a.V = V;
+    a.N = N;
+    a.selected = selected;
+    a.temperature = temperature;
+    a.gamma = gamma;
+    a.loss = loss;
+    a.accept_len = accept_len;
+    a.out_tokens = out_tokens;
+    a.diag = diag;
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+    a.stream = static_cast<cudaStream_t>(stream);
+    return run(a);
+}
+
+spec_status spec_cactus_verify(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                               const int32_t* draft_tokens, const uint64_t* seeds, int B, int K, int V,
+                               float temperature, float delta, int32_t* accept_len, int32_t* out_tokens, float* diag,
+                               float* gamma_star, void* workspace, size_t workspace_bytes, void* stream) {
+    spec_status s = check_common(target_logits, draft_logits, dtype, B, K, V, 1, temperature, workspace, workspace_bytes);
+    if (s != SPEC_OK) return s;
+    if (std::isnan(delta) || std::isinf(delta) || delta < 0.f)
+        return fail(SPEC_ERR_INVALID, "delta must be finite and >= 0 (got %g)", static_cast<double>(delta));
+    if (B == 0) return SPEC_OK;
+    if (!draft_tokens || !seeds || !accept_len || !out_tokens)
+        return fail(SPEC_ERR_INVALID, "draft_tokens, seeds, accept_len and out_tokens must not be NULL");
+    Call a = {};
+    a.target = target_logits;
+    a.others = draft_logits;
+    a.dtype = dtype;
+    a.tokens = draft_tokens;
+    a.seeds = seeds;
+    a.B = B;
+    a.K = K;
+    a.V = V;
+    a.N = 1;
+    a.selected = 0;
+    a.temperature = temperature;
+    a.delta = delta;
+    a.cactus = 1;
+    a.accept_len = accept_len;
+    a.out_tokens = out_tokens;
+    a.diag = diag;
+    a.gamma_star = gamma_star;
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+    a.stream = static_cast<cudaStream_t>(stream);
+    return run(a);
+}
+
+spec_status spec_read_status(const void* workspace, uint32_t* status_out, void* stream) {
+    if (!workspace || !status_out) return fail(SPEC_ERR_INVALID, "workspace and status_out must not be NULL");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(status_out, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "status read failed: %s", cudaGetErrorString(e));
+    return SPEC_OK;
+}
+
+spec_status spec_clear_status(void* workspace, void* stream) {
+    if (!workspace) return fail(SPEC_ERR_INVALID, "workspace must not be NULL");
+    cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "status clear failed: %s", cudaGetErrorString(e));
+    return SPEC_OK;
+}
+
+const char* spec_last_error(void) { return g_err; }
+
+int spec_debug_set_cluster_size(int C) {
+    if (C != 0 && C != 1 && C != 2 && C != 4 && C != 8 && C != 16) return -1;
+    g_cluster_override = C;
+    return 0;
+}
+
+}  // extern "C"

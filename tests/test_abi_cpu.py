@@ -1,0 +1,94 @@
+"""CPU checks of the C ABI: the library builds for sm_103a, loads without a GPU, exports every function
+declared in include/specverify.h, and rejects bad arguments on the host before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "specverify.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_decoding_verification_target_gb300 import _build
+    _build.build()
+    import speculative_decoding_verification_target_gb300 as sv
+    return sv.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(spec_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_three_calls():
+    names = declared_functions()
+    for n in ("spec_verify", "spec_counterfactual_gamma", "spec_cactus_verify", "spec_workspace_size",
+              "spec_last_error"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    import speculative_decoding_verification_target_gb300 as sv
+    names = declared_functions()
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(sv.EXPORTS) == set(names)
+
+
+def test_workspace_size(lib):
+    import speculative_decoding_verification_target_gb300 as sv
+    assert sv.workspace_size(64, 5, 128256, 1) == 256 + 64 * 6 * 32
+    assert sv.workspace_size(0, 5, 1000, 1) == 256
+
+
+def _call_verify(lib, **kw):
+    a = dict(target=1 << 20, draft=1 << 21, dtype=0, tokens=1 << 22, seeds=1 << 23, B=2, K=3, V=1000, T=1.0,
+             acc=1 << 24, out=1 << 25, diag=None, ws=1 << 26, wsb=1 << 20, stream=None)
+    a.update(kw)
+    P = ctypes.c_void_p
+    return lib.spec_verify(P(a["target"]), P(a["draft"]), a["dtype"], P(a["tokens"]), P(a["seeds"]), a["B"],
+                           a["K"], a["V"], ctypes.c_float(a["T"]), P(a["acc"]), P(a["out"]),
+                           P(a["diag"]) if a["diag"] else None, P(a["ws"]), a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(K=0), 1), (dict(K=65), 1), (dict(V=0), 1), (dict(V=262145), 1), (dict(B=-1), 1), (dict(T=0.0), 3),
+    (dict(T=-1.0), 1), (dict(T=float("inf")), 1), (dict(T=float("nan")), 1), (dict(dtype=7), 1),
+    (dict(target=0), 1), (dict(tokens=0), 1), (dict(ws=0), 1), (dict(ws=(1 << 26) + 4), 1), (dict(wsb=16), 1),
+])
+def test_host_validation(lib, kw, code):
+    assert _call_verify(lib, **kw) == code
+    assert lib.spec_last_error()
+
+
+def test_B_zero_returns_ok_without_gpu(lib):
+    assert _call_verify(lib, B=0, target=0, draft=0, tokens=0, seeds=0, acc=0, out=0, ws=0) == 0
+
+
+def test_counterfactual_and_cactus_validation(lib):
+    P = ctypes.c_void_p
+    f = ctypes.c_float
+    good = P(1 << 20)
+    # selected out of range
+    rc = lib.spec_counterfactual_gamma(good, good, 0, 3, 2, 2, 100, f(1.0), good, None, 3, good, good, good, good,
+                                       None, P(1 << 26), 1 << 20, None)
+    assert rc == 1
+    rc = lib.spec_counterfactual_gamma(good, good, 0, 0, 2, 2, 100, f(1.0), good, None, -1, None, None, None, None,
+                                       None, P(1 << 26), 1 << 20, None)
+    assert rc == 1   # N = 0
+    rc = lib.spec_cactus_verify(good, good, 0, good, good, 2, 2, 100, f(1.0), f(-0.5), good, good, None, None,
+                                P(1 << 26), 1 << 20, None)
+    assert rc == 1
+    rc = lib.spec_cactus_verify(good, good, 0, good, good, 2, 2, 100, f(1.0), f(float("nan")), good, good, None,
+                                None, P(1 << 26), 1 << 20, None)
+    assert rc == 1
+
+
+def test_cluster_override_hook(lib):
+    assert lib.spec_debug_set_cluster_size(3) == -1
+    assert lib.spec_debug_set_cluster_size(8) == 0
+    assert lib.spec_debug_set_cluster_size(0) == 0

@@ -1,0 +1,332 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the same seeded inputs.
+
+Small cases span several 256-token tiles, several CTAs of a cluster (forced cluster sizes), a ragged last
+slice, unaligned rows (V odd: element-wise staging instead of bulk copies) and fp32 logits; the five named
+workloads run at full size (the largest checked on a stated sample of sequences through seq_index).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from parity_util import (PROB_TOL, assert_chain, assert_diag, host, oracle_verify, to_device)
+
+pytestmark = pytest.mark.gpu
+
+sv = pytest.importorskip("speculative_decoding_verification_target_gb300")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    sv.load(build_if_missing=True)
+    yield
+    sv.set_cluster_size(0)
+
+
+@pytest.fixture(autouse=True)
+def _auto_cluster():
+    sv.set_cluster_size(0)
+    yield
+    sv.set_cluster_size(0)
+
+
+def small(V, B=6, K=4, dtype="bf16", T=1.0, sigma=1.5, peaks=5, N=1, sigmas=None, selected=0, seed=11):
+    sig = tuple(sigmas) if sigmas is not None else (sigma,)
+    return workloads.Workload("t", B=B, K=K, V=V, N=len(sig), dtype=dtype, temperature=T, peaks=peaks,
+                              draft_sigmas=sig, selected=selected, gen_seed=seed)
+
+
+# ------------------------------------------------------------------------------------------------
+# standard verification
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("V,C,dtype", [
+    (1000, 0, "fp32"), (1000, 0, "bf16"), (4099, 0, "bf16"), (4099, 4, "bf16"), (8192, 2, "fp32"),
+    (20000, 8, "bf16"), (20001, 8, "bf16"), (65536, 0, "bf16"), (128256, 0, "bf16"), (151936, 0, "bf16"),
+    (3000, 16, "bf16"),
+])
+def test_verify_small(V, C, dtype):
+    sv.set_cluster_size(C)
+    w = small(V, dtype=dtype, T=0.8)
+    inp = workloads.make(w)
+    ref = oracle_verify(inp)
+    g = to_device(inp)
+    out = sv.verify(g["target"], g["draft"], g["tokens"], g["seeds"], w.temperature)
+    torch.cuda.synchronize()
+    assert_diag(out, ref)
+    assert_chain(out, ref, w.K)
+    assert sv.read_status(out["workspace"]) == 0
+
+
+def test_verify_deterministic():
+    w = small(30011, B=16, K=5)
+    g = to_device(workloads.make(w))
+    a = sv.verify(g["target"], g["draft"], g["tokens"], g["seeds"])
+    b = sv.verify(g["target"], g["draft"], g["tokens"], g["seeds"])
+    torch.cuda.synchronize()
+    for k in ("accept_len", "out_tokens", "diag"):
+        assert torch.equal(a[k], b[k])
+
+
+def test_verify_cluster_size_invariance():
+    w = small(50000, B=8, K=3)
+    g = to_device(workloads.make(w))
+    outs = []
+    for C in (2, 4, 8, 16):
+        sv.set_cluster_size(C)
+        o = sv.verify(g["target"], g["draft"], g["tokens"], g["seeds"])
+        torch.cuda.synchronize()
+        outs.append(o)
+    for o in outs[1:]:
+        assert torch.equal(o["accept_len"], outs[0]["accept_len"])
+        assert torch.allclose(o["diag"], outs[0]["diag"], atol=PROB_TOL, rtol=0)
+
+
+@pytest.mark.parametrize("name", ["tiny_sps_v1000", "sps_llama3_b64_k5"])
+def test_verify_named_workloads_full(name):
+    w = workloads.WORKLOADS[name]
+    inp = workloads.make(w, device="cuda")
+    ref = oracle_verify(inp)
+    out = sv.verify(inp["target"], inp["draft"], inp["tokens"], inp["seeds"], w.temperature)
+    torch.cuda.synchronize()
+    assert_diag(out, ref)
+    assert_chain(out, ref, w.K)
+
+
+# ------------------------------------------------------------------------------------------------
+# edge cases
+# ------------------------------------------------------------------------------------------------
+def test_B_zero_is_noop():
+    t = torch.zeros((0, 3, 100), dtype=torch.bfloat16, device="cuda")
+    d = torch.zeros((0, 2, 100), dtype=torch.bfloat16, device="cuda")
+    tok = torch.zeros((0, 2), dtype=torch.int32, device="cuda")
+    seeds = torch.zeros(0, dtype=torch.int64, device="cuda")
+    ws = sv.new_workspace(1, 2, 100)
+    out = sv.verify(t, d, tok, seeds, workspace=ws)
+    assert out["accept_len"].numel() == 0
+
+
+def test_vocab_of_one_and_two():
+    for V in (1, 2):
+        w = small(V, B=5, K=3, peaks=0)
+        inp = workloads.make(w)
+        ref = oracle_verify(inp)
+        g = to_device(inp)
+        out = sv.verify(g["target"], g["draft"], g["tokens"], g["seeds"])
+        torch.cuda.synchronize()
+        assert_diag(out, ref)
+        assert_chain(out, ref, w.K)
+    # V = 1: every draft is the only token, always accepted, Z = 0
+    assert np.all(out["accept_len"].cpu().numpy() >= 0)
+
+
+def test_perfect_draft_always_accepts():
+    w = small(7000, B=8, K=5)
+    inp = workloads.make(w)
+    inp["draft"] = inp["target"][:, :w.K].clone()
+    ref = oracle_verify(inp)
+    g = to_device(inp)
+    out = sv.verify(g["target"], g["draft"], g["tokens"], g["seeds"])
+    torch.cuda.synchronize()
+    assert np.all(out["accept_len"].cpu().numpy() == w.K)
+    assert np.all(out["diag"].cpu().numpy()[..., 2] <= 1e-6)
+    assert_chain(out, ref, w.K)
+
+
+def test_disjoint_support_always_rejects():
+    B, K, V = 6, 3, 512
+    t = torch.full((B, K + 1, V), float("-inf"))
+    d = torch.full((B, K, V), float("-inf"))
+    gen = torch.Generator().manual_seed(3)
+    t[:, :, V // 2:] = torch.randn((B, K + 1, V - V // 2), generator=gen)
+    d[:, :, :V // 2] = torch.randn((B, K, V // 2), generator=gen)
+    tok = torch.randint(0, V // 2, (B, K), generator=gen, dtype=torch.int32)
+    seeds = torch.arange(B, dtype=torch.int64)
+    inp = dict(target=t.to(torch.bfloat16), draft=d.to(torch.bfloat16), tokens=tok, seeds=seeds, temperature=1.0)
+    ref = oracle_verify(inp)
+    g = to_device(inp)
+    out = sv.verify(g["target"], g["draft"], g["tokens"], g["seeds"])
+    torch.cuda.synchronize()
+    assert np.all(out["accept_len"].cpu().numpy() == 0)
+    assert np.all(out["out_tokens"].cpu().numpy()[:, 0] >= V // 2)
+    assert_diag(out, ref)
+    assert_chain(out, ref, K)
+
+
+def test_masked_logits_and_bad_token_status():
+    w = small(3000, B=4, K=3)
+    inp = workloads.make(w)
+    inp["target"][:, :, :100] = float("-inf")
+    inp["tokens"][1, 1] = w.V + 5          # out of range: flagged, verified as a zero-probability proposal
+    inp["tokens"][2, 0] = -1
+    ref = oracle_verify(dict(inp, tokens=inp["tokens"].clamp(0, w.V - 1)))
+    g = to_device(inp)
+    ws = sv.new_workspace(w.B, w.K, w.V)
+    out = sv.verify(g["target"], g["draft"], g["tokens"], g["seeds"], workspace=ws)
+    torch.cuda.synchronize()
+    assert sv.read_status(ws) & sv.STATUS_BAD_TOKEN
+    d = out["diag"].cpu().numpy()
+    assert d[1, 1, 0] == 0.0 and d[1, 1, 1] == 0.0
+    assert out["accept_len"][1].item() <= 1 and out["accept_len"][2].item() == 0
+    tok = out["out_tokens"].cpu().numpy()
+    assert np.all(tok[tok >= 0] >= 100)             # masked tokens are never emitted
+    sv.clear_status(ws)
+    assert sv.read_status(ws) == 0
+
+
+def test_invalid_arguments_raise():
+    w = small(1000, B=2, K=2)
+    g = to_device(workloads.make(w))
+    with pytest.raises(sv.SpecError) as e:
+        sv.verify(g["target"], g["draft"], g["tokens"], g["seeds"], temperature=0.0)
+    assert e.value.code == sv.SPEC_ERR_UNSUPPORTED
+    with pytest.raises(sv.SpecError) as e:
+        sv.verify(g["target"], g["draft"], g["tokens"], g["seeds"], temperature=float("nan"))
+    assert e.value.code == sv.SPEC_ERR_INVALID
+    with pytest.raises(sv.SpecError) as e:
+        sv.cactus_verify(g["target"], g["draft"], g["tokens"], g["seeds"], delta=-1.0)
+    assert e.value.code == sv.SPEC_ERR_INVALID
+    small_ws = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(sv.SpecError):
+        sv.verify(g["target"], g["draft"], g["tokens"], g["seeds"], workspace=small_ws)
+
+
+# ------------------------------------------------------------------------------------------------
+# losslessness on the GPU: chi-square of emitted tokens against p_target
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("V", [3, 8, 64])
+def test_gpu_chi2_lossless(V):
+    from scipy import special, stats
+    rng = np.random.default_rng(V)
+    n = 1 << 17
+    p = special.softmax(rng.normal(0, 1.5, V)).astype(np.float64)
+    q = special.softmax(np.log(p) + rng.normal(0, 1.0, V))
+    lt = np.log(p).astype(np.float32)
+    ld = np.log(q).astype(np.float32)
+    t = torch.from_numpy(np.broadcast_to(lt, (n, 2, V)).copy()).cuda()
+    d = torch.from_numpy(np.broadcast_to(ld, (n, 1, V)).copy()).cuda()
+    tok = torch.from_numpy(rng.choice(V, size=(n, 1), p=q / q.sum()).astype(np.int32)).cuda()
+    seeds = torch.full((n,), 12345, dtype=torch.int64, device="cuda")
+    out = sv.verify(t, d, tok, seeds, want_diag=False)
+    torch.cuda.synchronize()
+    first = out["out_tokens"][:, 0].cpu().numpy()
+    counts = np.bincount(first, minlength=V)
+    pf = np.exp(lt.astype(np.float64))
+    pf /= pf.sum()
+    assert stats.chisquare(counts, pf * n).pvalue > 1e-6
+    # and the rejection rate is Z = 1 - sum min(p, q)
+    qf = np.exp(ld.astype(np.float64))
+    qf /= qf.sum()
+    rej = (out["accept_len"].cpu().numpy() == 0).mean()
+    z = np.maximum(pf - qf, 0).sum()
+    assert abs(rej - z) < 5 * np.sqrt(z * (1 - z) / n) + 1e-4
+
+
+# ------------------------------------------------------------------------------------------------
+# Cactus
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("delta", [0.0, 0.75, 1.0])
+@pytest.mark.parametrize("V,C", [(3000, 0), (40000, 8)])
+def test_cactus_small(delta, V, C):
+    sv.set_cluster_size(C)
+    w = small(V, B=8, K=5, sigma=2.0)
+    inp = workloads.make(w)
+    ref = oracle.cactus(host(inp["target"]), host(inp["draft"]), inp["tokens"].numpy(),
+                        inp["seeds"].numpy().astype(np.uint64), delta, w.temperature)
+    g = to_device(inp)
+    out = sv.cactus_verify(g["target"], g["draft"], g["tokens"], g["seeds"], delta, w.temperature)
+    torch.cuda.synchronize()
+    assert np.abs(out["gamma_star"].cpu().numpy() - ref["gamma_star"]).max() <= PROB_TOL
+    assert_diag(out, ref)
+    assert_chain(out, ref, w.K)
+
+
+def test_cactus_delta_zero_bit_identical_to_verify():
+    w = small(151936, B=6, K=4, sigma=2.0)
+    g = to_device(workloads.make(w))
+    a = sv.verify(g["target"], g["draft"], g["tokens"], g["seeds"])
+    c = sv.cactus_verify(g["target"], g["draft"], g["tokens"], g["seeds"], 0.0)
+    torch.cuda.synchronize()
+    assert torch.equal(a["accept_len"], c["accept_len"])
+    assert torch.equal(a["out_tokens"], c["out_tokens"])
+    assert torch.equal(a["diag"], c["diag"])
+
+
+def test_cactus_named_workload_sampled():
+    w = workloads.WORKLOADS["cactus_qwen_b128_m20"]
+    inp = workloads.make(w, device="cuda")
+    sel = torch.arange(0, w.B, 8)
+    for delta in w.deltas:
+        out = sv.cactus_verify(inp["target"], inp["draft"], inp["tokens"], inp["seeds"], delta, w.temperature)
+        torch.cuda.synchronize()
+        ref = oracle.cactus(host(inp["target"][sel]), host(inp["draft"][sel]), inp["tokens"][sel].cpu().numpy(),
+                            inp["seeds"][sel].cpu().numpy().astype(np.uint64), delta, w.temperature,
+                            seq_index=sel.numpy())
+        sub = {k: out[k][sel.cuda()] for k in ("accept_len", "out_tokens", "diag")}
+        assert np.abs(out["gamma_star"][sel.cuda()].cpu().numpy() - ref["gamma_star"]).max() <= PROB_TOL
+        assert_diag(sub, ref)
+        assert_chain(sub, ref, w.K)
+
+
+# ------------------------------------------------------------------------------------------------
+# HedgeSpec counterfactual gamma
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("V,C,selected", [(5000, 0, -1), (5000, 0, 1), (33333, 8, 2), (33336, 4, 0)])
+def test_counterfactual_small(V, C, selected):
+    sv.set_cluster_size(C)
+    w = small(V, B=5, K=4, sigmas=(0.5, 1.0, 2.0, 4.0), selected=max(selected, 0))
+    inp = workloads.make(w)
+    ref = oracle.counterfactual(host(inp["target"]), host(inp["drafters"]), w.temperature, selected,
+                                inp["tokens"].numpy(), inp["seeds"].numpy().astype(np.uint64))
+    g = to_device(inp)
+    out = sv.counterfactual_gamma(g["target"], g["drafters"], w.temperature, selected, g["tokens"], g["seeds"])
+    torch.cuda.synchronize()
+    gam = out["gamma"].cpu().numpy()
+    assert np.abs(gam - ref["gamma"]).max() <= PROB_TOL
+    assert np.abs(out["loss"].cpu().numpy() - (1 - ref["gamma"])).max() <= PROB_TOL
+    assert np.abs((1 - gam) - ref["tv"]).max() <= PROB_TOL          # gamma = 1 - TV
+    if selected >= 0:
+        assert_diag(out, ref)
+        assert_chain(out, ref, w.K)
+        # the fused chain equals a plain verify of the selected drafter
+        v = sv.verify(g["target"], g["drafters"][selected].contiguous(), g["tokens"], g["seeds"], w.temperature)
+        torch.cuda.synchronize()
+        assert torch.equal(v["accept_len"], out["accept_len"]) and torch.equal(v["out_tokens"], out["out_tokens"])
+
+
+def test_counterfactual_named_full():
+    w = workloads.WORKLOADS["hedgespec_n7_b32_k5"]
+    inp = workloads.make(w, device="cuda")
+    out = sv.counterfactual_gamma(inp["target"], inp["drafters"], w.temperature, w.selected, inp["tokens"],
+                                  inp["seeds"])
+    torch.cuda.synchronize()
+    ref = oracle.counterfactual(host(inp["target"]), host(inp["drafters"]), w.temperature, w.selected,
+                                inp["tokens"].cpu().numpy(), inp["seeds"].cpu().numpy().astype(np.uint64))
+    assert np.abs(out["gamma"].cpu().numpy() - ref["gamma"]).max() <= PROB_TOL
+    assert_diag(out, ref)
+    assert_chain(out, ref, w.K)
+
+
+def test_large_pool_named_sampled():
+    """21 drafters, B=256, K=8, V=151936, T=0.7, fused verify of drafter 4: gamma for every drafter and the
+    chain checked on 16 sampled sequences (the oracle on all 256 would take minutes)."""
+    w = workloads.WORKLOADS["hedgespec_n21_b256_k8"]
+    inp = workloads.make(w, device="cuda")
+    out = sv.counterfactual_gamma(inp["target"], inp["drafters"], w.temperature, w.selected, inp["tokens"],
+                                  inp["seeds"])
+    torch.cuda.synchronize()
+    sel = torch.arange(3, w.B, 16)
+    selc = sel.cuda()
+    ref = oracle.counterfactual(host(inp["target"][selc]), host(inp["drafters"][:, selc]), w.temperature,
+                                w.selected, inp["tokens"][selc].cpu().numpy(),
+                                inp["seeds"][selc].cpu().numpy().astype(np.uint64), seq_index=sel.numpy())
+    assert np.abs(out["gamma"][:, selc].cpu().numpy() - ref["gamma"]).max() <= PROB_TOL
+    sub = {k: out[k][selc] for k in ("accept_len", "out_tokens", "diag")}
+    assert_diag(sub, ref)
+    assert_chain(sub, ref, w.K)
+    # properties over the whole batch
+    gam = out["gamma"].cpu().numpy()
+    assert np.all((gam > 0) & (gam <= 1.0 + 1e-6))
+    assert np.all(np.diff(gam.mean(axis=(1, 2))) < 0.05)   # larger drafter noise, lower acceptance (on average)
