@@ -43,21 +43,67 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait that lets the thread sleep (up to `hint_ns`) until the phase completes: no hot polling.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Same, with acquire ordering at cluster scope (arrivals come from other CTAs of the cluster).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Waits for phase `parity` of `bar` to complete, giving up after `limit_ns` of wall time. Returns false
 // (and ORs `flag` into *status) when it gave up. The wait cannot hang the GPU.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, unsigned* status,
                                                   unsigned flag, uint64_t limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
+    constexpr uint32_t HINT = 20000;   // ns
+    if (CLUSTER ? mbar_try_wait_cluster(bar, parity, HINT) : mbar_try_wait_sleep(bar, parity, HINT)) return true;
     const uint64_t t0 = global_timer_ns();
     for (;;) {
-#pragma unroll 1
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+        if (CLUSTER ? mbar_try_wait_cluster(bar, parity, HINT) : mbar_try_wait_sleep(bar, parity, HINT)) return true;
         if (global_timer_ns() - t0 > limit_ns) {
             atomicOr(status, flag);
             return false;
         }
     }
+}
+
+// Local arrive (release at CTA scope).
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Arrive on an mbarrier of another CTA of the cluster (address from map_to_rank), releasing this
+// thread's earlier shared::cluster stores to that CTA.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbarrier_init_cluster() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Named barrier over the first `nthreads` threads (barrier 0 is __syncthreads).
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // Bulk copy global -> this CTA's shared memory; completion is signalled as transaction bytes on `bar`.
@@ -123,6 +169,13 @@ __device__ __forceinline__ void cluster_sync_all() {
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// log2(x) via the SFU (lg2.approx): absolute error ~2^-22 for x near 1.
+__device__ __forceinline__ float lg2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
 

@@ -4,6 +4,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <algorithm>
 #include <mutex>
 
 #include "specverify.h"
@@ -38,25 +39,27 @@ struct Plan {
     int tma = 0;
 };
 
-size_t fixed_smem(int C, int tiles_cap) {
-    return MAX_SLOTS * 8 + static_cast<size_t>(2 * C * 8) * 4 + static_cast<size_t>(tiles_cap) * 4 + NWARPS * 4 * 4 +
-           8 * 4 + 8 * 4;
+size_t fixed_smem(int C) {
+    // full/empty barriers, two exchange barriers, exchange records [2][C][8], per-warp (max, sum) pairs
+    return 2 * MAX_SLOTS * 8 + 2 * 8 + static_cast<size_t>(2 * C * 8) * 4 + NWC * 4 * 4;
 }
 
 int passes_for(int slice_elems) {
     const int chunks = (slice_elems + CHUNK - 1) / CHUNK;
-    const int need = (chunks + NT - 1) / NT;
+    const int need = (chunks + NTC - 1) / NTC;
     static const int supported[] = {1, 2, 4, 5, 8};
     for (int p : supported)
         if (p >= need) return p;
     return -1;
 }
 
+int slice_for(int V, int C) { return ((V + SLICE_Q - 1) / SLICE_Q + C - 1) / C * SLICE_Q; }
+int tiles_cap_for(int slice_elems) { return (slice_elems + TILE - 1) / TILE; }
+
 // Chooses the cluster size C (vocabulary split), the per-CTA slice, the register passes P and the number
 // of shared-memory row slots. Two CTAs per SM are preferred (one computes while the other's copies
 // land); the slot counts shrink until that fits.
 bool make_plan(int V, int elem_bytes, int n_other, bool aligned, Plan& pl) {
-    const int q_tiles = (V + SLICE_Q - 1) / SLICE_Q;
     int cands[5] = {1, 2, 4, 8, 16};
     int start = 0;
     if (g_cluster_override > 0) {
@@ -72,13 +75,12 @@ bool make_plan(int V, int elem_bytes, int n_other, bool aligned, Plan& pl) {
         }
         Plan p;
         p.C = C;
-        p.slice_elems = (q_tiles + C - 1) / C * SLICE_Q;
+        p.slice_elems = slice_for(V, C);
         p.P = passes_for(p.slice_elems);
         if (p.P < 0) continue;
         p.slot_bytes = p.slice_elems * elem_bytes;
-        const int ntiles = (p.slice_elems + TILE - 1) / TILE;
-        p.tiles_cap = (ntiles + 3) / 4 * 4;
-        const size_t fixed = fixed_smem(C, p.tiles_cap);
+        p.tiles_cap = tiles_cap_for(p.slice_elems);
+        const size_t fixed = fixed_smem(C);
         const size_t two_per_sm = SMEM_PER_SM / 2 - SMEM_RESERVED_PER_CTA;
         // preferences: (ts, r)
         const int pref_verify[][2] = {{2, 1}, {1, 1}};
@@ -186,6 +188,28 @@ cudaError_t max_clusters(KernelFn fn, int C, size_t smem, int& out) {
     return cudaSuccess;
 }
 
+// Workspace layout: [status header][records B*(K+1)*REC][tile masses B*(K+1)*Cmax*tiles][gamma partials
+// N*B*K*Cmax*NWC]. The per-row regions are sized for the largest cluster split so that any plan fits.
+struct WsLayout {
+    size_t rec_off, tiles_off, gpart_off, total;
+    int tiles_row;   // floats per row in the tile region (>= C * tiles_cap for every plan)
+    int gpart_row;   // floats per (drafter, b, j) in the gamma region (>= C * NWC)
+};
+
+WsLayout ws_layout(int B, int K, int V, int N) {
+    WsLayout w;
+    int tiles_row = 0;
+    for (int C : {1, 2, 4, 8, 16}) tiles_row = std::max(tiles_row, C * tiles_cap_for(slice_for(V, C)));
+    w.tiles_row = tiles_row;
+    w.gpart_row = 16 * NWC;
+    const size_t rows = static_cast<size_t>(B) * static_cast<size_t>(K + 1);
+    w.rec_off = WS_HEADER;
+    w.tiles_off = w.rec_off + rows * REC * sizeof(float);
+    w.gpart_off = w.tiles_off + rows * static_cast<size_t>(tiles_row) * sizeof(float);
+    w.total = w.gpart_off + static_cast<size_t>(N) * B * K * static_cast<size_t>(w.gpart_row) * sizeof(float);
+    return w;
+}
+
 struct Call {
     const void* target;
     const void* others;
@@ -222,11 +246,12 @@ spec_status run(const Call& a) {
     cudaError_t e = max_clusters(fn, pl.C, pl.smem, ncl);
     if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "occupancy query failed: %s", cudaGetErrorString(e));
 
+    const WsLayout wl = ws_layout(a.B, a.K, a.V, a.N);
+    unsigned char* ws = static_cast<unsigned char*>(a.workspace);
     KParams k = {};
     k.target = static_cast<const unsigned char*>(a.target);
     k.others = static_cast<const unsigned char*>(a.others);
     k.tokens = chain ? a.tokens : nullptr;
-    k.seeds = chain ? a.seeds : nullptr;
     k.B = a.B;
     k.K = a.K;
     k.V = a.V;
@@ -242,12 +267,13 @@ spec_status run(const Call& a) {
     k.ts = pl.ts;
     k.r = pl.r;
     k.slot_bytes = pl.slot_bytes;
+    // the kernels index the tile region as (row * C + rank) * tiles_cap + tile: rows are C * tiles_cap <=
+    // wl.tiles_row floats apart, so the region sized with wl.tiles_row holds every plan
     k.tiles_cap = pl.tiles_cap;
-    k.gamma = a.gamma;
-    k.loss = a.loss;
-    unsigned char* ws = static_cast<unsigned char*>(a.workspace);
     k.status = reinterpret_cast<unsigned*>(ws);
-    k.rec = chain ? reinterpret_cast<float*>(ws + WS_HEADER) : nullptr;
+    k.rec = chain ? reinterpret_cast<float*>(ws + wl.rec_off) : nullptr;
+    k.tiles = chain ? reinterpret_cast<float*>(ws + wl.tiles_off) : nullptr;
+    k.gpart = a.gamma ? reinterpret_cast<float*>(ws + wl.gpart_off) : nullptr;
 
     const int grid_clusters = ncl < k.num_items ? ncl : k.num_items;
     cudaLaunchConfig_t cfg = {};
@@ -265,29 +291,56 @@ spec_status run(const Call& a) {
     e = cudaLaunchKernelEx(&cfg, fn, k);
     if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "verification kernel launch failed: %s", cudaGetErrorString(e));
 
+    // follow-up kernels: launched with programmatic stream serialisation, they wait on the grid above
+    // (griddepcontrol.wait) while their launch overlaps its tail
+    cudaLaunchAttribute pa[1];
+    pa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pa[0].val.programmaticStreamSerializationAllowed = 1;
+    const int per_block = 8;   // warps per block
+    if (a.gamma) {
+        GParams g = {};
+        g.gpart = k.gpart;
+        g.n_out = a.N * a.B * a.K;
+        g.C = pl.C;
+        g.gamma = a.gamma;
+        g.loss = a.loss;
+        cudaLaunchConfig_t gc = {};
+        gc.gridDim = dim3(static_cast<unsigned>((g.n_out + per_block - 1) / per_block), 1, 1);
+        gc.blockDim = dim3(per_block * 32, 1, 1);
+        gc.stream = a.stream;
+        gc.attrs = pa;
+        gc.numAttrs = 1;
+        e = cudaLaunchKernelEx(&gc, gamma_reduce_kernel, g);
+        if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "gamma reduction launch failed: %s", cudaGetErrorString(e));
+    }
     if (chain) {
         FParams f = {};
         f.rec = k.rec;
+        f.tiles = k.tiles;
+        f.target = k.target;
+        f.other = k.others + static_cast<size_t>(a.selected) * a.B * a.K * static_cast<size_t>(a.V) * eb;
         f.tokens = a.tokens;
         f.seeds = a.seeds;
         f.B = a.B;
         f.K = a.K;
+        f.V = a.V;
+        f.C = pl.C;
+        f.slice_elems = pl.slice_elems;
+        f.tiles_cap = pl.tiles_cap;
+        f.aligned = aligned ? 1 : 0;
+        f.c = k.c;
         f.accept_len = a.accept_len;
         f.out_tokens = a.out_tokens;
         f.diag = a.diag;
         f.gamma_star = a.gamma_star;
         cudaLaunchConfig_t fc = {};
-        cudaLaunchAttribute fa[1];
-        const int per_block = 8;   // sequences (warps) per block
         fc.gridDim = dim3(static_cast<unsigned>((a.B + per_block - 1) / per_block), 1, 1);
         fc.blockDim = dim3(per_block * 32, 1, 1);
-        fc.dynamicSmemBytes = 0;
         fc.stream = a.stream;
-        fa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        fa[0].val.programmaticStreamSerializationAllowed = 1;
-        fc.attrs = fa;
+        fc.attrs = pa;
         fc.numAttrs = 1;
-        e = cudaLaunchKernelEx(&fc, finish_kernel, f);
+        e = a.dtype == SPEC_BF16 ? cudaLaunchKernelEx(&fc, finish_kernel<Bf16>, f)
+                                 : cudaLaunchKernelEx(&fc, finish_kernel<F32>, f);
         if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "chain kernel launch failed: %s", cudaGetErrorString(e));
     }
     return SPEC_OK;
@@ -321,10 +374,8 @@ using namespace specv;
 extern "C" {
 
 size_t spec_workspace_size(int B, int K, int V, int N) {
-    (void)V;
-    (void)N;
-    if (B < 0 || K < 0) return 0;
-    return WS_HEADER + static_cast<size_t>(B) * static_cast<size_t>(K + 1) * REC * sizeof(float);
+    if (B < 0 || K < 0 || V < 1 || N < 1) return 0;
+    return ws_layout(B, K, V, N).total;
 }
 
 spec_status spec_verify(const void* target_logits, const void* draft_logits, spec_dtype dtype,

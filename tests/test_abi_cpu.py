@@ -41,7 +41,13 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_workspace_size(lib):
     import speculative_decoding_verification_target_gb300 as sv
-    assert sv.workspace_size(64, 5, 128256, 1) == 256 + 64 * 6 * 32
+    # header + per-row records + per-row tile masses + gamma partials; monotone in every size
+    base = sv.workspace_size(64, 5, 128256, 1)
+    assert base >= 256 + 64 * 6 * 32 + 64 * 6 * (128256 // 256) * 4
+    assert sv.workspace_size(128, 5, 128256, 1) > base
+    assert sv.workspace_size(64, 8, 128256, 1) > base
+    assert sv.workspace_size(64, 5, 151936, 1) > base
+    assert sv.workspace_size(64, 5, 128256, 7) > base
     assert sv.workspace_size(0, 5, 1000, 1) == 256
 
 
