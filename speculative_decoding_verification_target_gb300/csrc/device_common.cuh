@@ -70,16 +70,21 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
 }
 
 // Waits for phase `parity` of `bar` to complete, giving up after `limit_ns` of wall time. Returns false
-// (and ORs `flag` into *status) when it gave up. The wait cannot hang the GPU.
+// (and ORs `flag` into *status) when it gave up. Between polls the warp sleeps (exponential backoff up to
+// 256 ns) so that waiting warps do not take issue slots from the warps that compute. The wait cannot hang
+// the GPU.
 template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, unsigned* status,
                                                   unsigned flag, uint64_t limit_ns) {
-    constexpr uint32_t HINT = 20000;   // ns
+    constexpr uint32_t HINT = 1000;   // ns
     if (CLUSTER ? mbar_try_wait_cluster(bar, parity, HINT) : mbar_try_wait_sleep(bar, parity, HINT)) return true;
     const uint64_t t0 = global_timer_ns();
-    for (;;) {
+    uint32_t backoff = 16;
+    for (int it = 0;; ++it) {
+        __nanosleep(backoff);
+        if (backoff < 256) backoff <<= 1;
         if (CLUSTER ? mbar_try_wait_cluster(bar, parity, HINT) : mbar_try_wait_sleep(bar, parity, HINT)) return true;
-        if (global_timer_ns() - t0 > limit_ns) {
+        if ((it & 63) == 63 && global_timer_ns() - t0 > limit_ns) {
             atomicOr(status, flag);
             return false;
         }
@@ -195,13 +200,20 @@ __device__ __forceinline__ MaxSum ms_merge(MaxSum a, MaxSum b, float c) {
     const float m = fmaxf(a.m, b.m);
     return {m, a.s * ex2((a.m - m) * c) + b.s * ex2((b.m - m) * c)};
 }
+// Warp-wide max of a float (one redux instruction on sm_100-family GPUs).
+__device__ __forceinline__ float warp_max(float v) {
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
+
+// Warp-wide merge of (max, sum) pairs: M = max of the lanes' maxima, S = sum of s * 2^((m - M) c).
+// One redux, one exp2 per lane and a butterfly sum: every lane returns the same pair.
 __device__ __forceinline__ MaxSum warp_ms(MaxSum v, float c) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        MaxSum w{__shfl_xor_sync(0xffffffffu, v.m, o), __shfl_xor_sync(0xffffffffu, v.s, o)};
-        v = ms_merge(v, w, c);
-    }
-    return v;
+    const bool has = v.s > 0.f;
+    const float M = warp_max(has ? v.m : __uint_as_float(0xFF800000u));
+    const float s = has ? v.s * ex2((v.m - M) * c) : 0.f;
+    return {M, warp_sum(s)};
 }
 
 // ------------------------------------------------------------------------------------------------

@@ -203,6 +203,32 @@ __device__ __forceinline__ MaxSum local_stats(const typename E::Raw (&raw)[P], f
     return {m, s2.x + s2.y};
 }
 
+// Same statistics streamed from a shared-memory slot (no register copy of the row is kept).
+template <class E, int P>
+__device__ __forceinline__ MaxSum local_stats_smem(const unsigned char* slot, int ctid, int nchunks, float c) {
+    typename E::Max mm = E::max_init();
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+        const int k = p * NTC + ctid;
+        if (k < nchunks) mm = E::max_acc(mm, E::lds(slot, k));
+    }
+    const float m = E::max_fin(mm);
+    if (!(m > __uint_as_float(0xFF800000u))) return {m, 0.f};
+    const float2 cc = make_float2(c, c);
+    const float2 nb = make_float2(-m * c, -m * c);
+    float2 s2 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+        const int k = p * NTC + ctid;
+        if (k < nchunks) {
+            const typename E::Raw r = E::lds(slot, k);
+#pragma unroll
+            for (int w = 0; w < 4; ++w) s2 = __fadd2_rn(s2, ex2x2(__ffma2_rn(E::pair(r, w), cc, nb)));
+        }
+    }
+    return {m, s2.x + s2.y};
+}
+
 // Overlap only: adds 2^min(log2 h, log2 p_other) of the chunk's 8 elements to acc.
 template <class E>
 __device__ __forceinline__ float2 chunk_overlap(const typename E::Raw& rt, const typename E::Raw& ro, float2 cc,
@@ -306,24 +332,15 @@ __device__ __forceinline__ void cactus_scalars(float q, float delta, float& gsta
     log2s = log2f(s);
 }
 
-// Merge of word pair (wm, ws) over the cluster's records (C a power of two); the result is returned to
-// every lane of the calling warp.
+// Merge of word pair (wm, ws) over the cluster's records; every lane of the calling warp gets the result.
 __device__ __forceinline__ MaxSum merge_ranks(const float* rec8, uint32_t C, int lane, int wm, int ws, float c) {
     MaxSum v{__uint_as_float(0xFF800000u), 0.f};
     if (lane < static_cast<int>(C)) v = {rec8[lane * 8 + wm], rec8[lane * 8 + ws]};
-    for (int o = 1; o < static_cast<int>(C); o <<= 1) {
-        MaxSum w{__shfl_xor_sync(0xffffffffu, v.m, o), __shfl_xor_sync(0xffffffffu, v.s, o)};
-        v = ms_merge(v, w, c);
-    }
-    // lanes >= C only merged empties: take lane 0's value everywhere
-    return {__shfl_sync(0xffffffffu, v.m, 0), __shfl_sync(0xffffffffu, v.s, 0)};
+    return warp_ms(v, c);
 }
 
 __device__ __forceinline__ float max_ranks(const float* rec8, uint32_t C, int lane, int word) {
-    float v = __uint_as_float(0xFF800000u);
-    if (lane < static_cast<int>(C)) v = rec8[lane * 8 + word];
-    for (int o = 1; o < static_cast<int>(C); o <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return __shfl_sync(0xffffffffu, v, 0);
+    return warp_max(lane < static_cast<int>(C) ? rec8[lane * 8 + word] : __uint_as_float(0xFF800000u));
 }
 
 __device__ __forceinline__ int drafter_at(int i, int N, int selected) {
@@ -415,6 +432,15 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams prm) {
         const int ctid = tid;   // 0 .. NTC-1
         int g = 0;              // other rows consumed so far
         int e = 0;              // exchanges so far
+        // the draft token of an item is loaded one item ahead so that its latency stays hidden
+        auto token_of = [&](int kk) {
+            if (kk >= my_items || !prm.tokens) return -1;
+            const int ww = cid + kk * ncl;
+            const int jj = ww % J;
+            return jj < K ? __ldg(prm.tokens + static_cast<size_t>(ww / J) * K + jj) : -1;
+        };
+        int tok_next = token_of(0);
+        MaxSum st_t_next{NINF, 0.f};
         for (int k = 0; k < my_items; ++k) {
             const int w = cid + k * ncl;
             const int b = w / J, j = w % J;
@@ -422,21 +448,24 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams prm) {
             const size_t row = static_cast<size_t>(b) * (K + 1) + j;
             const int ts_slot = k % prm.ts;
             const unsigned char* tslot = slots + static_cast<size_t>(ts_slot) * prm.slot_bytes;
+            const int tok = tok_next;
+            tok_next = token_of(k + 1);
             int tl = -1;   // the draft token's index within my slice, -1 if elsewhere (or no token)
             if (j < K && prm.tokens) {
-                const int tok = __ldg(prm.tokens + static_cast<size_t>(b) * K + j);
                 const bool ok = tok >= 0 && tok < prm.V;
                 if (!ok && ctid == 0 && rank == 0) atomicOr(prm.status, STATUS_BAD_TOKEN);
                 if (ok && tok >= slice_start && tok < slice_start + n_el) tl = tok - slice_start;
             }
 
-            // ---- target row: local statistics ----
-            mbar_wait_bounded(&full[ts_slot], static_cast<uint32_t>((k / prm.ts) & 1), prm.status, STATUS_TIMEOUT, WAIT_LIMIT_NS);
+            // ---- target row: local statistics (already computed during the previous item's exchange
+            // when two target slots let the next target arrive early) ----
             MaxSum st_t;
-            {
-                Raw rt[P];
-                load_raw<E, P>(tslot, ctid, nchunks, rt);
-                st_t = local_stats<E, P>(rt, c);
+            if (k > 0 && prm.ts >= 2) {
+                st_t = st_t_next;
+            } else {
+                mbar_wait_bounded(&full[ts_slot], static_cast<uint32_t>((k / prm.ts) & 1), prm.status, STATUS_TIMEOUT,
+                                  WAIT_LIMIT_NS);
+                st_t = local_stats_smem<E, P>(tslot, ctid, nchunks, c);
             }
             float bt = 0.f, btp = 0.f, ht = 0.f;   // row scalars, identical in every consumer thread
             Raw ro[P];
@@ -486,7 +515,18 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams prm) {
                         mbar_arrive_remote(map_to_rank(smem_addr(&xbar[xp]), static_cast<uint32_t>(lane)));
                     }
                 }
-                mbar_wait_bounded<true>(&xbar[xp], static_cast<uint32_t>((e >> 1) & 1), prm.status, STATUS_TIMEOUT, WAIT_LIMIT_NS);
+                // while the records travel: statistics of the next item's target, if its slot is separate
+                if (i == 0 && prm.ts >= 2 && k + 1 < my_items) {
+                    const int ns = (k + 1) % prm.ts;
+                    mbar_wait_bounded(&full[ns], static_cast<uint32_t>(((k + 1) / prm.ts) & 1), prm.status,
+                                      STATUS_TIMEOUT, WAIT_LIMIT_NS);
+                    st_t_next = local_stats_smem<E, P>(slots + static_cast<size_t>(ns) * prm.slot_bytes, ctid, nchunks, c);
+                }
+                // only warp 0 polls for the cluster's records; the others park in the named barrier
+                if (warp == 0)
+                    mbar_wait_bounded<true>(&xbar[xp], static_cast<uint32_t>((e >> 1) & 1), prm.status, STATUS_TIMEOUT,
+                                            WAIT_LIMIT_NS);
+                named_sync(2, NTC);
                 ++e;
                 // every warp merges the cluster's records itself (no broadcast round trip)
                 const float* r8 = xchg + xp * C * 8;
