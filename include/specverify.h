@@ -122,10 +122,15 @@ spec_status spec_clear_status(void* workspace, void* stream);
 /* Thread-local message describing the last non-OK status returned on this thread. */
 const char* spec_last_error(void);
 
-/* Tuning and test hook: forces the number of CTAs that split one vocabulary row (1, 2, 4, 8 or 16; 0
- * restores the automatic choice). Process-wide, not thread-safe; results do not depend on it beyond
- * floating-point summation order. Returns 0, or -1 for an unsupported value. */
+/* Tuning and test hook: forces the number of CTAs that split one vocabulary row (1 to 16; 0 restores the
+ * automatic choice). Process-wide, not thread-safe; results do not depend on it beyond floating-point
+ * summation order. Returns 0, or -1 for an unsupported value. */
 int spec_debug_set_cluster_size(int C);
+
+/* Tuning and test hook: the launch plan of the last call made on this thread, as five ints: cluster size C,
+ * shared-memory stages per CTA, clusters launched, resident-target mode (0/1), pieces per CTA slice.
+ * out5 is host memory. Returns 0, or -1 for a NULL pointer. */
+int spec_debug_last_plan(int* out5);
 
 #ifdef __cplusplus
 }

@@ -20,7 +20,8 @@ from . import _build
 SPEC_OK, SPEC_ERR_INVALID, SPEC_ERR_CUDA, SPEC_ERR_UNSUPPORTED = 0, 1, 2, 3
 STATUS_BAD_TOKEN, STATUS_TIMEOUT = 1, 2
 EXPORTS = ("spec_workspace_size", "spec_verify", "spec_counterfactual_gamma", "spec_cactus_verify",
-           "spec_read_status", "spec_clear_status", "spec_last_error", "spec_debug_set_cluster_size")
+           "spec_read_status", "spec_clear_status", "spec_last_error", "spec_debug_set_cluster_size",
+           "spec_debug_last_plan")
 
 _lib = None
 
@@ -63,6 +64,8 @@ def load(build_if_missing: bool = False):
     lib.spec_last_error.restype = ctypes.c_char_p
     lib.spec_debug_set_cluster_size.argtypes = [I]
     lib.spec_debug_set_cluster_size.restype = I
+    lib.spec_debug_last_plan.argtypes = [ctypes.POINTER(ctypes.c_int)]
+    lib.spec_debug_last_plan.restype = I
     _lib = lib
     return lib
 
@@ -124,6 +127,13 @@ def set_cluster_size(C: int):
     """Tuning / test hook: CTAs per vocabulary row (0 = automatic)."""
     if load().spec_debug_set_cluster_size(int(C)) != 0:
         raise ValueError("unsupported cluster size %r" % C)
+
+
+def last_plan() -> dict:
+    """Tuning / test hook: the launch plan of the last call on this thread."""
+    out = (ctypes.c_int * 5)()
+    load().spec_debug_last_plan(out)
+    return dict(C=out[0], stages=out[1], clusters=out[2], resident=out[3], pieces=out[4])
 
 
 def _outputs(B, K, device, accept_len, out_tokens, diag, want_diag):

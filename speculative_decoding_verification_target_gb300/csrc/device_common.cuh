@@ -91,15 +91,36 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     }
 }
 
+// Shared-memory word with release / acquire ordering at CTA scope.
+__device__ __forceinline__ void st_release_shared(int* p, int v) {
+    asm volatile("st.release.cta.shared.b32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_shared(const int* p) {
+    int v;
+    asm volatile("ld.acquire.cta.shared.b32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+    return v;
+}
+
 // Local arrive (release at CTA scope).
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Local arrive counting as `count` arrivals.
+__device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
 }
 
 // Arrive on an mbarrier of another CTA of the cluster (address from map_to_rank), releasing this
 // thread's earlier shared::cluster stores to that CTA.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// Orders this thread's earlier generic-proxy accesses to shared memory before its later async-proxy
+// (bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void fence_mbarrier_init_cluster() {
@@ -112,8 +133,8 @@ __device__ __forceinline__ void named_sync(int id, int nthreads) {
 }
 
 // Bulk copy global -> this CTA's shared memory; completion is signalled as transaction bytes on `bar`.
-// dst and src must be 16-byte aligned, bytes a multiple of 16. L2 policy evict-first: the logits are
-// streamed once.
+// dst and src must be 16-byte aligned, bytes a multiple of 16. `policy` is an L2 cache policy from
+// createpolicy (evict-first for data read for the last time).
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
                                           uint64_t policy) {
     asm volatile(
@@ -125,6 +146,12 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
 

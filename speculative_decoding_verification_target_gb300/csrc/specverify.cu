@@ -27,111 +27,25 @@ constexpr int MAX_K = 64;
 constexpr int MAX_V = 262144;
 constexpr int MAX_N = 64;
 constexpr size_t WS_HEADER = 256;          // status word + padding
-constexpr int SMEM_PER_SM = 233472;        // GB300: 228 KiB per SM
-constexpr int SMEM_RESERVED_PER_CTA = 1024;
 constexpr int SMEM_MAX_PER_CTA = 232448;   // opt-in maximum per CTA
 
 int g_cluster_override = 0;   // test / tuning hook (0 = automatic)
+thread_local int g_last_plan[5] = {0, 0, 0, 0, 0};   // C, S, clusters launched, resident, pieces per slice
 
 struct Plan {
-    int C = 1, slice_elems = 0, P = 1, ts = 1, r = 1, slot_bytes = 0, tiles_cap = 0;
+    int C = 1, slice_elems = 0, pcap = 0, R = 0, resident = 0, tma = 0, ncl = 0;
     size_t smem = 0;
-    int tma = 0;
 };
 
-size_t fixed_smem(int C) {
-    // full/empty barriers, two exchange barriers, exchange records [2][C][8], per-warp (max, sum) pairs
-    return 2 * MAX_SLOTS * 8 + 2 * 8 + static_cast<size_t>(2 * C * 8) * 4 + NWC * 4 * 4;
-}
-
-int passes_for(int slice_elems) {
-    const int chunks = (slice_elems + CHUNK - 1) / CHUNK;
-    const int need = (chunks + NTC - 1) / NTC;
-    static const int supported[] = {1, 2, 4, 5, 8};
-    for (int p : supported)
-        if (p >= need) return p;
-    return -1;
-}
-
 int slice_for(int V, int C) { return ((V + SLICE_Q - 1) / SLICE_Q + C - 1) / C * SLICE_Q; }
-int tiles_cap_for(int slice_elems) { return (slice_elems + TILE - 1) / TILE; }
+int pcap_for(int slice_elems) { return (slice_elems + PE - 1) / PE; }
 
-// Chooses the cluster size C (vocabulary split), the per-CTA slice, the register passes P and the number
-// of shared-memory row slots. Two CTAs per SM are preferred (one computes while the other's copies
-// land); the slot counts shrink until that fits.
-bool make_plan(int V, int elem_bytes, int n_other, bool aligned, Plan& pl) {
-    int cands[5] = {1, 2, 4, 8, 16};
-    int start = 0;
-    if (g_cluster_override > 0) {
-        cands[0] = g_cluster_override;
-        start = 0;
-    }
-    const int ncand = g_cluster_override > 0 ? 1 : 5;
-    for (int ci = start; ci < ncand; ++ci) {
-        const int C = cands[ci];
-        // small vocabularies stay in one CTA; large ones use a cluster of 8 (16 only if 8 cannot hold)
-        if (g_cluster_override == 0) {
-            if (V > 8192 && C < 8) continue;
-        }
-        Plan p;
-        p.C = C;
-        p.slice_elems = slice_for(V, C);
-        p.P = passes_for(p.slice_elems);
-        if (p.P < 0) continue;
-        p.slot_bytes = p.slice_elems * elem_bytes;
-        p.tiles_cap = tiles_cap_for(p.slice_elems);
-        const size_t fixed = fixed_smem(C);
-        const size_t two_per_sm = SMEM_PER_SM / 2 - SMEM_RESERVED_PER_CTA;
-        // preferences: (ts, r)
-        const int pref_verify[][2] = {{2, 1}, {1, 1}};
-        const int pref_many[][2] = {{1, 2}, {1, 1}};
-        const auto& pref = n_other >= 2 ? pref_many : pref_verify;
-        bool ok = false;
-        for (const auto& tr : pref) {
-            const size_t need = static_cast<size_t>(tr[0] + tr[1]) * p.slot_bytes + fixed;
-            if (need <= two_per_sm) {
-                p.ts = tr[0];
-                p.r = tr[1];
-                p.smem = need;
-                ok = true;
-                break;
-            }
-        }
-        if (!ok) {
-            // one CTA per SM: more slots
-            const int pref_one[][2] = {{2, 2}, {1, 2}, {1, 1}};
-            for (const auto& tr : pref_one) {
-                const size_t need = static_cast<size_t>(tr[0] + tr[1]) * p.slot_bytes + fixed;
-                if (need <= static_cast<size_t>(SMEM_MAX_PER_CTA)) {
-                    p.ts = tr[0];
-                    p.r = tr[1];
-                    p.smem = need;
-                    ok = true;
-                    break;
-                }
-            }
-        }
-        if (!ok) continue;
-        p.tma = aligned ? 1 : 0;
-        pl = p;
-        return true;
-    }
-    return false;
+// barriers, exchange entries, scalars and the abort flag (see the layout note above rows_kernel)
+size_t fixed_smem(int R, int C) {
+    return static_cast<size_t>(W * R + 4 + 3 * NXB) * 8 + static_cast<size_t>(NXB * W * XW + NXB * C * XW + NXB * XW) * 4 + 16;
 }
 
 using KernelFn = void (*)(const KParams);
-
-template <class E>
-KernelFn pick_kernel(int P) {
-    switch (P) {
-        case 1: return rows_kernel<E, 1>;
-        case 2: return rows_kernel<E, 2>;
-        case 4: return rows_kernel<E, 4>;
-        case 5: return rows_kernel<E, 5>;
-        case 8: return rows_kernel<E, 8>;
-        default: return nullptr;
-    }
-}
 
 struct OccKey {
     KernelFn fn;
@@ -144,6 +58,7 @@ OccKey g_occ_keys[64];
 int g_occ_vals[64];
 int g_occ_n = 0;
 
+// Number of clusters of C CTAs with `smem` bytes each that fit on the GPU at once (cached per device).
 cudaError_t max_clusters(KernelFn fn, int C, size_t smem, int& out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -188,20 +103,91 @@ cudaError_t max_clusters(KernelFn fn, int C, size_t smem, int& out) {
     return cudaSuccess;
 }
 
-// Workspace layout: [status header][records B*(K+1)*REC][tile masses B*(K+1)*Cmax*tiles][gamma partials
-// N*B*K*Cmax*NWC]. The per-row regions are sized for the largest cluster split so that any plan fits.
+// Rows handled by the busiest of ncl clusters: items are dealt round robin, the B*K verified positions
+// (1 + N rows each) first and the B bonus rows (1 row each) last.
+long long busiest_rows(int BK, int B_bonus, int N, int ncl) {
+    long long worst = 0;
+    for (int c = 0; c < ncl; ++c) {
+        const long long pos = BK / ncl + (c < BK % ncl ? 1 : 0);
+        // bonus items are numbers BK .. BK + B_bonus - 1; count those congruent to c mod ncl
+        const int first = ((c - BK % ncl) % ncl + ncl) % ncl;   // offset of the first bonus item of c
+        const long long bon = B_bonus > first ? (B_bonus - 1 - first) / ncl + 1 : 0;
+        worst = std::max(worst, pos * (1 + N) + bon);
+    }
+    return worst;
+}
+
+// Chooses the cluster size C and the ring depth R. Each CTA holds, per consumer warp, R slots of one piece
+// and, when items have two or more drafters (resident mode), two copies of its target slice. Among the
+// cluster sizes whose shared memory fits, the plan minimises an estimate of the busiest CTA's time:
+// (rows of its cluster) x (slice length + a fixed per-row cost of the cluster-wide statistics exchange,
+// worth about UNIT_COST_EL logits of streaming), using the number of clusters the GPU places at once.
+// In streamed mode a slice is re-read from L2 about two rows after its first read; when (CTAs) x (two rows
+// of a slice) exceeds half of L2 the estimate grows with the excess. Ties go to the smaller cluster.
+constexpr double UNIT_COST_EL = 40000.0;
+
+spec_status make_plan(KernelFn fn, int V, int eb, int N, int BK, int B_bonus, bool aligned, Plan& out) {
+    static const int auto_cands[] = {1, 2, 4, 8, 16};
+    const int* cands = auto_cands;
+    int ncand = 5;
+    int forced[1];
+    if (g_cluster_override > 0) {
+        forced[0] = g_cluster_override;
+        cands = forced;
+        ncand = 1;
+    }
+    const int resident = N >= 2 ? 1 : 0;
+    const size_t slot_bytes = static_cast<size_t>(PE) * eb;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int l2 = 0;
+    cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
+    bool found = false;
+    double best = 0.0;
+    for (int ci = 0; ci < ncand; ++ci) {
+        Plan p;
+        p.C = cands[ci];
+        p.slice_elems = slice_for(V, p.C);
+        p.pcap = pcap_for(p.slice_elems);
+        p.resident = resident;
+        p.tma = aligned ? 1 : 0;
+        const size_t tb = resident ? (static_cast<size_t>(p.slice_elems) * eb + 127) / 128 * 128 : 0;
+        int R = MAX_R;
+        while (R >= 1 && 2 * tb + W * R * slot_bytes + fixed_smem(R, p.C) > static_cast<size_t>(SMEM_MAX_PER_CTA)) --R;
+        if (R < 1) continue;
+        p.R = R;
+        p.smem = 2 * tb + W * R * slot_bytes + fixed_smem(R, p.C);
+        int ncl = 0;
+        const cudaError_t e = max_clusters(fn, p.C, p.smem, ncl);
+        if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "occupancy query failed: %s", cudaGetErrorString(e));
+        p.ncl = ncl;
+        double cost = static_cast<double>(busiest_rows(BK, B_bonus, N, ncl)) * (p.slice_elems + UNIT_COST_EL);
+        const double footprint = static_cast<double>(ncl) * p.C * 2.0 * p.slice_elems * eb;
+        if (!resident && l2 > 0 && footprint > l2 / 2.0) cost *= 1.0 + (footprint - l2 / 2.0) / l2;
+        if (!found || cost < best * 0.999) {
+            best = cost;
+            out = p;
+            found = true;
+        }
+    }
+    if (!found) return fail(SPEC_ERR_UNSUPPORTED, "no launch plan fits V=%d (cluster override %d)", V, g_cluster_override);
+    return SPEC_OK;
+}
+
+// Workspace layout: [status header][records B*(K+1)*REC][piece masses B*(K+1)*pieces_row][gamma partials
+// N*B*K*16*W]. The per-row regions are sized for the largest cluster split so that any plan fits.
 struct WsLayout {
     size_t rec_off, tiles_off, gpart_off, total;
-    int tiles_row;   // floats per row in the tile region (>= C * tiles_cap for every plan)
-    int gpart_row;   // floats per (drafter, b, j) in the gamma region (>= C * NWC)
+    int tiles_row;   // floats per row in the piece-mass region (>= C * pcap for every plan)
+    int gpart_row;   // floats per (drafter, b, j) in the gamma region (>= C * W)
 };
 
 WsLayout ws_layout(int B, int K, int V, int N) {
     WsLayout w;
     int tiles_row = 0;
-    for (int C : {1, 2, 4, 8, 16}) tiles_row = std::max(tiles_row, C * tiles_cap_for(slice_for(V, C)));
+    for (int C = 1; C <= 16; ++C) tiles_row = std::max(tiles_row, C * pcap_for(slice_for(V, C)));
     w.tiles_row = tiles_row;
-    w.gpart_row = 16 * NWC;
+    w.gpart_row = 16 * W;
     const size_t rows = static_cast<size_t>(B) * static_cast<size_t>(K + 1);
     w.rec_off = WS_HEADER;
     w.tiles_off = w.rec_off + rows * REC * sizeof(float);
@@ -235,16 +221,15 @@ spec_status run(const Call& a) {
     const int eb = a.dtype == SPEC_BF16 ? 2 : 4;
     const bool chain = a.selected >= 0;
     const uintptr_t align_mask = 15;
+    // bulk copies need 16-byte aligned pieces of whole 8-logit chunks
     const bool aligned = ((reinterpret_cast<uintptr_t>(a.target) | reinterpret_cast<uintptr_t>(a.others)) & align_mask) == 0 &&
-                         (static_cast<size_t>(a.V) * eb) % 16 == 0;
+                         (static_cast<size_t>(a.V) * eb) % 16 == 0 && a.V % CHUNK == 0;
+    KernelFn fn = a.dtype == SPEC_BF16 ? rows_kernel<Bf16> : rows_kernel<F32>;
+    const int BK = a.B * a.K;
+    const int B_bonus = chain ? a.B : 0;
     Plan pl;
-    if (!make_plan(a.V, eb, a.N, aligned, pl))
-        return fail(SPEC_ERR_UNSUPPORTED, "no launch plan fits V=%d (cluster override %d)", a.V, g_cluster_override);
-    KernelFn fn = a.dtype == SPEC_BF16 ? pick_kernel<Bf16>(pl.P) : pick_kernel<F32>(pl.P);
-    if (!fn) return fail(SPEC_ERR_UNSUPPORTED, "no kernel for %d passes", pl.P);
-    int ncl = 0;
-    cudaError_t e = max_clusters(fn, pl.C, pl.smem, ncl);
-    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "occupancy query failed: %s", cudaGetErrorString(e));
+    spec_status st = make_plan(fn, a.V, eb, a.N, BK, B_bonus, aligned, pl);
+    if (st != SPEC_OK) return st;
 
     const WsLayout wl = ws_layout(a.B, a.K, a.V, a.N);
     unsigned char* ws = static_cast<unsigned char*>(a.workspace);
@@ -257,25 +242,30 @@ spec_status run(const Call& a) {
     k.V = a.V;
     k.N = a.N;
     k.selected = a.selected;
-    k.J = chain ? a.K + 1 : a.K;
-    k.num_items = a.B * k.J;
+    k.BK = BK;
+    k.num_items = BK + B_bonus;
     k.c = static_cast<float>(1.4426950408889634 / static_cast<double>(a.temperature));
     k.delta = a.delta;
     k.cactus = a.cactus;
     k.slice_elems = pl.slice_elems;
-    k.tma = pl.tma;
-    k.ts = pl.ts;
-    k.r = pl.r;
-    k.slot_bytes = pl.slot_bytes;
-    // the kernels index the tile region as (row * C + rank) * tiles_cap + tile: rows are C * tiles_cap <=
+    // the kernels index the piece-mass region as (row * C + rank) * pcap + piece: rows are C * pcap <=
     // wl.tiles_row floats apart, so the region sized with wl.tiles_row holds every plan
-    k.tiles_cap = pl.tiles_cap;
+    k.pcap = pl.pcap;
+    k.tma = pl.tma;
+    k.resident = pl.resident;
+    k.R = pl.R;
+    k.lead = 1;
     k.status = reinterpret_cast<unsigned*>(ws);
     k.rec = chain ? reinterpret_cast<float*>(ws + wl.rec_off) : nullptr;
     k.tiles = chain ? reinterpret_cast<float*>(ws + wl.tiles_off) : nullptr;
     k.gpart = a.gamma ? reinterpret_cast<float*>(ws + wl.gpart_off) : nullptr;
 
-    const int grid_clusters = ncl < k.num_items ? ncl : k.num_items;
+    const int grid_clusters = pl.ncl < k.num_items ? pl.ncl : k.num_items;
+    g_last_plan[0] = pl.C;
+    g_last_plan[1] = pl.R;
+    g_last_plan[2] = grid_clusters;
+    g_last_plan[3] = pl.resident;
+    g_last_plan[4] = pl.pcap;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute at[1];
     cfg.gridDim = dim3(static_cast<unsigned>(grid_clusters * pl.C), 1, 1);
@@ -288,7 +278,7 @@ spec_status run(const Call& a) {
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, fn, k);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, fn, k);
     if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "verification kernel launch failed: %s", cudaGetErrorString(e));
 
     // follow-up kernels: launched with programmatic stream serialisation, they wait on the grid above
@@ -326,7 +316,7 @@ spec_status run(const Call& a) {
         f.V = a.V;
         f.C = pl.C;
         f.slice_elems = pl.slice_elems;
-        f.tiles_cap = pl.tiles_cap;
+        f.pcap = pl.pcap;
         f.aligned = aligned ? 1 : 0;
         f.c = k.c;
         f.accept_len = a.accept_len;
@@ -494,8 +484,14 @@ spec_status spec_clear_status(void* workspace, void* stream) {
 
 const char* spec_last_error(void) { return g_err; }
 
+int spec_debug_last_plan(int* out5) {
+    if (!out5) return -1;
+    for (int i = 0; i < 5; ++i) out5[i] = g_last_plan[i];
+    return 0;
+}
+
 int spec_debug_set_cluster_size(int C) {
-    if (C != 0 && C != 1 && C != 2 && C != 4 && C != 8 && C != 16) return -1;
+    if (C < 0 || C > 16) return -1;
     g_cluster_override = C;
     return 0;
 }

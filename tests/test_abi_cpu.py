@@ -41,9 +41,10 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_workspace_size(lib):
     import speculative_decoding_verification_target_gb300 as sv
-    # header + per-row records + per-row tile masses + gamma partials; monotone in every size
+    # header + per-row records + per-row piece masses (one per 2048 logits at least) + gamma partials;
+    # monotone in every size
     base = sv.workspace_size(64, 5, 128256, 1)
-    assert base >= 256 + 64 * 6 * 32 + 64 * 6 * (128256 // 256) * 4
+    assert base >= 256 + 64 * 6 * 32 + 64 * 6 * (128256 // 2048) * 4 + 64 * 5 * 4
     assert sv.workspace_size(128, 5, 128256, 1) > base
     assert sv.workspace_size(64, 8, 128256, 1) > base
     assert sv.workspace_size(64, 5, 151936, 1) > base
@@ -95,6 +96,8 @@ def test_counterfactual_and_cactus_validation(lib):
 
 
 def test_cluster_override_hook(lib):
-    assert lib.spec_debug_set_cluster_size(3) == -1
+    assert lib.spec_debug_set_cluster_size(17) == -1
+    assert lib.spec_debug_set_cluster_size(-1) == -1
+    assert lib.spec_debug_set_cluster_size(12) == 0
     assert lib.spec_debug_set_cluster_size(8) == 0
     assert lib.spec_debug_set_cluster_size(0) == 0
