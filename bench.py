@@ -143,18 +143,56 @@ def max_over_ranks(pg, torch, v, device):
 # ------------------------------------------------------------------------------------------------
 # CPU oracle timing (reference arm and cpu_baseline)
 # ------------------------------------------------------------------------------------------------
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one row-kernel launch, from an ncu capture of
+# this benchmark's own command (profiles/), keyed by a hash of the kernel sources it was taken with: when the
+# sources change the recorded number no longer applies and the JSON line reports null.
+RECORDED_TRAFFIC = {
+    "da891611c878ba80": {"sps_llama3_b64_k5": 261182720 + 4624384},
+}
+
+
+def kernel_source_hash():
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "speculative_decoding_verification_target_gb300", "csrc", "*.cu*"))):
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def kind_of(w):
+    """Which entry point a workload exercises: counterfactual gamma (N > 1, fused verify of the selected
+    drafter), Cactus (workloads with a delta list; the largest delta is timed) or standard verification."""
+    if w.N > 1:
+        return "counterfactual"
+    if w.deltas:
+        return "cactus"
+    return "verify"
+
+
 def time_oracle(w, inp_host, n_seq, repeats=1):
     import oracle
     sel = np.arange(n_seq)
     t = workloads.to_numpy_logits(inp_host["target"][:n_seq])
-    d = workloads.to_numpy_logits(inp_host["draft"][:n_seq])
     tok = inp_host["tokens"][:n_seq].numpy()
     seeds = inp_host["seeds"][:n_seq].numpy().astype(np.uint64)
+    kind = kind_of(w)
+    if kind == "counterfactual":
+        d = workloads.to_numpy_logits(inp_host["drafters"][:, :n_seq])
+    else:
+        d = workloads.to_numpy_logits(inp_host["draft"][:n_seq])
     oracle.build()
     cores = os.cpu_count() or 1
     t0 = time.perf_counter()
     for _ in range(repeats):
-        oracle.verify(t, d, tok, seeds, w.temperature, seq_index=sel, nthreads=cores)
+        if kind == "counterfactual":
+            oracle.counterfactual(t, d, w.temperature, w.selected, tok, seeds, seq_index=sel, nthreads=cores)
+        elif kind == "cactus":
+            oracle.cactus(t, d, tok, seeds, max(w.deltas), w.temperature, seq_index=sel, nthreads=cores)
+        else:
+            oracle.verify(t, d, tok, seeds, w.temperature, seq_index=sel, nthreads=cores)
     dt = (time.perf_counter() - t0) / repeats
     return n_seq * w.K / dt, dt, cores
 
@@ -204,15 +242,29 @@ def run_ours(args, w):
     ring = min(ring, args.max_ring)
     batches = [workloads.make(w.scaled(gen_seed=w.gen_seed + 101 * i + 7919 * rank), device=dev)
                for i in range(ring)]
-    ws = sv.new_workspace(w.B, w.K, w.V, 1, dev)
+    kind = kind_of(w)
+    ws = sv.new_workspace(w.B, w.K, w.V, w.N, dev)
     acc = torch.empty(w.B, dtype=torch.int32, device=dev)
     outt = torch.empty((w.B, w.K + 1), dtype=torch.int32, device=dev)
+    gam = torch.empty((w.N, w.B, w.K), dtype=torch.float32, device=dev) if kind == "counterfactual" else None
     stream = torch.cuda.current_stream(dev)
+    # kernels per call: the row kernel and the chain-finish kernel, plus the gamma reduction for gamma calls
+    launches_per_call = 3 if kind == "counterfactual" else 2
+
+    def call(bt, s=None):
+        if kind == "counterfactual":
+            sv.counterfactual_gamma(bt["target"], bt["drafters"], w.temperature, w.selected, bt["tokens"],
+                                    bt["seeds"], gamma=gam, want_loss=False, accept_len=acc, out_tokens=outt,
+                                    want_diag=False, workspace=ws, stream=s)
+        elif kind == "cactus":
+            sv.cactus_verify(bt["target"], bt["draft"], bt["tokens"], bt["seeds"], max(w.deltas), w.temperature,
+                             accept_len=acc, out_tokens=outt, want_diag=False, workspace=ws, stream=s)
+        else:
+            sv.verify(bt["target"], bt["draft"], bt["tokens"], bt["seeds"], w.temperature, accept_len=acc,
+                      out_tokens=outt, want_diag=False, workspace=ws, stream=s)
 
     def step(i):
-        bt = batches[i % ring]
-        sv.verify(bt["target"], bt["draft"], bt["tokens"], bt["seeds"], w.temperature, accept_len=acc,
-                  out_tokens=outt, want_diag=False, workspace=ws)
+        call(batches[i % ring])
 
     for i in range(args.warmup):
         step(i)
@@ -247,24 +299,28 @@ def run_ours(args, w):
     eager_ms = e_start.elapsed_time(e_stop) / args.steps
     status = sv.read_status(ws)
 
-    # end to end through the public call: pinned host inputs -> device, verify, results -> host
+    # end to end through the public call: pinned host inputs -> device, the call, results -> host
     hb = batches[0]
-    host_in = {k: hb[k].to("cpu").pin_memory() for k in ("target", "draft", "tokens", "seeds")}
+    in_keys = ("target", "drafters" if kind == "counterfactual" else "draft", "tokens", "seeds")
+    host_in = {k: hb[k].to("cpu").pin_memory() for k in in_keys}
     dev_in = {k: torch.empty_like(hb[k]) for k in host_in}
     host_out = {"accept_len": torch.empty(w.B, dtype=torch.int32).pin_memory(),
                 "out_tokens": torch.empty((w.B, w.K + 1), dtype=torch.int32).pin_memory()}
+    if gam is not None:
+        host_out["gamma"] = torch.empty(tuple(gam.shape), dtype=torch.float32).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
     d2h = sum(v.numel() * v.element_size() for v in host_out.values())
 
     def e2e_step():
         for k in host_in:
             dev_in[k].copy_(host_in[k], non_blocking=True)
-        sv.verify(dev_in["target"], dev_in["draft"], dev_in["tokens"], dev_in["seeds"], w.temperature,
-                  accept_len=acc, out_tokens=outt, want_diag=False, workspace=ws, stream=stream)
+        call(dev_in, stream)
         host_out["accept_len"].copy_(acc, non_blocking=True)
         host_out["out_tokens"].copy_(outt, non_blocking=True)
+        if gam is not None:
+            host_out["gamma"].copy_(gam, non_blocking=True)
 
-    e2e_steps = max(3, min(args.steps, 20))
+    e2e_steps = max(3, min(args.steps, 20 if batch_bytes < (2 << 30) else 3))
     for _ in range(2):
         e2e_step()
     barrier(pg, torch)
@@ -290,23 +346,28 @@ def run_ours(args, w):
         "dtype": "bf16" if w.dtype == "bf16" else "fp32", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "K": w.K, "V": w.V, "N": w.N, "temperature": w.temperature,
                    "positions_per_step_per_gpu": w.positions, "bytes_per_step_per_gpu": batch_bytes,
+                   "entry_point": {"verify": "spec_verify", "cactus": "spec_cactus_verify (delta %g)" % max(
+                       w.deltas or (0.0,)), "counterfactual": "spec_counterfactual_gamma (N %d, fused verify "
+                       "of drafter %d)" % (w.N, w.selected)}[kind],
                    "l2": "inputs larger than L2: ring of %d distinct batches (%.0f MB) > 129 MB L2" % (
                        ring, ring * batch_bytes / 1e6),
                    "parallelism": "replicas over sequences" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None, "peak_kind": peak_kind,
-                     "kernel": "rows_kernel + chain-finish kernel: one whole verify call (graph replay timed "
-                               "with CUDA events on the launching stream, divided by the steps)",
+                     "traffic": RECORDED_TRAFFIC.get(kernel_source_hash(), {}).get(w.name), "peak_kind": peak_kind,
+                     "kernel": "rows_kernel (+ the small chain-finish%s kernel): one whole %s call, graph replay "
+                               "timed with CUDA events on the launching stream, divided by the steps" % (
+                                   " and gamma-reduction" if kind == "counterfactual" else "", kind),
                      "avg_call_us": avg_call_s * 1e6, "eager_call_us": eager_ms * 1e3,
                      "frac_of_8tbs_nominal": achieved / 8000.0},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms / e2e_steps},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": launches_per_call * args.steps,
         "clocks": clocks.summary(),
         "device_status": status,
     }
     if not args.no_cpu_baseline:
-        host = {k: batches[0][k].to("cpu") for k in ("target", "draft", "tokens", "seeds")}
+        host = {k: batches[0][k].to("cpu") for k in ("target", "drafters" if kind == "counterfactual" else "draft",
+                                                       "tokens", "seeds")}
         n_seq = min(w.B, args.cpu_sequences)
         reps, total_dt = 0, 0.0
         while total_dt < args.cpu_seconds and reps < 1000:

@@ -25,7 +25,7 @@
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream). Calls are asynchronous:
  *    they enqueue kernels and return without synchronising.
  *  - Uniforms: Philox4x32-10 (Salmon et al., SC'11) with key = seeds[b] (low word, high word) and counter
- *    (position j, sequence b, stream, 0); output word 0 maps to ((w >> 8) + 0.5) * 2^-24. Stream 0 gives
+ *    (position j, sequence b, stream, 0); output word 0 maps to ((w >> 9) + 0.5) * 2^-23. Stream 0 gives
  *    the accept uniform r of position j; stream 1 gives the resample uniform u of position j (or of the
  *    bonus row at j = K).
  *  - Inverse CDF in ascending token id: the emitted token is the smallest x whose running mass exceeds
