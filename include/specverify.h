@@ -113,6 +113,28 @@ spec_status spec_cactus_verify(const void* target_logits, const void* draft_logi
                                float* diag, float* gamma_star, void* workspace, size_t workspace_bytes,
                                void* stream);
 
+/* spec_verify for callers that cannot allocate device memory: same inputs, outputs and semantics, but no
+ * workspace argument. Some callers run where allocation is not allowed or not possible: inside a memory
+ * budget fixed in advance, under an allocator that must not grow, or from code that has no allocator at all.
+ * The pages have no counterpart of this entry point; it only changes where the scratch lives.
+ *  - Scratch: a fixed 32 MiB region of device memory inside the library (one per device, part of the loaded
+ *    library image). A call whose workspace would exceed it (spec_workspace_size(B, K, V, 1) > 32 MiB)
+ *    returns SPEC_ERR_UNSUPPORTED before any CUDA call; spec_verify with a caller workspace has no such
+ *    limit.
+ *  - The first call on each device looks the region's address up (cudaGetSymbolAddress, with that device
+ *    current); make it before any stream capture.
+ *  - The region's first word is the status word, the only part that must start at zero: the region starts
+ *    zeroed, and every call clears the word on `stream` before its kernels run.
+ *  - All calls on one device share the region: calls that can overlap on the GPU (different streams, or
+ *    several host threads) race on it and give wrong results. Serialise them.
+ *  - status_out: nullable host pointer. When given, the call also waits for `stream` and stores this call's
+ *    status bits (SPEC_STATUS_*) there.
+ * Nothing is allocated: no cudaMalloc, no allocating library routine. */
+spec_status spec_verify_static(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                               const int32_t* draft_tokens, const uint64_t* seeds, int B, int K, int V,
+                               float temperature, int32_t* accept_len, int32_t* out_tokens, float* diag,
+                               uint32_t* status_out, void* stream);
+
 /* Copies the workspace status word to *status_out (host), synchronising `stream`. */
 spec_status spec_read_status(const void* workspace, uint32_t* status_out, void* stream);
 

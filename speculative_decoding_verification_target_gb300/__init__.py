@@ -21,7 +21,7 @@ SPEC_OK, SPEC_ERR_INVALID, SPEC_ERR_CUDA, SPEC_ERR_UNSUPPORTED = 0, 1, 2, 3
 STATUS_BAD_TOKEN, STATUS_TIMEOUT = 1, 2
 EXPORTS = ("spec_workspace_size", "spec_verify", "spec_counterfactual_gamma", "spec_cactus_verify",
            "spec_read_status", "spec_clear_status", "spec_last_error", "spec_debug_set_cluster_size",
-           "spec_debug_last_plan")
+           "spec_debug_last_plan", "spec_verify_static")
 
 _lib = None
 
@@ -66,6 +66,8 @@ def load(build_if_missing: bool = False):
     lib.spec_debug_set_cluster_size.restype = I
     lib.spec_debug_last_plan.argtypes = [ctypes.POINTER(ctypes.c_int)]
     lib.spec_debug_last_plan.restype = I
+    lib.spec_verify_static.argtypes = [P, P, I, P, P, I, I, I, F, P, P, P, ctypes.POINTER(ctypes.c_uint32), P]
+    lib.spec_verify_static.restype = I
     _lib = lib
     return lib
 

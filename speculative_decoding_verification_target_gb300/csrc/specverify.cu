@@ -356,6 +356,32 @@ spec_status check_common(const void* target, const void* others, spec_dtype dtyp
     return SPEC_OK;
 }
 
+// Scratch for spec_verify_static: one fixed region per device, part of the library image (static storage,
+// so it starts zeroed). Its address is looked up once per device.
+constexpr size_t STATIC_SCRATCH_BYTES = size_t(32) << 20;
+__device__ __align__(256) unsigned char g_static_scratch[STATIC_SCRATCH_BYTES];
+
+constexpr int MAX_DEVICES = 64;
+std::mutex g_static_mu;
+void* g_static_ptr[MAX_DEVICES] = {};
+
+spec_status static_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "cudaGetDevice failed: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= MAX_DEVICES) return fail(SPEC_ERR_UNSUPPORTED, "device index %d beyond %d", dev, MAX_DEVICES);
+    std::lock_guard<std::mutex> lk(g_static_mu);
+    if (!g_static_ptr[dev]) {
+        void* ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+        if (e != cudaSuccess || !ptr)
+            return fail(SPEC_ERR_CUDA, "looking up the static scratch region failed: %s", cudaGetErrorString(e));
+        g_static_ptr[dev] = ptr;
+    }
+    *out = g_static_ptr[dev];
+    return SPEC_OK;
+}
+
 }  // namespace
 }  // namespace specv
 
@@ -464,6 +490,63 @@ spec_status spec_cactus_verify(const void* target_logits, const void* draft_logi
     a.workspace_bytes = workspace_bytes;
     a.stream = static_cast<cudaStream_t>(stream);
     return run(a);
+}
+
+spec_status spec_verify_static(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                               const int32_t* draft_tokens, const uint64_t* seeds, int B, int K, int V,
+                               float temperature, int32_t* accept_len, int32_t* out_tokens, float* diag,
+                               uint32_t* status_out, void* stream) {
+    // sizes first: an oversized call is refused before any CUDA call
+    if (B >= 0 && K >= 1 && K <= MAX_K && V >= 1 && V <= MAX_V) {
+        const size_t need = spec_workspace_size(B, K, V, 1);
+        if (need > STATIC_SCRATCH_BYTES)
+            return fail(SPEC_ERR_UNSUPPORTED,
+                        "B=%d K=%d V=%d needs %zu bytes of scratch; the static region holds %zu (use spec_verify with "
+                        "a caller workspace)", B, K, V, need, STATIC_SCRATCH_BYTES);
+    }
+    if (dtype != SPEC_BF16 && dtype != SPEC_FP32) return fail(SPEC_ERR_INVALID, "unknown dtype %d", static_cast<int>(dtype));
+    if (B < 0) return fail(SPEC_ERR_INVALID, "B must be >= 0 (got %d)", B);
+    if (K < 1 || K > MAX_K) return fail(SPEC_ERR_INVALID, "K must be in [1, %d] (got %d)", MAX_K, K);
+    if (V < 1 || V > MAX_V) return fail(SPEC_ERR_INVALID, "V must be in [1, %d] (got %d)", MAX_V, V);
+    if (std::isnan(temperature) || std::isinf(temperature) || temperature < 0.f)
+        return fail(SPEC_ERR_INVALID, "temperature must be finite and > 0 (got %g)", static_cast<double>(temperature));
+    if (temperature == 0.f) return fail(SPEC_ERR_UNSUPPORTED, "temperature 0 (greedy) is not supported");
+    if (B == 0) return SPEC_OK;
+    if (!target_logits || !draft_logits) return fail(SPEC_ERR_INVALID, "logits pointers must not be NULL");
+    spec_status s = SPEC_OK;
+    if (!draft_tokens || !seeds || !accept_len || !out_tokens)
+        return fail(SPEC_ERR_INVALID, "draft_tokens, seeds, accept_len and out_tokens must not be NULL");
+    void* scratch = nullptr;
+    s = static_scratch(&scratch);
+    if (s != SPEC_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // the status word is the only part of the scratch that must start at zero
+    cudaError_t e = cudaMemsetAsync(scratch, 0, sizeof(uint32_t), st);
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "status clear failed: %s", cudaGetErrorString(e));
+    Call a = {};
+    a.target = target_logits;
+    a.others = draft_logits;
+    a.dtype = dtype;
+    a.tokens = draft_tokens;
+    a.seeds = seeds;
+    a.B = B;
+    a.K = K;
+    a.V = V;
+    a.N = 1;
+    a.selected = 0;
+    a.temperature = temperature;
+    a.accept_len = accept_len;
+    a.out_tokens = out_tokens;
+    a.diag = diag;
+    a.workspace = scratch;
+    a.workspace_bytes = STATIC_SCRATCH_BYTES;
+    a.stream = st;
+    s = run(a);
+    if (s != SPEC_OK || !status_out) return s;
+    e = cudaMemcpyAsync(status_out, scratch, sizeof(uint32_t), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "status read failed: %s", cudaGetErrorString(e));
+    return SPEC_OK;
 }
 
 spec_status spec_read_status(const void* workspace, uint32_t* status_out, void* stream) {

@@ -101,3 +101,20 @@ def test_cluster_override_hook(lib):
     assert lib.spec_debug_set_cluster_size(12) == 0
     assert lib.spec_debug_set_cluster_size(8) == 0
     assert lib.spec_debug_set_cluster_size(0) == 0
+
+
+def test_static_scratch_entry_refuses_oversized_calls_without_a_gpu(lib):
+    # the static-scratch variant checks its size limit before any CUDA call
+    P = ctypes.c_void_p
+    good = P(1 << 20)
+    st = ctypes.c_uint32(0)
+    rc = lib.spec_verify_static(good, good, 0, good, good, 4096, 64, 262144, ctypes.c_float(1.0), good, good, None,
+                                ctypes.byref(st), None)
+    assert rc == 3
+    assert b"static region" in lib.spec_last_error()
+    rc = lib.spec_verify_static(None, None, 0, None, None, 0, 5, 1000, ctypes.c_float(1.0), None, None, None, None,
+                                None)
+    assert rc == 0   # B = 0 is a no-op
+    rc = lib.spec_verify_static(good, good, 0, good, good, 2, 0, 1000, ctypes.c_float(1.0), good, good, None, None,
+                                None)
+    assert rc == 1
