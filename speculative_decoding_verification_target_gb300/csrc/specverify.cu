@@ -237,6 +237,8 @@ spec_status run(const Call& a) {
     k.target = static_cast<const unsigned char*>(a.target);
     k.others = static_cast<const unsigned char*>(a.others);
     k.tokens = chain ? a.tokens : nullptr;
+    k.seeds = chain ? a.seeds : nullptr;
+    k.all_residuals = a.diag ? 1 : 0;
     k.B = a.B;
     k.K = a.K;
     k.V = a.V;

@@ -75,6 +75,8 @@ struct KParams {
     const unsigned char* target;   // [B, K+1, V]
     const unsigned char* others;   // [N, B, K, V]
     const int32_t* tokens;         // [B, K] (null: gamma only)
+    const uint64_t* seeds;         // [B] (with tokens)
+    int all_residuals;             // 1: residual masses for every position (diag wants Z everywhere)
     int B, K, V, N;
     int selected;                  // drafter whose chain is verified (processed last); -1: none
     int BK;                        // B * K: items below BK are (b, j < K), the rest are bonus rows
@@ -486,7 +488,7 @@ __device__ __forceinline__ float piece_mass(int mode, const typename E::Raw (&rt
 //   full[W * R], tfull[2], tempty[2], lbar[NXB], cbar[NXB], sbar[NXB]   mbarriers
 //   lx[NXB][W][XW]        consumer-warp partials of a unit  (max_t, sum_t, max_o, sum_o, x_t, x_o)
 //   cx[NXB][C][XW]        the CTAs' partials of a unit, written by every CTA of the cluster
-//   sc[NXB][XW]           row scalars of a unit             (bt, bo, btp, h(t))
+//   sc[NXB][XW]           row scalars of a unit             (bt, bo, btp, h(t), residual needed)
 //   abort flag
 struct Ctx {
     unsigned char* tbuf;
@@ -779,6 +781,7 @@ __device__ __forceinline__ void consumer_warp(const Ctx& x, const KParams& p, in
             ctx_wait(x, p, &x.sbar[pu % NXB], static_cast<uint32_t>((pu / NXB) & 1));
             const float* sp = x.sc + (pu % NXB) * XW;
             const float bt = sp[0], bo = sp[1], btp = sp[2], ht = sp[3];
+            const bool need_res = sp[4] != 0.f;   // verified row that rejects (or every row when diag is wanted)
             if (res && f0 < np) ctx_wait(x, p, &x.tfull[prev.k & 1], static_cast<uint32_t>((prev.k >> 1) & 1));
             const size_t row = static_cast<size_t>(prev.b) * (K + 1) + prev.j;
             const unsigned char* tb = x.tbuf + static_cast<size_t>(prev.k & 1) * x.tb_bytes;
@@ -792,11 +795,11 @@ __device__ __forceinline__ void consumer_warp(const Ctx& x, const KParams& p, in
                     if (res) piece_load<E>(tb + static_cast<size_t>(pc) * PE * eb, piece_chunks(x, pc), lane, rt);
                     else take(pc, rt, -1, unused);
                     take(pc, ro, -1, unused);
-                    if (ver) {
+                    if (ver && need_res) {
                         const int et = (tl >= 0 && tl / PE == pc) ? tl % PE : -1;
                         const float m = piece_mass<E>(1, rt, ro, lane, c, bt, bo, et, ht, acc);
                         if (lane == 0 && tiles) tiles[pc] = m;
-                    } else {
+                    } else if (!ver || p.gpart) {
                         piece_overlap<E>(rt, ro, c, bt, bo, acc);
                     }
                 }
@@ -903,12 +906,22 @@ __device__ __forceinline__ void reducer_warp(const Ctx& x, const KParams& p, int
         }
         const float bo = cur.n > 0 ? beta_of(go, c) : 0.f;
         const float pd = ver ? prob_of(gxo, go, c) : 0.f;
+        // The residual of a verified position is drawn from only if the position rejects. The decision is
+        // the finish kernel's own comparison on the same floats (h(t) and p_draft(t) go to the record
+        // unchanged), so an accepted position can skip its residual masses.
+        float need_residual = 1.f;
+        if (ver && !p.all_residuals && p.seeds) {
+            const float r = philox_uniform(__ldg(p.seeds + cur.b), static_cast<uint32_t>(cur.b),
+                                           static_cast<uint32_t>(cur.j), 0u);
+            need_residual = r * pd < ht ? 0.f : 1.f;
+        }
         if (lane == 0) {
             float* s = x.sc + xb * XW;
             s[0] = bt;
             s[1] = bo;
             s[2] = btp;
             s[3] = ht;
+            s[4] = need_residual;
             mbar_arrive(&x.sbar[xb]);
             if (x.rank == 0) {
                 if (cur.i == 0 && cur.j < K && p.tokens && !(cur.tok >= 0 && cur.tok < p.V))
@@ -1160,6 +1173,76 @@ __device__ int scan_pick(const FParams& f, const unsigned char* trow, const unsi
     return last_pos;
 }
 
+// The same scan over one piece of at most PE logits, with every load issued before the scan (one memory
+// latency instead of one per 256 logits). Lane l holds logits e_begin + 256 r + 8 l .. + 7 of round r.
+template <class E>
+__device__ int scan_pick_piece(const FParams& f, const unsigned char* trow, const unsigned char* orow, int mode,
+                               int e_begin, int e_end, float bt, float bo, int tok, float ht, float tp, float before,
+                               int lane) {
+    using Raw = typename E::Raw;
+    Raw rt[PCH], ro[PCH];
+#pragma unroll
+    for (int r = 0; r < PCH; ++r) {
+        const int e0 = e_begin + r * 32 * CHUNK + lane * CHUNK;
+        rt[r] = e0 < e_end ? E::gchunk(trow, e0, e_end, f.aligned) : E::ninf();
+        ro[r] = (mode == 1 && e0 < e_end) ? E::gchunk(orow, e0, e_end, f.aligned) : rt[r];
+    }
+    int last_pos = -1;
+#pragma unroll 1
+    for (int r = 0; r < PCH; ++r) {
+        const int base = e_begin + r * 32 * CHUNK;
+        if (base >= e_end) break;
+        const int e0 = base + lane * CHUNK;
+        float v[8];
+        float m = 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = 0.f;
+        Raw a = rt[0], b = ro[0];
+#pragma unroll
+        for (int q = 1; q < PCH; ++q)
+            if (q == r) {
+                a = rt[q];
+                b = ro[q];
+            }
+        if (e0 < e_end) {
+            const int et = (tok >= e0 && tok < e0 + CHUNK) ? tok - e0 : -1;
+            float ovl = 0.f;
+            chunk_values<E>(mode, a, b, f.c, bt, bo, et, ht, v, ovl);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) m += v[q];
+        }
+        const float incl = warp_incl_scan(m, lane);
+        const unsigned over = __ballot_sync(0xffffffffu, m > 0.f && before + incl > tp);
+        const unsigned posm = __ballot_sync(0xffffffffu, m > 0.f);
+        if (over) {
+            const int ln = __ffs(over) - 1;
+            int pick = -1;
+            if (lane == ln) {
+                float acc = before + incl - m;
+                int lp = -1;
+                for (int q = 0; q < 8; ++q) {
+                    acc += v[q];
+                    if (v[q] > 0.f) {
+                        lp = q;
+                        if (pick < 0 && acc > tp) pick = q;
+                    }
+                }
+                pick = e0 + (pick >= 0 ? pick : lp);
+            }
+            return __shfl_sync(0xffffffffu, pick, ln);
+        }
+        if (posm) {
+            const int ln = 31 - __clz(posm);
+            int lp = -1;
+            for (int q = 0; q < 8; ++q)
+                if (v[q] > 0.f) lp = q;
+            last_pos = __shfl_sync(0xffffffffu, e0 + lp, ln);
+        }
+        before = __shfl_sync(0xffffffffu, before + incl, 31);
+    }
+    return last_pos;
+}
+
 template <class E>
 __global__ void __launch_bounds__(256) finish_kernel(const FParams f) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -1256,7 +1339,8 @@ __global__ void __launch_bounds__(256) finish_kernel(const FParams f) {
         if (ft >= 0) {
             int e_begin = 0, len = 0;
             fp_piece(f, row, ft, &e_begin, &len);
-            emitted = scan_pick<E>(f, trow, orow, mode, e_begin, e_begin + len, bt, bo, tok, ht, tp, before_piece, lane);
+            emitted = scan_pick_piece<E>(f, trow, orow, mode, e_begin, e_begin + len, bt, bo, tok, ht, tp, before_piece,
+                                         lane);
         }
     }
 

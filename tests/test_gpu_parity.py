@@ -330,3 +330,47 @@ def test_large_pool_named_sampled():
     gam = out["gamma"].cpu().numpy()
     assert np.all((gam > 0) & (gam <= 1.0 + 1e-6))
     assert np.all(np.diff(gam.mean(axis=(1, 2))) < 0.05)   # larger drafter noise, lower acceptance (on average)
+
+
+# ------------------------------------------------------------------------------------------------
+# without diag the row pass skips the residual masses of accepted positions; the outputs must not change
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("V,B,K,C", [(5000, 16, 6, 0), (50000, 12, 5, 4), (128256, 24, 5, 0)])
+def test_verify_without_diag_matches(V, B, K, C):
+    sv.set_cluster_size(C)
+    w = small(V, B=B, K=K, sigma=1.0)
+    g = to_device(workloads.make(w))
+    full = sv.verify(g["target"], g["draft"], g["tokens"], g["seeds"], w.temperature)
+    lean = sv.verify(g["target"], g["draft"], g["tokens"], g["seeds"], w.temperature, want_diag=False)
+    torch.cuda.synchronize()
+    assert torch.equal(full["accept_len"], lean["accept_len"])
+    assert torch.equal(full["out_tokens"], lean["out_tokens"])
+    acc = full["accept_len"].cpu().numpy()
+    assert 0 < acc.mean() < K   # both accepted and rejected positions occur
+    ref = oracle_verify(workloads.make(w))
+    assert_chain(lean, ref, w.K)
+
+
+@pytest.mark.parametrize("delta", [0.0, 1.0])
+def test_cactus_without_diag_matches(delta):
+    w = small(20000, B=16, K=8, sigma=2.0)
+    g = to_device(workloads.make(w))
+    full = sv.cactus_verify(g["target"], g["draft"], g["tokens"], g["seeds"], delta, w.temperature)
+    lean = sv.cactus_verify(g["target"], g["draft"], g["tokens"], g["seeds"], delta, w.temperature, want_diag=False)
+    torch.cuda.synchronize()
+    assert torch.equal(full["accept_len"], lean["accept_len"])
+    assert torch.equal(full["out_tokens"], lean["out_tokens"])
+
+
+def test_counterfactual_without_diag_matches():
+    w = small(33333, B=8, K=5, sigmas=(0.7, 1.5, 3.0), selected=1)
+    g = to_device(workloads.make(w))
+    full = sv.counterfactual_gamma(g["target"], g["drafters"], w.temperature, w.selected, g["tokens"], g["seeds"])
+    lean = sv.counterfactual_gamma(g["target"], g["drafters"], w.temperature, w.selected, g["tokens"], g["seeds"],
+                                   want_diag=False)
+    torch.cuda.synchronize()
+    assert torch.equal(full["accept_len"], lean["accept_len"])
+    assert torch.equal(full["out_tokens"], lean["out_tokens"])
+    # accepted positions of the selected drafter take the overlap-only pass 2 (h(t) unpatched): same gamma
+    # up to rounding
+    assert (full["gamma"] - lean["gamma"]).abs().max().item() <= 1e-6
