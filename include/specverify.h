@@ -20,8 +20,8 @@
  *
  * Conventions for every call:
  *  - Tensor pointers are DEVICE memory owned by the caller, contiguous, row-major. Logits are bf16 or fp32
- *    (spec_dtype). The library allocates nothing; it reads the logits once and writes only the outputs and
- *    the caller's workspace.
+ *    (spec_dtype). The library allocates nothing; it reads every logit once (plus, for the draw of each
+ *    sequence, the one row pair it draws from) and writes only the outputs and the caller's workspace.
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream). Calls are asynchronous:
  *    they enqueue kernels and return without synchronising.
  *  - Uniforms: Philox4x32-10 (Salmon et al., SC'11) with key = seeds[b] (low word, high word) and counter
@@ -144,14 +144,23 @@ spec_status spec_clear_status(void* workspace, void* stream);
 /* Thread-local message describing the last non-OK status returned on this thread. */
 const char* spec_last_error(void);
 
-/* Tuning and test hook: forces the number of CTAs that split one vocabulary row (1 to 16; 0 restores the
- * automatic choice). Process-wide, not thread-safe; results do not depend on it beyond floating-point
- * summation order. Returns 0, or -1 for an unsupported value. */
+/* Tuning and test hook: forces the number of CTAs that split one vocabulary row in the fused row kernel of
+ * spec_counterfactual_gamma (1 to 16; 0 restores the automatic choice). Process-wide, not thread-safe;
+ * results do not depend on it beyond floating-point summation order. Returns 0, or -1 for an unsupported
+ * value. */
 int spec_debug_set_cluster_size(int C);
 
-/* Tuning and test hook: the launch plan of the last call made on this thread, as five ints: cluster size C,
- * shared-memory stages per CTA, clusters launched, resident-target mode (0/1), pieces per CTA slice.
- * out5 is host memory. Returns 0, or -1 for a NULL pointer. */
+/* Tuning and test hook: forces the number of CTAs of the statistics pass of spec_verify, spec_verify_cactus
+ * and spec_verify_static (1 to 1024; 0 restores the automatic choice, every SM once). The grid fixes how
+ * the rows are cut into per-warp segments, so results depend on it only through floating-point summation
+ * order. Process-wide, not thread-safe. Returns 0, or -1 for an unsupported value. */
+int spec_debug_set_stats_grid(int ctas);
+
+/* Tuning and test hook: the launch plan of the last call made on this thread, as five ints. Fused row
+ * kernel (spec_counterfactual_gamma): cluster size C, shared-memory stages per consumer warp, clusters
+ * launched, resident-target mode (0/1), pieces per CTA slice. Statistics pass (the other entry points):
+ * 0, ring slots per warp, CTAs launched, 0, pieces per row. out5 is host memory. Returns 0, or -1 for a
+ * NULL pointer. */
 int spec_debug_last_plan(int* out5);
 
 #ifdef __cplusplus

@@ -21,7 +21,7 @@ SPEC_OK, SPEC_ERR_INVALID, SPEC_ERR_CUDA, SPEC_ERR_UNSUPPORTED = 0, 1, 2, 3
 STATUS_BAD_TOKEN, STATUS_TIMEOUT = 1, 2
 EXPORTS = ("spec_workspace_size", "spec_verify", "spec_counterfactual_gamma", "spec_cactus_verify",
            "spec_read_status", "spec_clear_status", "spec_last_error", "spec_debug_set_cluster_size",
-           "spec_debug_last_plan", "spec_verify_static")
+           "spec_debug_last_plan", "spec_verify_static", "spec_debug_set_stats_grid")
 
 _lib = None
 
@@ -64,6 +64,8 @@ def load(build_if_missing: bool = False):
     lib.spec_last_error.restype = ctypes.c_char_p
     lib.spec_debug_set_cluster_size.argtypes = [I]
     lib.spec_debug_set_cluster_size.restype = I
+    lib.spec_debug_set_stats_grid.argtypes = [I]
+    lib.spec_debug_set_stats_grid.restype = I
     lib.spec_debug_last_plan.argtypes = [ctypes.POINTER(ctypes.c_int)]
     lib.spec_debug_last_plan.restype = I
     lib.spec_verify_static.argtypes = [P, P, I, P, P, I, I, I, F, P, P, P, ctypes.POINTER(ctypes.c_uint32), P]
@@ -126,9 +128,15 @@ def clear_status(ws, stream=None):
 
 
 def set_cluster_size(C: int):
-    """Tuning / test hook: CTAs per vocabulary row (0 = automatic)."""
+    """Tuning / test hook: CTAs per vocabulary row of the fused counterfactual kernel (0 = automatic)."""
     if load().spec_debug_set_cluster_size(int(C)) != 0:
         raise ValueError("unsupported cluster size %r" % C)
+
+
+def set_stats_grid(ctas: int):
+    """Tuning / test hook: CTAs of the statistics pass of verify / cactus_verify (0 = automatic)."""
+    if load().spec_debug_set_stats_grid(int(ctas)) != 0:
+        raise ValueError("unsupported statistics grid %r" % ctas)
 
 
 def last_plan() -> dict:

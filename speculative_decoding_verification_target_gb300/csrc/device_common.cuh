@@ -143,6 +143,12 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
         : "memory");
 }
 
+// Bulk prefetch of [src, src + bytes) into L2 (no completion to wait for). src 16-byte aligned, bytes a
+// multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -188,6 +194,12 @@ __device__ __forceinline__ void st_cluster_f32x4(uint32_t addr, float a, float b
     asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c),
                  "f"(d)
                  : "memory");
+}
+// Load of a float from the shared memory of a CTA of the cluster (address from map_to_rank).
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
 }
 // Full cluster barrier; release/acquire orders the shared::cluster stores issued before it.
 __device__ __forceinline__ void cluster_sync_all() {

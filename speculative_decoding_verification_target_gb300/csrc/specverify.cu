@@ -8,7 +8,7 @@
 #include <mutex>
 
 #include "specverify.h"
-#include "specverify_kernels.cuh"
+#include "specverify_chain.cuh"
 
 namespace specv {
 namespace {
@@ -30,6 +30,7 @@ constexpr size_t WS_HEADER = 256;          // status word + padding
 constexpr int SMEM_MAX_PER_CTA = 232448;   // opt-in maximum per CTA
 
 int g_cluster_override = 0;   // test / tuning hook (0 = automatic)
+int g_stats_grid_override = 0;   // CTAs of the statistics kernel (0 = automatic)
 thread_local int g_last_plan[5] = {0, 0, 0, 0, 0};   // C, S, clusters launched, resident, pieces per slice
 
 struct Plan {
@@ -175,9 +176,10 @@ spec_status make_plan(KernelFn fn, int V, int eb, int N, int BK, int B_bonus, bo
 }
 
 // Workspace layout: [status header][records B*(K+1)*REC][piece masses B*(K+1)*pieces_row][gamma partials
-// N*B*K*16*W]. The per-row regions are sized for the largest cluster split so that any plan fits.
+// N*B*K*16*W][segment partials of the statistics pass]. The per-row regions are sized for the largest
+// cluster split so that any plan fits; the segment region for the largest statistics grid.
 struct WsLayout {
-    size_t rec_off, tiles_off, gpart_off, total;
+    size_t rec_off, tiles_off, gpart_off, part_off, total;
     int tiles_row;   // floats per row in the piece-mass region (>= C * pcap for every plan)
     int gpart_row;   // floats per (drafter, b, j) in the gamma region (>= C * W)
 };
@@ -192,7 +194,14 @@ WsLayout ws_layout(int B, int K, int V, int N) {
     w.rec_off = WS_HEADER;
     w.tiles_off = w.rec_off + rows * REC * sizeof(float);
     w.gpart_off = w.tiles_off + rows * static_cast<size_t>(tiles_row) * sizeof(float);
-    w.total = w.gpart_off + static_cast<size_t>(N) * B * K * static_cast<size_t>(w.gpart_row) * sizeof(float);
+    w.part_off = w.gpart_off + static_cast<size_t>(N) * B * K * static_cast<size_t>(w.gpart_row) * sizeof(float);
+    w.part_off = (w.part_off + 15) / 16 * 16;   // float2 entries
+    // segment (warp g, row r) of the statistics pass at entry g + r: fewer than min(G, pieces) + rows entries
+    const long long srows = static_cast<long long>(B) * (2 * K + 1);
+    const long long pieces = srows * ((V + PE - 1) / PE);
+    const long long gmax = static_cast<long long>(S_MAX_CTAS) * SW;
+    w.total = w.part_off + static_cast<size_t>(std::min(pieces, gmax) + srows) * sizeof(float2);
+    w.total = (w.total + 15) / 16 * 16;
     return w;
 }
 
@@ -216,6 +225,168 @@ struct Call {
     cudaStream_t stream;
 };
 
+// CTAs of the statistics kernel resident at once (occupancy x SMs, cached per device and shared memory).
+using StatsFn = void (*)(const SParams);
+std::mutex g_socc_mu;
+struct SOccEntry {
+    StatsFn fn;
+    size_t smem;
+    int device, ctas;
+};
+SOccEntry g_socc[16];
+int g_socc_n = 0;
+
+cudaError_t stats_ctas(StatsFn fn, size_t smem, int& out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    {
+        std::lock_guard<std::mutex> lk(g_socc_mu);
+        for (int i = 0; i < g_socc_n; ++i)
+            if (g_socc[i].fn == fn && g_socc[i].smem == smem && g_socc[i].device == dev) {
+                out = g_socc[i].ctas;
+                return cudaSuccess;
+            }
+    }
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX_PER_CTA);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0, sms = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, SNT, smem);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1 || sms < 1) return cudaErrorInvalidConfiguration;
+    out = std::min(per_sm * sms, S_MAX_CTAS);
+    std::lock_guard<std::mutex> lk(g_socc_mu);
+    if (g_socc_n < 16) g_socc[g_socc_n++] = {fn, smem, dev, out};
+    return cudaSuccess;
+}
+
+// Raises the dynamic shared-memory ceiling of a draw kernel once per device (its chunk masses need up to
+// 128 KB).
+std::mutex g_dsm_mu;
+struct DsmEntry {
+    const void* fn;
+    int device;
+};
+DsmEntry g_dsm[32];
+int g_dsm_n = 0;
+
+template <class Fn>
+cudaError_t draw_smem_ceiling(Fn fn, int dev) {
+    std::lock_guard<std::mutex> lk(g_dsm_mu);
+    for (int i = 0; i < g_dsm_n; ++i)
+        if (g_dsm[i].fn == reinterpret_cast<const void*>(fn) && g_dsm[i].device == dev) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX_PER_CTA - 8192);
+    if (e == cudaSuccess && g_dsm_n < 32) g_dsm[g_dsm_n++] = {reinterpret_cast<const void*>(fn), dev};
+    return e;
+}
+
+// Chain verification of one drafter (standard and Cactus): statistics pass over every row, then one cluster
+// per sequence for the chain and its draw (specverify_chain.cuh).
+spec_status run_chain(const Call& a, bool aligned) {
+    const int eb = a.dtype == SPEC_BF16 ? 2 : 4;
+    const WsLayout wl = ws_layout(a.B, a.K, a.V, a.N);
+    unsigned char* ws = static_cast<unsigned char*>(a.workspace);
+    SParams s = {};
+    s.rows_a = static_cast<const unsigned char*>(a.target);
+    s.rows_b = static_cast<const unsigned char*>(a.others);
+    s.rows_a_n = static_cast<long long>(a.B) * (a.K + 1);
+    s.rows_n = s.rows_a_n + static_cast<long long>(a.B) * a.K;
+    s.V = a.V;
+    s.np = (a.V + PE - 1) / PE;
+    s.P = s.rows_n * s.np;
+    s.c = static_cast<float>(1.4426950408889634 / static_cast<double>(a.temperature));
+    s.tma = aligned ? 1 : 0;
+    const size_t slot_bytes = static_cast<size_t>(PE) * eb;
+    int R = S_MAX_R;
+    while (R > 1 && static_cast<size_t>(SW) * R * (slot_bytes + 8) > static_cast<size_t>(SMEM_MAX_PER_CTA)) --R;
+    s.R = R;
+    const size_t smem = s.tma ? static_cast<size_t>(SW) * R * (slot_bytes + 8) : 0;
+    StatsFn sfn = a.dtype == SPEC_BF16 ? stats_kernel<Bf16> : stats_kernel<F32>;
+    int ctas = 0;
+    cudaError_t e = stats_ctas(sfn, smem, ctas);
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "occupancy query failed: %s", cudaGetErrorString(e));
+    if (g_stats_grid_override > 0) ctas = g_stats_grid_override;
+    const long long need = (s.P + SW - 1) / SW;   // no more warps than pieces
+    if (ctas > need) ctas = static_cast<int>(need);
+    s.G = ctas * SW;
+    s.part = reinterpret_cast<float2*>(ws + wl.part_off);
+    s.status = reinterpret_cast<unsigned*>(ws);
+    g_last_plan[0] = 0;
+    g_last_plan[1] = R;
+    g_last_plan[2] = ctas;
+    g_last_plan[3] = 0;
+    g_last_plan[4] = s.np;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
+    cfg.blockDim = dim3(SNT, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = a.stream;
+    e = cudaLaunchKernelEx(&cfg, sfn, s);
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "statistics kernel launch failed: %s", cudaGetErrorString(e));
+
+    DParams d = {};
+    d.target = s.rows_a;
+    d.draft = s.rows_b;
+    d.part = s.part;
+    d.P = s.P;
+    d.G = s.G;
+    d.np = s.np;
+    d.rows_a_n = s.rows_a_n;
+    d.tokens = a.tokens;
+    d.seeds = a.seeds;
+    d.B = a.B;
+    d.K = a.K;
+    d.V = a.V;
+    d.c = s.c;
+    d.delta = a.delta;
+    d.cactus = a.cactus;
+    d.accept_len = a.accept_len;
+    d.out_tokens = a.out_tokens;
+    d.diag = a.diag;
+    d.gamma_star = a.gamma_star;
+    d.status = s.status;
+    // CTAs per sequence: the largest power of two up to D_MAX_CPS that keeps the grid within one CTA per SM
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    int cps = 1;
+    while (cps < D_MAX_CPS && static_cast<long long>(a.B) * cps * 2 <= sms) cps *= 2;
+    d.cps = cps;
+    // chunk masses, plus (bulk-copy mode) a two-piece slot and an mbarrier per warp when they fit
+    const size_t cm_bytes = static_cast<size_t>((s.np + cps - 1) / cps) * D_CPP * sizeof(float);
+    const size_t ring_bytes = static_cast<size_t>(DW) * (2 * static_cast<size_t>(PE) * eb + sizeof(uint64_t));
+    const size_t dsmem_cap = SMEM_MAX_PER_CTA - 8192;   // the ceiling draw_smem_ceiling sets
+    d.tma = aligned && cm_bytes + ring_bytes <= dsmem_cap ? 1 : 0;
+    const size_t dsmem = cm_bytes + (d.tma ? ring_bytes : 0);
+    using DrawFn = void (*)(const DParams);
+    DrawFn dfn = a.dtype == SPEC_BF16 ? (aligned ? draw_kernel<Bf16, true> : draw_kernel<Bf16, false>)
+                                      : (aligned ? draw_kernel<F32, true> : draw_kernel<F32, false>);
+    e = draw_smem_ceiling(dfn, dev);
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "draw kernel attribute failed: %s", cudaGetErrorString(e));
+    // launched with programmatic stream serialisation: its CTAs start as the grid above frees SMs and wait
+    // for it (griddepcontrol.wait) after reading their inputs
+    cudaLaunchAttribute da[2];
+    da[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    da[0].val.programmaticStreamSerializationAllowed = 1;
+    da[1].id = cudaLaunchAttributeClusterDimension;
+    da[1].val.clusterDim.x = static_cast<unsigned>(cps);
+    da[1].val.clusterDim.y = 1;
+    da[1].val.clusterDim.z = 1;
+    cudaLaunchConfig_t dc = {};
+    dc.gridDim = dim3(static_cast<unsigned>(a.B * cps), 1, 1);
+    dc.blockDim = dim3(DNT, 1, 1);
+    dc.dynamicSmemBytes = dsmem;
+    dc.stream = a.stream;
+    dc.attrs = da;
+    dc.numAttrs = 2;
+    e = cudaLaunchKernelEx(&dc, dfn, d);
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "draw kernel launch failed: %s", cudaGetErrorString(e));
+    return SPEC_OK;
+}
+
 spec_status run(const Call& a) {
     if (a.B == 0) return SPEC_OK;
     const int eb = a.dtype == SPEC_BF16 ? 2 : 4;
@@ -224,6 +395,7 @@ spec_status run(const Call& a) {
     // bulk copies need 16-byte aligned pieces of whole 8-logit chunks
     const bool aligned = ((reinterpret_cast<uintptr_t>(a.target) | reinterpret_cast<uintptr_t>(a.others)) & align_mask) == 0 &&
                          (static_cast<size_t>(a.V) * eb) % 16 == 0 && a.V % CHUNK == 0;
+    if (chain && a.N == 1 && !a.gamma) return run_chain(a, aligned);
     KernelFn fn = a.dtype == SPEC_BF16 ? rows_kernel<Bf16> : rows_kernel<F32>;
     const int BK = a.B * a.K;
     const int B_bonus = chain ? a.B : 0;
@@ -319,7 +491,6 @@ spec_status run(const Call& a) {
         f.C = pl.C;
         f.slice_elems = pl.slice_elems;
         f.pcap = pl.pcap;
-        f.aligned = aligned ? 1 : 0;
         f.c = k.c;
         f.accept_len = a.accept_len;
         f.out_tokens = a.out_tokens;
@@ -331,8 +502,10 @@ spec_status run(const Call& a) {
         fc.stream = a.stream;
         fc.attrs = pa;
         fc.numAttrs = 1;
-        e = a.dtype == SPEC_BF16 ? cudaLaunchKernelEx(&fc, finish_kernel<Bf16>, f)
-                                 : cudaLaunchKernelEx(&fc, finish_kernel<F32>, f);
+        if (a.dtype == SPEC_BF16)
+            e = aligned ? cudaLaunchKernelEx(&fc, finish_kernel<Bf16, true>, f) : cudaLaunchKernelEx(&fc, finish_kernel<Bf16, false>, f);
+        else
+            e = aligned ? cudaLaunchKernelEx(&fc, finish_kernel<F32, true>, f) : cudaLaunchKernelEx(&fc, finish_kernel<F32, false>, f);
         if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "chain kernel launch failed: %s", cudaGetErrorString(e));
     }
     return SPEC_OK;
@@ -578,6 +751,12 @@ int spec_debug_last_plan(int* out5) {
 int spec_debug_set_cluster_size(int C) {
     if (C < 0 || C > 16) return -1;
     g_cluster_override = C;
+    return 0;
+}
+
+int spec_debug_set_stats_grid(int ctas) {
+    if (ctas < 0 || ctas > S_MAX_CTAS) return -1;
+    g_stats_grid_override = ctas;
     return 0;
 }
 

@@ -138,18 +138,32 @@ struct Bf16 {
         const int padded = (n_el + CHUNK - 1) / CHUNK * CHUNK;
         for (int e = 0; e < padded; ++e) d[e] = e < n_el ? __ldg(s + e) : static_cast<uint16_t>(0xFF80u);
     }
-    // one chunk of a row in global memory, -inf beyond n_el (rows of any alignment)
-    __device__ static Raw gchunk(const unsigned char* row, int e0, int n_el, bool aligned) {
-        if (aligned && e0 + CHUNK <= n_el) return __ldcs(reinterpret_cast<const uint4*>(row) + e0 / CHUNK);
-        uint32_t w[4];
+    // One chunk of a row in global memory, -inf from element n_el on. AL: the row is 16-byte aligned and n_el
+    // a multiple of CHUNK, so a chunk is in range whole or not at all: one predicated 16-byte load into
+    // registers preset to -inf, with no branch and no register merge after it, so that all the loads of a
+    // piece stay in flight together. Otherwise element by element (rows of any alignment).
+    template <bool AL>
+    __device__ static Raw gload(const unsigned char* row, int e0, int n_el) {
+        if constexpr (AL) {
+            uint4 v = ninf();
+            const uint4* ptr = reinterpret_cast<const uint4*>(row) + e0 / CHUNK;
+            asm volatile(
+                "{\n\t.reg .pred q;\n\tsetp.lt.s32 q, %4, %5;\n\t"
+                "@q ld.global.cs.v4.u32 {%0, %1, %2, %3}, [%6];\n\t}"
+                : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w)
+                : "r"(e0), "r"(n_el), "l"(ptr));
+            return v;
+        } else {
+            uint32_t w[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int e = e0 + 2 * q;
-            const uint32_t lo = e < n_el ? __ldg(reinterpret_cast<const uint16_t*>(row) + e) : 0xFF80u;
-            const uint32_t hi = e + 1 < n_el ? __ldg(reinterpret_cast<const uint16_t*>(row) + e + 1) : 0xFF80u;
-            w[q] = lo | (hi << 16);
+            for (int q = 0; q < 4; ++q) {
+                const int e = e0 + 2 * q;
+                const uint32_t lo = e < n_el ? __ldg(reinterpret_cast<const uint16_t*>(row) + e) : 0xFF80u;
+                const uint32_t hi = e + 1 < n_el ? __ldg(reinterpret_cast<const uint16_t*>(row) + e + 1) : 0xFF80u;
+                w[q] = lo | (hi << 16);
+            }
+            return make_uint4(w[0], w[1], w[2], w[3]);
         }
-        return make_uint4(w[0], w[1], w[2], w[3]);
     }
 };
 
@@ -190,16 +204,26 @@ struct F32 {
         const int padded = (n_el + CHUNK - 1) / CHUNK * CHUNK;
         for (int e = 0; e < padded; ++e) d[e] = e < n_el ? __ldg(s + e) : 0xFF800000u;
     }
-    __device__ static Raw gchunk(const unsigned char* row, int e0, int n_el, bool aligned) {
+    template <bool AL>
+    __device__ static Raw gload(const unsigned char* row, int e0, int n_el) {
         const float* f = reinterpret_cast<const float*>(row);
-        if (aligned && e0 + CHUNK <= n_el) {
-            const float4* p = reinterpret_cast<const float4*>(f + e0);
-            return {__ldcs(p), __ldcs(p + 1)};
-        }
-        float v[8];
+        if constexpr (AL) {
+            Raw v = ninf();
+            const float* ptr = f + e0;
+            asm volatile(
+                "{\n\t.reg .pred q;\n\tsetp.lt.s32 q, %8, %9;\n\t"
+                "@q ld.global.cs.v4.f32 {%0, %1, %2, %3}, [%10];\n\t"
+                "@q ld.global.cs.v4.f32 {%4, %5, %6, %7}, [%10+16];\n\t}"
+                : "+f"(v.a.x), "+f"(v.a.y), "+f"(v.a.z), "+f"(v.a.w), "+f"(v.b.x), "+f"(v.b.y), "+f"(v.b.z),
+                  "+f"(v.b.w)
+                : "r"(e0), "r"(n_el), "l"(ptr));
+            return v;
+        } else {
+            float v[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) v[q] = e0 + q < n_el ? __ldg(f + e0 + q) : __uint_as_float(0xFF800000u);
-        return {make_float4(v[0], v[1], v[2], v[3]), make_float4(v[4], v[5], v[6], v[7])};
+            for (int q = 0; q < 8; ++q) v[q] = e0 + q < n_el ? __ldg(f + e0 + q) : __uint_as_float(0xFF800000u);
+            return {make_float4(v[0], v[1], v[2], v[3]), make_float4(v[4], v[5], v[6], v[7])};
+        }
     }
 };
 
@@ -439,12 +463,13 @@ __device__ __forceinline__ void piece_stats(const typename E::Raw (&r)[PCH], flo
         const float2 cc = make_float2(c, c);
         const float nb = -m * c;
         const float2 nb2 = make_float2(nb, nb);
-        float2 s2 = make_float2(0.f, 0.f);
+        float2 s2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
         for (int q = 0; q < PCH; ++q)
 #pragma unroll
-            for (int w = 0; w < 4; ++w) s2 = __fadd2_rn(s2, ex2x2(__ffma2_rn(E::pair(r[q], w), cc, nb2)));
-        s += s2.x + s2.y;
+            for (int w = 0; w < 4; ++w) s2[w] = __fadd2_rn(s2[w], ex2x2(__ffma2_rn(E::pair(r[q], w), cc, nb2)));
+        const float2 t = __fadd2_rn(__fadd2_rn(s2[0], s2[1]), __fadd2_rn(s2[2], s2[3]));   // independent chains
+        s += t.x + t.y;
     }
 }
 
@@ -453,8 +478,10 @@ template <class E>
 __device__ __forceinline__ void piece_overlap(const typename E::Raw (&rt)[PCH], const typename E::Raw (&ro)[PCH], float c,
                                               float bt, float bo, float2& acc) {
     const float2 cc = make_float2(c, c), bt2 = make_float2(bt, bt), bo2 = make_float2(bo, bo);
+    float2 a4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-    for (int q = 0; q < PCH; ++q) acc = chunk_overlap<E>(rt[q], ro[q], cc, bt2, bo2, acc);
+    for (int q = 0; q < PCH; ++q) a4[q & 3] = chunk_overlap<E>(rt[q], ro[q], cc, bt2, bo2, a4[q & 3]);
+    acc = __fadd2_rn(acc, __fadd2_rn(__fadd2_rn(a4[0], a4[1]), __fadd2_rn(a4[2], a4[3])));
 }
 
 // Pass 2 with masses: mode 1, residual (h - p_other)+ of the verified row (overlap added to acc); mode 2,
@@ -673,11 +700,14 @@ __device__ __forceinline__ void consumer_warp(const Ctx& x, const KParams& p, in
 
     Walker iss;   // runs R row pieces ahead of consumption
     int issued = 0, consumed = 0;
+    int islot = 0, cslot = 0;   // issued % R and consumed % R, kept as wrapping counters
+    uint32_t cpar = 0;          // (consumed / R) & 1
     auto issue_one = [&]() {
         const unsigned char* src;
         int len, last_read;
         if (!walker_next<E>(iss, p, x, w, src, len, last_read)) return;
-        const int slot = issued % R;
+        const int slot = islot;
+        if (++islot == R) islot = 0;
         unsigned char* dst = ring + static_cast<size_t>(slot) * x.slot_bytes;
         if (p.tma) {
             if (lane == 0) {
@@ -696,9 +726,13 @@ __device__ __forceinline__ void consumer_warp(const Ctx& x, const KParams& p, in
     };
     // Next row piece into registers (the piece's chunks pc); `tl`, if inside the piece, is read as `xv`.
     auto take = [&](int pc, Raw (&r)[PCH], int tl, float& xv) {
-        const int slot = consumed % R;
+        const int slot = cslot;
         const unsigned char* src = ring + static_cast<size_t>(slot) * x.slot_bytes;
-        ctx_wait(x, p, &full[slot], static_cast<uint32_t>((consumed / R) & 1));
+        ctx_wait(x, p, &full[slot], cpar);
+        if (++cslot == R) {
+            cslot = 0;
+            cpar ^= 1u;
+        }
         piece_load<E>(src, piece_chunks(x, pc), lane, r);
         if (tl >= 0 && tl / PE == pc && lane == ((tl % PE) / CHUNK) % 32) xv = E::at(src, tl % PE);
         __syncwarp();
@@ -1091,7 +1125,7 @@ struct FParams {
     const unsigned char* other;  // verified drafter rows: row (b, j) starts at element (b * K + j) * V
     const int32_t* tokens;       // [B, K]
     const uint64_t* seeds;       // [B]
-    int B, K, V, C, slice_elems, pcap, aligned;
+    int B, K, V, C, slice_elems, pcap;
     float c;
     int32_t* accept_len;         // [B]
     int32_t* out_tokens;         // [B, K+1]
@@ -1121,8 +1155,8 @@ __device__ __forceinline__ float fp_piece(const FParams& f, size_t row, int flat
 // and returns the first element whose running mass (starting at `before`) exceeds tp; when none does,
 // the last element with positive mass (-1 if there is none). mode 1: residual (h - p_other)+, mode 2: h.
 // Logit `tok` of h is patched to ht. The values are computed exactly as in the row pass.
-template <class E>
-__device__ int scan_pick(const FParams& f, const unsigned char* trow, const unsigned char* orow, int mode, int e_begin,
+template <class E, bool AL>
+__device__ int scan_pick(float c, const unsigned char* trow, const unsigned char* orow, int mode, int e_begin,
                          int e_end, float bt, float bo, int tok, float ht, float tp, float before, int lane) {
     using Raw = typename E::Raw;
     int last_pos = -1;
@@ -1133,11 +1167,11 @@ __device__ int scan_pick(const FParams& f, const unsigned char* trow, const unsi
 #pragma unroll
         for (int q = 0; q < 8; ++q) v[q] = 0.f;
         if (e0 < e_end) {
-            const Raw rt = E::gchunk(trow, e0, e_end, f.aligned);
-            const Raw ro = mode == 1 ? E::gchunk(orow, e0, e_end, f.aligned) : rt;
+            const Raw rt = E::template gload<AL>(trow, e0, e_end);
+            const Raw ro = mode == 1 ? E::template gload<AL>(orow, e0, e_end) : rt;
             const int et = (tok >= e0 && tok < e0 + CHUNK) ? tok - e0 : -1;
             float ovl = 0.f;
-            chunk_values<E>(mode, rt, ro, f.c, bt, bo, et, ht, v, ovl);
+            chunk_values<E>(mode, rt, ro, c, bt, bo, et, ht, v, ovl);
 #pragma unroll
             for (int q = 0; q < 8; ++q) m += v[q];
         }
@@ -1175,17 +1209,16 @@ __device__ int scan_pick(const FParams& f, const unsigned char* trow, const unsi
 
 // The same scan over one piece of at most PE logits, with every load issued before the scan (one memory
 // latency instead of one per 256 logits). Lane l holds logits e_begin + 256 r + 8 l .. + 7 of round r.
-template <class E>
-__device__ int scan_pick_piece(const FParams& f, const unsigned char* trow, const unsigned char* orow, int mode,
-                               int e_begin, int e_end, float bt, float bo, int tok, float ht, float tp, float before,
-                               int lane) {
+template <class E, bool AL>
+__device__ int scan_pick_piece(float c, const unsigned char* trow, const unsigned char* orow, int mode, int e_begin,
+                               int e_end, float bt, float bo, int tok, float ht, float tp, float before, int lane) {
     using Raw = typename E::Raw;
     Raw rt[PCH], ro[PCH];
 #pragma unroll
     for (int r = 0; r < PCH; ++r) {
         const int e0 = e_begin + r * 32 * CHUNK + lane * CHUNK;
-        rt[r] = e0 < e_end ? E::gchunk(trow, e0, e_end, f.aligned) : E::ninf();
-        ro[r] = (mode == 1 && e0 < e_end) ? E::gchunk(orow, e0, e_end, f.aligned) : rt[r];
+        rt[r] = E::template gload<AL>(trow, e0, e_end);
+        ro[r] = mode == 1 ? E::template gload<AL>(orow, e0, e_end) : rt[r];
     }
     int last_pos = -1;
 #pragma unroll 1
@@ -1207,7 +1240,7 @@ __device__ int scan_pick_piece(const FParams& f, const unsigned char* trow, cons
         if (e0 < e_end) {
             const int et = (tok >= e0 && tok < e0 + CHUNK) ? tok - e0 : -1;
             float ovl = 0.f;
-            chunk_values<E>(mode, a, b, f.c, bt, bo, et, ht, v, ovl);
+            chunk_values<E>(mode, a, b, c, bt, bo, et, ht, v, ovl);
 #pragma unroll
             for (int q = 0; q < 8; ++q) m += v[q];
         }
@@ -1243,7 +1276,7 @@ __device__ int scan_pick_piece(const FParams& f, const unsigned char* trow, cons
     return last_pos;
 }
 
-template <class E>
+template <class E, bool AL>
 __global__ void __launch_bounds__(256) finish_kernel(const FParams f) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31;
@@ -1296,13 +1329,13 @@ __global__ void __launch_bounds__(256) finish_kernel(const FParams f) {
         // reject whose computed Z is not positive)
         float all = 0.f;
         for (int e0 = lane * CHUNK; e0 < f.V; e0 += 32 * CHUNK) {
-            const typename E::Raw rt = E::gchunk(trow, e0, f.V, f.aligned);
+            const typename E::Raw rt = E::template gload<AL>(trow, e0, f.V);
             float2 unused = make_float2(0.f, 0.f);
             const int et = (tok >= e0 && tok < e0 + CHUNK) ? tok - e0 : -1;
             all += chunk_mass_patched<E>(2, rt, rt, f.c, bt, 0.f, et, ht, unused);
         }
         const float tp = u * warp_sum(all);
-        emitted = scan_pick<E>(f, trow, trow, 2, 0, f.V, bt, 0.f, tok, ht, tp, 0.f, lane);
+        emitted = scan_pick<E, AL>(f.c, trow, trow, 2, 0, f.V, bt, 0.f, tok, ht, tp, 0.f, lane);
     } else {
         const float tp = u * Z;
         // first piece whose prefix exceeds tp (else the last piece with mass)
@@ -1339,8 +1372,8 @@ __global__ void __launch_bounds__(256) finish_kernel(const FParams f) {
         if (ft >= 0) {
             int e_begin = 0, len = 0;
             fp_piece(f, row, ft, &e_begin, &len);
-            emitted = scan_pick_piece<E>(f, trow, orow, mode, e_begin, e_begin + len, bt, bo, tok, ht, tp, before_piece,
-                                         lane);
+            emitted = scan_pick_piece<E, AL>(f.c, trow, orow, mode, e_begin, e_begin + len, bt, bo, tok, ht, tp,
+                                             before_piece, lane);
         }
     }
 

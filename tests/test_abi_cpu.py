@@ -41,10 +41,11 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_workspace_size(lib):
     import speculative_decoding_verification_target_gb300 as sv
-    # header + per-row records + per-row piece masses (one per 2048 logits at least) + gamma partials;
-    # monotone in every size
+    # header + per-row records + per-row piece masses (one per 2048 logits at least) + gamma partials +
+    # the statistics pass's segment partials (8 bytes each, at least one per row of the 2K + 1 of a
+    # sequence); monotone in every size
     base = sv.workspace_size(64, 5, 128256, 1)
-    assert base >= 256 + 64 * 6 * 32 + 64 * 6 * (128256 // 2048) * 4 + 64 * 5 * 4
+    assert base >= 256 + 64 * 6 * 32 + 64 * 6 * (128256 // 2048) * 4 + 64 * 5 * 4 + 64 * 11 * 8
     assert sv.workspace_size(128, 5, 128256, 1) > base
     assert sv.workspace_size(64, 8, 128256, 1) > base
     assert sv.workspace_size(64, 5, 151936, 1) > base
@@ -101,6 +102,14 @@ def test_cluster_override_hook(lib):
     assert lib.spec_debug_set_cluster_size(12) == 0
     assert lib.spec_debug_set_cluster_size(8) == 0
     assert lib.spec_debug_set_cluster_size(0) == 0
+
+
+def test_stats_grid_hook(lib):
+    assert lib.spec_debug_set_stats_grid(-1) == -1
+    assert lib.spec_debug_set_stats_grid(1025) == -1
+    assert lib.spec_debug_set_stats_grid(1024) == 0
+    assert lib.spec_debug_set_stats_grid(7) == 0
+    assert lib.spec_debug_set_stats_grid(0) == 0
 
 
 def test_static_scratch_entry_refuses_oversized_calls_without_a_gpu(lib):

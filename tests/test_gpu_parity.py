@@ -24,13 +24,16 @@ def _lib():
     sv.load(build_if_missing=True)
     yield
     sv.set_cluster_size(0)
+    sv.set_stats_grid(0)
 
 
 @pytest.fixture(autouse=True)
 def _auto_cluster():
     sv.set_cluster_size(0)
+    sv.set_stats_grid(0)
     yield
     sv.set_cluster_size(0)
+    sv.set_stats_grid(0)
 
 
 def small(V, B=6, K=4, dtype="bf16", T=1.0, sigma=1.5, peaks=5, N=1, sigmas=None, selected=0, seed=11):
@@ -48,7 +51,7 @@ def small(V, B=6, K=4, dtype="bf16", T=1.0, sigma=1.5, peaks=5, N=1, sigmas=None
     (3000, 16, "bf16"),
 ])
 def test_verify_small(V, C, dtype):
-    sv.set_cluster_size(C)
+    sv.set_stats_grid(C)   # C CTAs in the statistics pass: every warp's run spans several rows
     w = small(V, dtype=dtype, T=0.8)
     inp = workloads.make(w)
     ref = oracle_verify(inp)
@@ -70,18 +73,40 @@ def test_verify_deterministic():
         assert torch.equal(a[k], b[k])
 
 
-def test_verify_cluster_size_invariance():
+def test_verify_stats_grid_invariance():
+    """The statistics grid only changes how rows are cut into per-warp segments (summation order): every
+    grid meets the oracle bar, and the probabilities agree within the tolerance."""
     w = small(50000, B=8, K=3)
-    g = to_device(workloads.make(w))
+    inp = workloads.make(w)
+    ref = oracle_verify(inp)
+    g = to_device(inp)
     outs = []
-    for C in (4, 8, 12, 16):
-        sv.set_cluster_size(C)
+    for ctas in (1, 3, 5, 37, 0):
+        sv.set_stats_grid(ctas)
         o = sv.verify(g["target"], g["draft"], g["tokens"], g["seeds"])
         torch.cuda.synchronize()
+        assert sv.last_plan()["clusters"] == (ctas or sv.last_plan()["clusters"])
+        assert_diag(o, ref)
+        assert_chain(o, ref, w.K)
         outs.append(o)
     for o in outs[1:]:
-        assert torch.equal(o["accept_len"], outs[0]["accept_len"])
         assert torch.allclose(o["diag"], outs[0]["diag"], atol=PROB_TOL, rtol=0)
+
+
+def test_verify_fewer_pieces_than_warps():
+    """One sequence of one draft over a 1000-token vocabulary: three pieces in all, so most warps of the
+    statistics grid have no run; and a grid of one CTA over many rows."""
+    for B, K, V, ctas in ((1, 1, 1000, 0), (1, 1, 1000, 4), (12, 7, 3000, 1)):
+        sv.set_stats_grid(ctas)
+        w = small(V, B=B, K=K)
+        inp = workloads.make(w)
+        ref = oracle_verify(inp)
+        g = to_device(inp)
+        out = sv.verify(g["target"], g["draft"], g["tokens"], g["seeds"], w.temperature)
+        torch.cuda.synchronize()
+        assert_diag(out, ref)
+        assert_chain(out, ref, w.K)
+        assert sv.read_status(out["workspace"]) == 0
 
 
 @pytest.mark.parametrize("name", ["tiny_sps_v1000", "sps_llama3_b64_k5"])
@@ -230,7 +255,7 @@ def test_gpu_chi2_lossless(V):
 @pytest.mark.parametrize("delta", [0.0, 0.75, 1.0])
 @pytest.mark.parametrize("V,C", [(3000, 0), (40000, 8)])
 def test_cactus_small(delta, V, C):
-    sv.set_cluster_size(C)
+    sv.set_stats_grid(C)
     w = small(V, B=8, K=5, sigma=2.0)
     inp = workloads.make(w)
     ref = oracle.cactus(host(inp["target"]), host(inp["draft"]), inp["tokens"].numpy(),
@@ -290,10 +315,12 @@ def test_counterfactual_small(V, C, selected):
     if selected >= 0:
         assert_diag(out, ref)
         assert_chain(out, ref, w.K)
-        # the fused chain equals a plain verify of the selected drafter
+        # a plain verify of the selected drafter (the two-kernel path, another summation order) meets the
+        # same bar against the same oracle chain
         v = sv.verify(g["target"], g["drafters"][selected].contiguous(), g["tokens"], g["seeds"], w.temperature)
         torch.cuda.synchronize()
-        assert torch.equal(v["accept_len"], out["accept_len"]) and torch.equal(v["out_tokens"], out["out_tokens"])
+        assert_diag(v, ref)
+        assert_chain(v, ref, w.K)
 
 
 def test_counterfactual_named_full():
@@ -333,11 +360,12 @@ def test_large_pool_named_sampled():
 
 
 # ------------------------------------------------------------------------------------------------
-# without diag the row pass skips the residual masses of accepted positions; the outputs must not change
+# without diag only the row pair of each sequence's draw is re-read (verify, Cactus), and the fused row
+# kernel skips the residual masses of accepted positions (counterfactual); the outputs must not change
 # ------------------------------------------------------------------------------------------------
 @pytest.mark.parametrize("V,B,K,C", [(5000, 16, 6, 0), (50000, 12, 5, 4), (128256, 24, 5, 0)])
 def test_verify_without_diag_matches(V, B, K, C):
-    sv.set_cluster_size(C)
+    sv.set_stats_grid(C)
     w = small(V, B=B, K=K, sigma=1.0)
     g = to_device(workloads.make(w))
     full = sv.verify(g["target"], g["draft"], g["tokens"], g["seeds"], w.temperature)
