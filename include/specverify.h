@@ -144,23 +144,16 @@ spec_status spec_clear_status(void* workspace, void* stream);
 /* Thread-local message describing the last non-OK status returned on this thread. */
 const char* spec_last_error(void);
 
-/* Tuning and test hook: forces the number of CTAs that split one vocabulary row in the fused row kernel of
- * spec_counterfactual_gamma (1 to 16; 0 restores the automatic choice). Process-wide, not thread-safe;
- * results do not depend on it beyond floating-point summation order. Returns 0, or -1 for an unsupported
- * value. */
-int spec_debug_set_cluster_size(int C);
-
 /* Tuning and test hook: forces the number of CTAs of the statistics pass of spec_verify, spec_verify_cactus
  * and spec_verify_static (1 to 1024; 0 restores the automatic choice, every SM once). The grid fixes how
  * the rows are cut into per-warp segments, so results depend on it only through floating-point summation
  * order. Process-wide, not thread-safe. Returns 0, or -1 for an unsupported value. */
 int spec_debug_set_stats_grid(int ctas);
 
-/* Tuning and test hook: the launch plan of the last call made on this thread, as five ints. Fused row
- * kernel (spec_counterfactual_gamma): cluster size C, shared-memory stages per consumer warp, clusters
- * launched, resident-target mode (0/1), pieces per CTA slice. Statistics pass (the other entry points):
- * 0, ring slots per warp, CTAs launched, 0, pieces per row. out5 is host memory. Returns 0, or -1 for a
- * NULL pointer. */
+/* Tuning and test hook: the launch plan of the last call made on this thread, as five ints: 0, ring slots
+ * per warp, CTAs launched, kernel (0: the statistics pass of spec_verify / spec_cactus_verify /
+ * spec_verify_static; 2: the gamma kernel of spec_counterfactual_gamma, which parks rows in tensor
+ * memory), pieces per row. out5 is host memory. Returns 0, or -1 for a NULL pointer. */
 int spec_debug_last_plan(int* out5);
 
 #ifdef __cplusplus

@@ -20,7 +20,7 @@ from . import _build
 SPEC_OK, SPEC_ERR_INVALID, SPEC_ERR_CUDA, SPEC_ERR_UNSUPPORTED = 0, 1, 2, 3
 STATUS_BAD_TOKEN, STATUS_TIMEOUT = 1, 2
 EXPORTS = ("spec_workspace_size", "spec_verify", "spec_counterfactual_gamma", "spec_cactus_verify",
-           "spec_read_status", "spec_clear_status", "spec_last_error", "spec_debug_set_cluster_size",
+           "spec_read_status", "spec_clear_status", "spec_last_error",
            "spec_debug_last_plan", "spec_verify_static", "spec_debug_set_stats_grid")
 
 _lib = None
@@ -62,8 +62,6 @@ def load(build_if_missing: bool = False):
     lib.spec_clear_status.restype = I
     lib.spec_last_error.argtypes = []
     lib.spec_last_error.restype = ctypes.c_char_p
-    lib.spec_debug_set_cluster_size.argtypes = [I]
-    lib.spec_debug_set_cluster_size.restype = I
     lib.spec_debug_set_stats_grid.argtypes = [I]
     lib.spec_debug_set_stats_grid.restype = I
     lib.spec_debug_last_plan.argtypes = [ctypes.POINTER(ctypes.c_int)]
@@ -127,12 +125,6 @@ def clear_status(ws, stream=None):
     _check(load().spec_clear_status(_p(ws), _stream(stream)))
 
 
-def set_cluster_size(C: int):
-    """Tuning / test hook: CTAs per vocabulary row of the fused counterfactual kernel (0 = automatic)."""
-    if load().spec_debug_set_cluster_size(int(C)) != 0:
-        raise ValueError("unsupported cluster size %r" % C)
-
-
 def set_stats_grid(ctas: int):
     """Tuning / test hook: CTAs of the statistics pass of verify / cactus_verify (0 = automatic)."""
     if load().spec_debug_set_stats_grid(int(ctas)) != 0:
@@ -143,7 +135,7 @@ def last_plan() -> dict:
     """Tuning / test hook: the launch plan of the last call on this thread."""
     out = (ctypes.c_int * 5)()
     load().spec_debug_last_plan(out)
-    return dict(C=out[0], stages=out[1], clusters=out[2], resident=out[3], pieces=out[4])
+    return dict(stages=out[1], ctas=out[2], kernel=out[3], pieces=out[4])
 
 
 def _outputs(B, K, device, accept_len, out_tokens, diag, want_diag):

@@ -1,5 +1,5 @@
-// Host side of the C ABI declared in include/specverify.h: argument validation, launch planning
-// (cluster size, vocabulary slice, shared-memory slots, persistent grid size) and the launches.
+// Host side of the C ABI declared in include/specverify.h: argument validation, launch configuration
+// (statistics grid, ring depth, draw clusters) and the launches.
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -8,7 +8,7 @@
 #include <mutex>
 
 #include "specverify.h"
-#include "specverify_chain.cuh"
+#include "specverify_gamma.cuh"
 
 namespace specv {
 namespace {
@@ -29,174 +29,20 @@ constexpr int MAX_N = 64;
 constexpr size_t WS_HEADER = 256;          // status word + padding
 constexpr int SMEM_MAX_PER_CTA = 232448;   // opt-in maximum per CTA
 
-int g_cluster_override = 0;   // test / tuning hook (0 = automatic)
 int g_stats_grid_override = 0;   // CTAs of the statistics kernel (0 = automatic)
-thread_local int g_last_plan[5] = {0, 0, 0, 0, 0};   // C, S, clusters launched, resident, pieces per slice
+thread_local int g_last_plan[5] = {0, 0, 0, 0, 0};   // see spec_debug_last_plan
 
-struct Plan {
-    int C = 1, slice_elems = 0, pcap = 0, R = 0, resident = 0, tma = 0, ncl = 0;
-    size_t smem = 0;
-};
-
-int slice_for(int V, int C) { return ((V + SLICE_Q - 1) / SLICE_Q + C - 1) / C * SLICE_Q; }
-int pcap_for(int slice_elems) { return (slice_elems + PE - 1) / PE; }
-
-// barriers, exchange entries, scalars and the abort flag (see the layout note above rows_kernel)
-size_t fixed_smem(int R, int C) {
-    return static_cast<size_t>(W * R + 4 + 3 * NXB) * 8 + static_cast<size_t>(NXB * W * XW + NXB * C * XW + NXB * XW) * 4 + 16;
-}
-
-using KernelFn = void (*)(const KParams);
-
-struct OccKey {
-    KernelFn fn;
-    int C;
-    size_t smem;
-    int device;
-};
-std::mutex g_occ_mu;
-OccKey g_occ_keys[64];
-int g_occ_vals[64];
-int g_occ_n = 0;
-
-// Number of clusters of C CTAs with `smem` bytes each that fit on the GPU at once (cached per device).
-cudaError_t max_clusters(KernelFn fn, int C, size_t smem, int& out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    {
-        std::lock_guard<std::mutex> lk(g_occ_mu);
-        for (int i = 0; i < g_occ_n; ++i)
-            if (g_occ_keys[i].fn == fn && g_occ_keys[i].C == C && g_occ_keys[i].smem == smem &&
-                g_occ_keys[i].device == dev) {
-                out = g_occ_vals[i];
-                return cudaSuccess;
-            }
-    }
-    // The attribute is a per-function ceiling shared by every plan: always the opt-in maximum, so that a
-    // later plan with less shared memory never lowers it under an earlier, cached one.
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX_PER_CTA);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute at[1];
-    cfg.gridDim = dim3(static_cast<unsigned>(C), 1, 1);
-    cfg.blockDim = dim3(NT, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = static_cast<unsigned>(C);
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
-    if (e != cudaSuccess) return e;
-    if (n < 1) return cudaErrorInvalidConfiguration;
-    std::lock_guard<std::mutex> lk(g_occ_mu);
-    if (g_occ_n < 64) {
-        g_occ_keys[g_occ_n] = {fn, C, smem, dev};
-        g_occ_vals[g_occ_n] = n;
-        ++g_occ_n;
-    }
-    out = n;
-    return cudaSuccess;
-}
-
-// Rows handled by the busiest of ncl clusters: items are dealt round robin, the B*K verified positions
-// (1 + N rows each) first and the B bonus rows (1 row each) last.
-long long busiest_rows(int BK, int B_bonus, int N, int ncl) {
-    long long worst = 0;
-    for (int c = 0; c < ncl; ++c) {
-        const long long pos = BK / ncl + (c < BK % ncl ? 1 : 0);
-        // bonus items are numbers BK .. BK + B_bonus - 1; count those congruent to c mod ncl
-        const int first = ((c - BK % ncl) % ncl + ncl) % ncl;   // offset of the first bonus item of c
-        const long long bon = B_bonus > first ? (B_bonus - 1 - first) / ncl + 1 : 0;
-        worst = std::max(worst, pos * (1 + N) + bon);
-    }
-    return worst;
-}
-
-// Chooses the cluster size C and the ring depth R. Each CTA holds, per consumer warp, R slots of one piece
-// and, when items have two or more drafters (resident mode), two copies of its target slice. Among the
-// cluster sizes whose shared memory fits, the plan minimises an estimate of the busiest CTA's time:
-// (rows of its cluster) x (slice length + a fixed per-row cost of the cluster-wide statistics exchange,
-// worth about UNIT_COST_EL logits of streaming), using the number of clusters the GPU places at once.
-// In streamed mode a slice is re-read from L2 about two rows after its first read; when (CTAs) x (two rows
-// of a slice) exceeds half of L2 the estimate grows with the excess. Ties go to the smaller cluster.
-constexpr double UNIT_COST_EL = 40000.0;
-
-spec_status make_plan(KernelFn fn, int V, int eb, int N, int BK, int B_bonus, bool aligned, Plan& out) {
-    static const int auto_cands[] = {1, 2, 4, 8, 16};
-    const int* cands = auto_cands;
-    int ncand = 5;
-    int forced[1];
-    if (g_cluster_override > 0) {
-        forced[0] = g_cluster_override;
-        cands = forced;
-        ncand = 1;
-    }
-    const int resident = N >= 2 ? 1 : 0;
-    const size_t slot_bytes = static_cast<size_t>(PE) * eb;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    int l2 = 0;
-    cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
-    bool found = false;
-    double best = 0.0;
-    for (int ci = 0; ci < ncand; ++ci) {
-        Plan p;
-        p.C = cands[ci];
-        p.slice_elems = slice_for(V, p.C);
-        p.pcap = pcap_for(p.slice_elems);
-        p.resident = resident;
-        p.tma = aligned ? 1 : 0;
-        const size_t tb = resident ? (static_cast<size_t>(p.slice_elems) * eb + 127) / 128 * 128 : 0;
-        int R = MAX_R;
-        while (R >= 1 && 2 * tb + W * R * slot_bytes + fixed_smem(R, p.C) > static_cast<size_t>(SMEM_MAX_PER_CTA)) --R;
-        if (R < 1) continue;
-        p.R = R;
-        p.smem = 2 * tb + W * R * slot_bytes + fixed_smem(R, p.C);
-        int ncl = 0;
-        const cudaError_t e = max_clusters(fn, p.C, p.smem, ncl);
-        if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "occupancy query failed: %s", cudaGetErrorString(e));
-        p.ncl = ncl;
-        double cost = static_cast<double>(busiest_rows(BK, B_bonus, N, ncl)) * (p.slice_elems + UNIT_COST_EL);
-        const double footprint = static_cast<double>(ncl) * p.C * 2.0 * p.slice_elems * eb;
-        if (!resident && l2 > 0 && footprint > l2 / 2.0) cost *= 1.0 + (footprint - l2 / 2.0) / l2;
-        if (!found || cost < best * 0.999) {
-            best = cost;
-            out = p;
-            found = true;
-        }
-    }
-    if (!found) return fail(SPEC_ERR_UNSUPPORTED, "no launch plan fits V=%d (cluster override %d)", V, g_cluster_override);
-    return SPEC_OK;
-}
-
-// Workspace layout: [status header][records B*(K+1)*REC][piece masses B*(K+1)*pieces_row][gamma partials
-// N*B*K*16*W][segment partials of the statistics pass]. The per-row regions are sized for the largest
-// cluster split so that any plan fits; the segment region for the largest statistics grid.
+// Workspace layout: [status header][row partials]. The row partials are the statistics pass's segment
+// (max, sum) pairs (segment (warp g, row r) at entry g + r: fewer than min(G, pieces) + rows entries, sized
+// for the largest grid) or, for the gamma kernel, one (max, sum) pair per statistics row (B (2K + 1)).
 struct WsLayout {
-    size_t rec_off, tiles_off, gpart_off, part_off, total;
-    int tiles_row;   // floats per row in the piece-mass region (>= C * pcap for every plan)
-    int gpart_row;   // floats per (drafter, b, j) in the gamma region (>= C * W)
+    size_t part_off, total;
 };
 
 WsLayout ws_layout(int B, int K, int V, int N) {
+    (void)N;
     WsLayout w;
-    int tiles_row = 0;
-    for (int C = 1; C <= 16; ++C) tiles_row = std::max(tiles_row, C * pcap_for(slice_for(V, C)));
-    w.tiles_row = tiles_row;
-    w.gpart_row = 16 * W;
-    const size_t rows = static_cast<size_t>(B) * static_cast<size_t>(K + 1);
-    w.rec_off = WS_HEADER;
-    w.tiles_off = w.rec_off + rows * REC * sizeof(float);
-    w.gpart_off = w.tiles_off + rows * static_cast<size_t>(tiles_row) * sizeof(float);
-    w.part_off = w.gpart_off + static_cast<size_t>(N) * B * K * static_cast<size_t>(w.gpart_row) * sizeof(float);
-    w.part_off = (w.part_off + 15) / 16 * 16;   // float2 entries
-    // segment (warp g, row r) of the statistics pass at entry g + r: fewer than min(G, pieces) + rows entries
+    w.part_off = WS_HEADER;
     const long long srows = static_cast<long long>(B) * (2 * K + 1);
     const long long pieces = srows * ((V + PE - 1) / PE);
     const long long gmax = static_cast<long long>(S_MAX_CTAS) * SW;
@@ -282,6 +128,73 @@ cudaError_t draw_smem_ceiling(Fn fn, int dev) {
     return e;
 }
 
+// The chain and its draw for one drafter (one cluster per sequence), launched with programmatic stream
+// serialisation behind the kernel that computed the row statistics: either the segment partials of
+// stats_kernel (part, P pieces over G warps) or whole-row pairs (row_ms, from gamma_kernel).
+spec_status launch_draw(const Call& a, bool aligned, const unsigned char* draft, const float2* part,
+                        const float2* row_ms, long long P, int G, unsigned* status) {
+    const int eb = a.dtype == SPEC_BF16 ? 2 : 4;
+    DParams d = {};
+    d.target = static_cast<const unsigned char*>(a.target);
+    d.draft = draft;
+    d.part = part;
+    d.row_ms = row_ms;
+    d.P = P;
+    d.G = G;
+    d.np = (a.V + PE - 1) / PE;
+    d.rows_a_n = static_cast<long long>(a.B) * (a.K + 1);
+    d.tokens = a.tokens;
+    d.seeds = a.seeds;
+    d.B = a.B;
+    d.K = a.K;
+    d.V = a.V;
+    d.c = static_cast<float>(1.4426950408889634 / static_cast<double>(a.temperature));
+    d.delta = a.delta;
+    d.cactus = a.cactus;
+    d.accept_len = a.accept_len;
+    d.out_tokens = a.out_tokens;
+    d.diag = a.diag;
+    d.gamma_star = a.gamma_star;
+    d.status = status;
+    // CTAs per sequence: the largest power of two up to D_MAX_CPS that keeps the grid within one CTA per SM
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    int cps = 1;
+    while (cps < D_MAX_CPS && static_cast<long long>(a.B) * cps * 2 <= sms) cps *= 2;
+    d.cps = cps;
+    // chunk masses, plus (bulk-copy mode) a two-piece slot and an mbarrier per warp when they fit
+    const size_t cm_bytes = static_cast<size_t>((d.np + cps - 1) / cps) * D_CPP * sizeof(float);
+    const size_t ring_bytes = static_cast<size_t>(DW) * (2 * static_cast<size_t>(PE) * eb + sizeof(uint64_t));
+    const size_t dsmem_cap = SMEM_MAX_PER_CTA - 8192;   // the ceiling draw_smem_ceiling sets
+    d.tma = aligned && cm_bytes + ring_bytes <= dsmem_cap ? 1 : 0;
+    const size_t dsmem = cm_bytes + (d.tma ? ring_bytes : 0);
+    using DrawFn = void (*)(const DParams);
+    DrawFn dfn = a.dtype == SPEC_BF16 ? (aligned ? draw_kernel<Bf16, true> : draw_kernel<Bf16, false>)
+                                      : (aligned ? draw_kernel<F32, true> : draw_kernel<F32, false>);
+    cudaError_t e = draw_smem_ceiling(dfn, dev);
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "draw kernel attribute failed: %s", cudaGetErrorString(e));
+    // its CTAs start as the grid before it frees SMs and wait for it (griddepcontrol.wait) after reading
+    // their inputs
+    cudaLaunchAttribute da[2];
+    da[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    da[0].val.programmaticStreamSerializationAllowed = 1;
+    da[1].id = cudaLaunchAttributeClusterDimension;
+    da[1].val.clusterDim.x = static_cast<unsigned>(cps);
+    da[1].val.clusterDim.y = 1;
+    da[1].val.clusterDim.z = 1;
+    cudaLaunchConfig_t dc = {};
+    dc.gridDim = dim3(static_cast<unsigned>(a.B * cps), 1, 1);
+    dc.blockDim = dim3(DNT, 1, 1);
+    dc.dynamicSmemBytes = dsmem;
+    dc.stream = a.stream;
+    dc.attrs = da;
+    dc.numAttrs = 2;
+    e = cudaLaunchKernelEx(&dc, dfn, d);
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "draw kernel launch failed: %s", cudaGetErrorString(e));
+    return SPEC_OK;
+}
+
 // Chain verification of one drafter (standard and Cactus): statistics pass over every row, then one cluster
 // per sequence for the chain and its draw (specverify_chain.cuh).
 spec_status run_chain(const Call& a, bool aligned) {
@@ -327,64 +240,57 @@ spec_status run_chain(const Call& a, bool aligned) {
     e = cudaLaunchKernelEx(&cfg, sfn, s);
     if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "statistics kernel launch failed: %s", cudaGetErrorString(e));
 
-    DParams d = {};
-    d.target = s.rows_a;
-    d.draft = s.rows_b;
-    d.part = s.part;
-    d.P = s.P;
-    d.G = s.G;
-    d.np = s.np;
-    d.rows_a_n = s.rows_a_n;
-    d.tokens = a.tokens;
-    d.seeds = a.seeds;
-    d.B = a.B;
-    d.K = a.K;
-    d.V = a.V;
-    d.c = s.c;
-    d.delta = a.delta;
-    d.cactus = a.cactus;
-    d.accept_len = a.accept_len;
-    d.out_tokens = a.out_tokens;
-    d.diag = a.diag;
-    d.gamma_star = a.gamma_star;
-    d.status = s.status;
-    // CTAs per sequence: the largest power of two up to D_MAX_CPS that keeps the grid within one CTA per SM
+    return launch_draw(a, aligned, static_cast<const unsigned char*>(a.others), s.part, nullptr, s.P, s.G, s.status);
+}
+
+// Counterfactual gamma for N drafters (gamma_kernel, one CTA per SM, rows whole per CTA), followed by the
+// chain and draw of drafter `selected` when one is given.
+spec_status run_gamma(const Call& a, bool aligned) {
+    const int eb = a.dtype == SPEC_BF16 ? 2 : 4;
+    const WsLayout wl = ws_layout(a.B, a.K, a.V, a.N);
+    unsigned char* ws = static_cast<unsigned char*>(a.workspace);
+    const bool chain = a.selected >= 0;
+    CgParams g = {};
+    g.target = static_cast<const unsigned char*>(a.target);
+    g.drafters = static_cast<const unsigned char*>(a.others);
+    g.B = a.B;
+    g.K = a.K;
+    g.V = a.V;
+    g.N = a.N;
+    const int pe = G_PIECE_BYTES / eb;
+    g.np = (a.V + pe - 1) / pe;
+    g.U = static_cast<long long>(a.B) * a.K * (a.N + 1) + (chain ? a.B : 0);
     int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    int cps = 1;
-    while (cps < D_MAX_CPS && static_cast<long long>(a.B) * cps * 2 <= sms) cps *= 2;
-    d.cps = cps;
-    // chunk masses, plus (bulk-copy mode) a two-piece slot and an mbarrier per warp when they fit
-    const size_t cm_bytes = static_cast<size_t>((s.np + cps - 1) / cps) * D_CPP * sizeof(float);
-    const size_t ring_bytes = static_cast<size_t>(DW) * (2 * static_cast<size_t>(PE) * eb + sizeof(uint64_t));
-    const size_t dsmem_cap = SMEM_MAX_PER_CTA - 8192;   // the ceiling draw_smem_ceiling sets
-    d.tma = aligned && cm_bytes + ring_bytes <= dsmem_cap ? 1 : 0;
-    const size_t dsmem = cm_bytes + (d.tma ? ring_bytes : 0);
-    using DrawFn = void (*)(const DParams);
-    DrawFn dfn = a.dtype == SPEC_BF16 ? (aligned ? draw_kernel<Bf16, true> : draw_kernel<Bf16, false>)
-                                      : (aligned ? draw_kernel<F32, true> : draw_kernel<F32, false>);
-    e = draw_smem_ceiling(dfn, dev);
-    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "draw kernel attribute failed: %s", cudaGetErrorString(e));
-    // launched with programmatic stream serialisation: its CTAs start as the grid above frees SMs and wait
-    // for it (griddepcontrol.wait) after reading their inputs
-    cudaLaunchAttribute da[2];
-    da[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    da[0].val.programmaticStreamSerializationAllowed = 1;
-    da[1].id = cudaLaunchAttributeClusterDimension;
-    da[1].val.clusterDim.x = static_cast<unsigned>(cps);
-    da[1].val.clusterDim.y = 1;
-    da[1].val.clusterDim.z = 1;
-    cudaLaunchConfig_t dc = {};
-    dc.gridDim = dim3(static_cast<unsigned>(a.B * cps), 1, 1);
-    dc.blockDim = dim3(DNT, 1, 1);
-    dc.dynamicSmemBytes = dsmem;
-    dc.stream = a.stream;
-    dc.attrs = da;
-    dc.numAttrs = 2;
-    e = cudaLaunchKernelEx(&dc, dfn, d);
-    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "draw kernel launch failed: %s", cudaGetErrorString(e));
-    return SPEC_OK;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess || sms < 1) return fail(SPEC_ERR_CUDA, "device query failed: %s", cudaGetErrorString(e));
+    g.G = static_cast<int>(std::min<long long>(sms, g.U));
+    g.c = static_cast<float>(1.4426950408889634 / static_cast<double>(a.temperature));
+    g.tma = aligned ? 1 : 0;
+    g.selected = chain ? a.selected : -1;
+    g.gamma = a.gamma;
+    g.loss = a.loss;
+    g.row_ms = chain ? reinterpret_cast<float2*>(ws + wl.part_off) : nullptr;
+    g.status = reinterpret_cast<unsigned*>(ws);
+    using GammaFn = void (*)(const CgParams);
+    GammaFn gfn = a.dtype == SPEC_BF16 ? gamma_kernel<Bf16> : gamma_kernel<F32>;
+    e = draw_smem_ceiling(gfn, dev);   // G_SMEM is below that ceiling
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "gamma kernel attribute failed: %s", cudaGetErrorString(e));
+    g_last_plan[0] = 0;
+    g_last_plan[1] = G_R;
+    g_last_plan[2] = g.G;
+    g_last_plan[3] = 2;
+    g_last_plan[4] = g.np;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(g.G), 1, 1);
+    cfg.blockDim = dim3(GNT, 1, 1);
+    cfg.dynamicSmemBytes = G_SMEM;   // also in the unaligned mode: keeps one CTA per SM for the TMEM allocation
+    cfg.stream = a.stream;
+    e = cudaLaunchKernelEx(&cfg, gfn, g);
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "gamma kernel launch failed: %s", cudaGetErrorString(e));
+    if (!chain) return SPEC_OK;
+    const unsigned char* draft = g.drafters + static_cast<size_t>(a.selected) * a.B * a.K * static_cast<size_t>(a.V) * eb;
+    return launch_draw(a, aligned, draft, nullptr, g.row_ms, 0, 0, g.status);
 }
 
 spec_status run(const Call& a) {
@@ -395,120 +301,9 @@ spec_status run(const Call& a) {
     // bulk copies need 16-byte aligned pieces of whole 8-logit chunks
     const bool aligned = ((reinterpret_cast<uintptr_t>(a.target) | reinterpret_cast<uintptr_t>(a.others)) & align_mask) == 0 &&
                          (static_cast<size_t>(a.V) * eb) % 16 == 0 && a.V % CHUNK == 0;
-    if (chain && a.N == 1 && !a.gamma) return run_chain(a, aligned);
-    KernelFn fn = a.dtype == SPEC_BF16 ? rows_kernel<Bf16> : rows_kernel<F32>;
-    const int BK = a.B * a.K;
-    const int B_bonus = chain ? a.B : 0;
-    Plan pl;
-    spec_status st = make_plan(fn, a.V, eb, a.N, BK, B_bonus, aligned, pl);
-    if (st != SPEC_OK) return st;
-
-    const WsLayout wl = ws_layout(a.B, a.K, a.V, a.N);
-    unsigned char* ws = static_cast<unsigned char*>(a.workspace);
-    KParams k = {};
-    k.target = static_cast<const unsigned char*>(a.target);
-    k.others = static_cast<const unsigned char*>(a.others);
-    k.tokens = chain ? a.tokens : nullptr;
-    k.seeds = chain ? a.seeds : nullptr;
-    k.all_residuals = a.diag ? 1 : 0;
-    k.B = a.B;
-    k.K = a.K;
-    k.V = a.V;
-    k.N = a.N;
-    k.selected = a.selected;
-    k.BK = BK;
-    k.num_items = BK + B_bonus;
-    k.c = static_cast<float>(1.4426950408889634 / static_cast<double>(a.temperature));
-    k.delta = a.delta;
-    k.cactus = a.cactus;
-    k.slice_elems = pl.slice_elems;
-    // the kernels index the piece-mass region as (row * C + rank) * pcap + piece: rows are C * pcap <=
-    // wl.tiles_row floats apart, so the region sized with wl.tiles_row holds every plan
-    k.pcap = pl.pcap;
-    k.tma = pl.tma;
-    k.resident = pl.resident;
-    k.R = pl.R;
-    k.lead = 1;
-    k.status = reinterpret_cast<unsigned*>(ws);
-    k.rec = chain ? reinterpret_cast<float*>(ws + wl.rec_off) : nullptr;
-    k.tiles = chain ? reinterpret_cast<float*>(ws + wl.tiles_off) : nullptr;
-    k.gpart = a.gamma ? reinterpret_cast<float*>(ws + wl.gpart_off) : nullptr;
-
-    const int grid_clusters = pl.ncl < k.num_items ? pl.ncl : k.num_items;
-    g_last_plan[0] = pl.C;
-    g_last_plan[1] = pl.R;
-    g_last_plan[2] = grid_clusters;
-    g_last_plan[3] = pl.resident;
-    g_last_plan[4] = pl.pcap;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute at[1];
-    cfg.gridDim = dim3(static_cast<unsigned>(grid_clusters * pl.C), 1, 1);
-    cfg.blockDim = dim3(NT, 1, 1);
-    cfg.dynamicSmemBytes = pl.smem;
-    cfg.stream = a.stream;
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = static_cast<unsigned>(pl.C);
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, fn, k);
-    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "verification kernel launch failed: %s", cudaGetErrorString(e));
-
-    // follow-up kernels: launched with programmatic stream serialisation, they wait on the grid above
-    // (griddepcontrol.wait) while their launch overlaps its tail
-    cudaLaunchAttribute pa[1];
-    pa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    pa[0].val.programmaticStreamSerializationAllowed = 1;
-    const int per_block = 8;   // warps per block
-    if (a.gamma) {
-        GParams g = {};
-        g.gpart = k.gpart;
-        g.n_out = a.N * a.B * a.K;
-        g.C = pl.C;
-        g.gamma = a.gamma;
-        g.loss = a.loss;
-        cudaLaunchConfig_t gc = {};
-        gc.gridDim = dim3(static_cast<unsigned>((g.n_out + per_block - 1) / per_block), 1, 1);
-        gc.blockDim = dim3(per_block * 32, 1, 1);
-        gc.stream = a.stream;
-        gc.attrs = pa;
-        gc.numAttrs = 1;
-        e = cudaLaunchKernelEx(&gc, gamma_reduce_kernel, g);
-        if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "gamma reduction launch failed: %s", cudaGetErrorString(e));
-    }
-    if (chain) {
-        FParams f = {};
-        f.rec = k.rec;
-        f.tiles = k.tiles;
-        f.target = k.target;
-        f.other = k.others + static_cast<size_t>(a.selected) * a.B * a.K * static_cast<size_t>(a.V) * eb;
-        f.tokens = a.tokens;
-        f.seeds = a.seeds;
-        f.B = a.B;
-        f.K = a.K;
-        f.V = a.V;
-        f.C = pl.C;
-        f.slice_elems = pl.slice_elems;
-        f.pcap = pl.pcap;
-        f.c = k.c;
-        f.accept_len = a.accept_len;
-        f.out_tokens = a.out_tokens;
-        f.diag = a.diag;
-        f.gamma_star = a.gamma_star;
-        cudaLaunchConfig_t fc = {};
-        fc.gridDim = dim3(static_cast<unsigned>((a.B + per_block - 1) / per_block), 1, 1);
-        fc.blockDim = dim3(per_block * 32, 1, 1);
-        fc.stream = a.stream;
-        fc.attrs = pa;
-        fc.numAttrs = 1;
-        if (a.dtype == SPEC_BF16)
-            e = aligned ? cudaLaunchKernelEx(&fc, finish_kernel<Bf16, true>, f) : cudaLaunchKernelEx(&fc, finish_kernel<Bf16, false>, f);
-        else
-            e = aligned ? cudaLaunchKernelEx(&fc, finish_kernel<F32, true>, f) : cudaLaunchKernelEx(&fc, finish_kernel<F32, false>, f);
-        if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "chain kernel launch failed: %s", cudaGetErrorString(e));
-    }
-    return SPEC_OK;
+    if (a.gamma) return run_gamma(a, aligned);
+    if (chain && a.N == 1) return run_chain(a, aligned);
+    return fail(SPEC_ERR_INVALID, "nothing to compute: no gamma and no chain");
 }
 
 spec_status check_common(const void* target, const void* others, spec_dtype dtype, int B, int K, int V, int N,
@@ -745,12 +540,6 @@ const char* spec_last_error(void) { return g_err; }
 int spec_debug_last_plan(int* out5) {
     if (!out5) return -1;
     for (int i = 0; i < 5; ++i) out5[i] = g_last_plan[i];
-    return 0;
-}
-
-int spec_debug_set_cluster_size(int C) {
-    if (C < 0 || C > 16) return -1;
-    g_cluster_override = C;
     return 0;
 }
 

@@ -24,8 +24,8 @@
 // ascending warp order), evaluate p(t) and q(t) at the draft tokens, run the chain (with the Cactus h when
 // asked), then compute the residual (or bonus) mass of every piece of row L in parallel, prefix-sum those
 // masses, and find the drawn token with one scan of the chosen piece. The per-element arithmetic is the
-// one of rows_kernel and finish_kernel (chunk_values / piece_mass / scan_pick_piece), so the two
-// verification paths compute every probability the same way.
+// one of the inverse-CDF scan (chunk_mass / chunk_values / scan_pick), so every probability of the draw is
+// computed the same way wherever it is needed.
 #pragma once
 #include "specverify_kernels.cuh"
 
@@ -196,7 +196,8 @@ constexpr int D_CPP = PE / CHUNK;       // chunks per piece
 struct DParams {
     const unsigned char* target;   // [B, K+1, V]
     const unsigned char* draft;    // [B, K, V]
-    const float2* part;            // stats_kernel's segment partials
+    const float2* part;            // stats_kernel's segment partials (when row_ms is null)
+    const float2* row_ms;          // or the (max, sum) of every statistics row, written by the gamma kernel
     long long P;                   // pieces of the statistics pass
     int G;                         // its warps
     int np;                        // pieces per row
@@ -215,8 +216,13 @@ struct DParams {
     unsigned* status;
 };
 
-// (max, sum) of statistics row r: its segments merged in ascending warp order. Warp-collective.
+// (max, sum) of statistics row r: its segments merged in ascending warp order (warp-collective), or the
+// row's entry of row_ms when the gamma kernel computed the rows whole.
 __device__ __forceinline__ MaxSum d_row_stats(const DParams& p, const Split& sp, long long r, float c, int lane) {
+    if (p.row_ms) {
+        const float2 v = p.row_ms[r];
+        return MaxSum{v.x, v.y};
+    }
     const long long g0 = sp.warp_of(r * p.np), g1 = sp.warp_of(r * p.np + p.np - 1);
     MaxSum a{__uint_as_float(0xFF800000u), 0.f};
     for (long long g = g0 + lane; g <= g1; g += 32) {
@@ -228,61 +234,63 @@ __device__ __forceinline__ MaxSum d_row_stats(const DParams& p, const Split& sp,
 
 // Masses of the chunks lane l holds of a piece (chunks l + 32 q): mode 1 the residual (h - q)+, mode 2 h
 // itself, element `et` of the piece (if >= 0) being h = hpatch. Element for element the values of
-// piece_mass and chunk_values.
+// chunk_mass and chunk_values.
 template <class E>
 __device__ __forceinline__ void piece_chunk_masses(int mode, const typename E::Raw (&rt)[PCH],
-                                                   const typename E::Raw (&ro)[PCH], int lane, float c, float bt,
-                                                   float bo, int et, float hpatch, float (&cm)[PCH]) {
-    const float2 cc = make_float2(c, c), bt2 = make_float2(bt, bt), bo2 = make_float2(bo, bo);
+                                                   const typename E::Raw (&ro)[PCH], int lane, float c, PairOff o,
+                                                   int et, float hpatch, float (&cm)[PCH]) {
     const int etc = et >= 0 ? et / CHUNK : -1;
     float2 unused = make_float2(0.f, 0.f);
 #pragma unroll
     for (int q = 0; q < PCH; ++q) {
         if (lane + 32 * q != etc) {
-            cm[q] = chunk_mass<E>(mode, rt[q], ro[q], cc, bt2, bo2, unused);
+            cm[q] = chunk_mass<E>(mode, rt[q], ro[q], c, o, unused);
         } else {
             float ovl = 0.f;
-            cm[q] = chunk_mass_patch_only<E>(mode, rt[q], ro[q], c, bt, bo, et % CHUNK, hpatch, ovl);
+            cm[q] = chunk_mass_patch_only<E>(mode, rt[q], ro[q], c, o, et % CHUNK, hpatch, ovl);
         }
     }
 }
 
-// A float of the shared memory of CTA `owner` of this cluster (this CTA's own when owner == self).
+// A float (double) of the shared memory of CTA `owner` of this cluster (this CTA's own when owner == self).
 __device__ __forceinline__ float cluster_f32(const float* local, uint32_t owner, uint32_t self) {
     return owner == self ? *local : ld_cluster_f32(map_to_rank(smem_addr(local), owner));
 }
+__device__ __forceinline__ double cluster_f64(const double* local, uint32_t owner, uint32_t self) {
+    return owner == self ? *local : ld_cluster_f64(map_to_rank(smem_addr(local), owner));
+}
 
-// Inverse CDF inside piece ft of the row (warp-collective): the chunk whose running mass (from `before`)
-// first exceeds tp, from the chunk masses its CTA kept (chunks 8 l .. 8 l + 7 to lane l), then the element
+// Inverse CDF inside piece ft of the row (warp-collective): the chunk whose running mass (from `before`,
+// accumulated in fp64 like every sum above the chunk) first exceeds tp, from the chunk masses its CTA kept (chunks 8 l .. 8 l + 7 to lane l), then the element
 // inside that chunk from its recomputed values. When rounding leaves no chunk above tp, the last chunk with
 // positive mass; inside the chunk, the last positive element likewise. -1 if the piece has no mass.
 template <class E, bool AL>
 __device__ int pick_in_piece(const float* cm_slot, uint32_t owner, uint32_t self, const unsigned char* trow,
-                             const unsigned char* orow, int mode, int e_begin, int V, float c, float bt, float bo,
-                             int tok, float ht, float tp, float before, int lane) {
+                             const unsigned char* orow, int mode, int e_begin, int V, float c, PairOff o,
+                             int tok, float ht, double tp, double before, int lane) {
     const int nch = (min(PE, V - e_begin) + CHUNK - 1) / CHUNK;
     float cv[8];
-    float loc = 0.f;
+    double loc = 0.0;
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
         const int k = 8 * lane + q;
         cv[q] = k < nch ? cluster_f32(cm_slot + k, owner, self) : 0.f;
-        loc += cv[q];
+        loc += static_cast<double>(cv[q]);
     }
-    const float incl = warp_incl_scan(loc, lane);
-    const unsigned over = __ballot_sync(0xffffffffu, loc > 0.f && before + incl > tp);
-    const unsigned posm = __ballot_sync(0xffffffffu, loc > 0.f);
+    const double incl = warp_incl_scan(loc, lane);
+    const unsigned over = __ballot_sync(0xffffffffu, loc > 0.0 && before + incl > tp);
+    const unsigned posm = __ballot_sync(0xffffffffu, loc > 0.0);
     if (!posm) return -1;
     const int ln = over ? __ffs(over) - 1 : 31 - __clz(posm);
     int chunk = -1;
-    float bchunk = 0.f;
+    double bchunk = 0.0;
     if (lane == ln) {
-        float a = before + incl - loc;
+        double a = before + incl - loc;
         int pk = -1, lp = -1;
-        float bpk = 0.f, blp = 0.f;
+        double bpk = 0.0, blp = 0.0;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-            const float a2 = a + cv[q];
+            const double a2 = a + cv[q];
             if (cv[q] > 0.f) {
                 lp = q;
                 blp = a;
@@ -303,8 +311,8 @@ __device__ int pick_in_piece(const float* cm_slot, uint32_t owner, uint32_t self
     const typename E::Raw ro = mode == 1 ? E::template gload<AL>(orow, e0, V) : rt;
     const int et = (tok >= e0 && tok < e0 + CHUNK) ? tok - e0 : -1;
     float v[8], ovl = 0.f;
-    chunk_values<E>(mode, rt, ro, c, bt, bo, et, ht, v, ovl);
-    float a = bchunk;
+    chunk_values<E>(mode, rt, ro, c, o, et, ht, v, ovl);
+    double a = bchunk;
     int pick = -1, lp = -1;
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
@@ -327,10 +335,12 @@ __global__ void __launch_bounds__(DNT, 1) draw_kernel(const __grid_constant__ DP
     // dynamic shared memory: [ceil(np / cps)][D_CPP] chunk masses of this CTA's pieces, then (bulk-copy
     // mode) one slot per warp holding a target piece and a draft piece, then one mbarrier per warp
     extern __shared__ __align__(128) float d_cm[];
-    __shared__ float s_ht[D_MAX_K + 1], s_pd[D_MAX_K], s_bt[D_MAX_K + 1], s_bo[D_MAX_K], s_btp[D_MAX_K + 1];
+    __shared__ float s_ht[D_MAX_K + 1], s_pd[D_MAX_K];
+    // row offsets: target rows (nm, plain l), the h rows of the chain (l with the Cactus scale), draft rows
+    __shared__ float s_nmt[D_MAX_K + 1], s_ltp[D_MAX_K + 1], s_lt[D_MAX_K], s_nmo[D_MAX_K], s_lo[D_MAX_K];
     __shared__ float s_xt[D_MAX_K], s_xd[D_MAX_K];
     __shared__ int s_tok[D_MAX_K];
-    __shared__ float s_tiles[D_MAX_PIECES];   // piece masses; entry pc is written by CTA pc % cps
+    __shared__ double s_tiles[D_MAX_PIECES];  // piece masses (fp64 sums of chunk masses); entry pc by CTA pc % cps
     __shared__ int s_L;
     const float NINF = __uint_as_float(0xFF800000u);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -384,13 +394,15 @@ __global__ void __launch_bounds__(DNT, 1) draw_kernel(const __grid_constant__ DP
         const float x = j < K ? (tgt ? s_xt[j] : s_xd[j]) : NINF;
         const MaxSum ms = d_row_stats(p, sp, r, c, lane);
         if (lane == 0) {
-            const float beta = beta_of(ms, c);
-            const float pt = prob_of(x, ms, c);   // 0 without a (valid) token
+            const RowOff o = row_off(ms);
+            const float pt = prob_at(x, o, c);   // 0 without a (valid) token
             if (tgt) {
-                s_btp[j] = beta;
+                s_nmt[j] = o.nm;
+                s_ltp[j] = o.l;
                 s_ht[j] = pt;
             } else {
-                s_bo[j] = beta;
+                s_nmo[j] = o.nm;
+                s_lo[j] = o.l;
                 s_pd[j] = pt;
             }
         }
@@ -404,14 +416,14 @@ __global__ void __launch_bounds__(DNT, 1) draw_kernel(const __grid_constant__ DP
             const int j = base + lane;
             bool acc = true;
             if (j < K) {
-                float ht = s_ht[j], bt = s_btp[j];
+                float ht = s_ht[j], lt = s_ltp[j];
                 if (p.cactus) {
                     float log2s;
                     cactus_scalars(s_ht[j], p.delta, ht, log2s);
-                    bt = s_btp[j] + log2s;
+                    lt = s_ltp[j] + log2s;
                 }
                 s_ht[j] = ht;
-                s_bt[j] = bt;
+                s_lt[j] = lt;
                 const float r = philox_uniform(seed, static_cast<uint32_t>(b), static_cast<uint32_t>(j), 0u);
                 acc = r * s_pd[j] < ht;
                 if (rank == 0) {
@@ -443,8 +455,7 @@ __global__ void __launch_bounds__(DNT, 1) draw_kernel(const __grid_constant__ DP
         const int mode = j < K ? 1 : 2;   // 1: residual (h - q)+ against the draft row, 2: the bonus p_target
         const unsigned char* trow = p.target + (static_cast<size_t>(b) * (K + 1) + j) * row_bytes;
         const unsigned char* orow = mode == 1 ? p.draft + (static_cast<size_t>(b) * K + j) * row_bytes : trow;
-        const float bt = mode == 1 ? s_bt[j] : s_btp[K];
-        const float bo = mode == 1 ? s_bo[j] : 0.f;
+        const PairOff po = mode == 1 ? PairOff{s_nmt[j], s_lt[j], s_nmo[j], s_lo[j]} : PairOff{s_nmt[K], s_ltp[K], 0.f, 0.f};
         const float ht = mode == 1 ? s_ht[j] : 0.f;
         const int tok = mode == 1 ? s_tok[j] : -1;
         // bulk copy of piece pc of both rows (the target alone for a bonus row) into this warp's slot
@@ -489,14 +500,14 @@ __global__ void __launch_bounds__(DNT, 1) draw_kernel(const __grid_constant__ DP
             }
             const int et = (tok >= pc * PE && tok < pc * PE + PE) ? tok - pc * PE : -1;
             float cm[PCH];
-            piece_chunk_masses<E>(mode, rt, ro, lane, c, bt, bo, et, ht, cm);
-            float loc = 0.f;
+            piece_chunk_masses<E>(mode, rt, ro, lane, c, po, et, ht, cm);
+            double loc = 0.0;
 #pragma unroll
             for (int q = 0; q < PCH; ++q) {
                 d_cm[i * D_CPP + lane + 32 * q] = cm[q];
-                loc += cm[q];
+                loc += static_cast<double>(cm[q]);
             }
-            const float m = warp_sum(loc);
+            const double m = warp_sum(loc);
             if (lane == 0) s_tiles[pc] = m;
         }
         cluster_sync_all();   // every CTA's masses are in place and visible to the cluster
@@ -504,45 +515,45 @@ __global__ void __launch_bounds__(DNT, 1) draw_kernel(const __grid_constant__ DP
             // piece masses in vocabulary order (np <= 4 * 32: lane l owns pieces seg l .. seg l + seg - 1)
             const int seg = (np + 31) / 32;
             const int lo = min(np, lane * seg), hi = min(np, lo + seg);
-            float tv[4];
-            float local = 0.f;
+            double tv[4];
+            double local = 0.0;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int t = lo + k;
-                tv[k] = t < hi ? cluster_f32(&s_tiles[t], static_cast<uint32_t>(t % cps), rank) : 0.f;
+                tv[k] = t < hi ? cluster_f64(&s_tiles[t], static_cast<uint32_t>(t % cps), rank) : 0.0;
                 local += tv[k];
             }
-            const float incl = warp_incl_scan(local, lane);
-            float excl = __shfl_up_sync(0xffffffffu, incl, 1);
-            if (lane == 0) excl = 0.f;
-            const float Z = __shfl_sync(0xffffffffu, incl, 31);
-            if (p.diag && j < K && lane == 0) p.diag[(static_cast<size_t>(b) * K + j) * 4 + 2] = Z;
+            const double incl = warp_incl_scan(local, lane);
+            double excl = __shfl_up_sync(0xffffffffu, incl, 1);
+            if (lane == 0) excl = 0.0;
+            const double Z = __shfl_sync(0xffffffffu, incl, 31);
+            if (p.diag && j < K && lane == 0) p.diag[(static_cast<size_t>(b) * K + j) * 4 + 2] = static_cast<float>(Z);
             if (j == L) {
                 const float u = philox_uniform(seed, static_cast<uint32_t>(b), static_cast<uint32_t>(L), 1u);
-                if (mode == 1 && !(Z > 0.f)) {
+                if (mode == 1 && !(Z > 0.0)) {
                     // the residual rounded to zero mass: draw from h over the whole row instead
-                    float all = 0.f;
+                    double all = 0.0;
                     for (int e0 = lane * CHUNK; e0 < V; e0 += 32 * CHUNK) {
                         const Raw rt = E::template gload<AL>(trow, e0, V);
                         float2 unused = make_float2(0.f, 0.f);
                         const int et = (tok >= e0 && tok < e0 + CHUNK) ? tok - e0 : -1;
-                        all += chunk_mass_patched<E>(2, rt, rt, c, bt, 0.f, et, ht, unused);
+                        all += static_cast<double>(chunk_mass_patched<E>(2, rt, rt, c, po, et, ht, unused));
                     }
-                    const float tp = u * warp_sum(all);
-                    emitted = scan_pick<E, AL>(c, trow, trow, 2, 0, V, bt, 0.f, tok, ht, tp, 0.f, lane);
+                    const double tp = static_cast<double>(u) * warp_sum(all);
+                    emitted = scan_pick<E, AL>(c, trow, trow, 2, 0, V, po, tok, ht, tp, 0.0, lane);
                 } else {
-                    const float tp = u * Z;
+                    const double tp = static_cast<double>(u) * Z;
                     // first piece whose prefix exceeds tp (else the last piece with mass)
                     int found = -1, lastp = -1;
-                    float before_found = 0.f, before_last = 0.f;
-                    float run = excl;
+                    double before_found = 0.0, before_last = 0.0;
+                    double run = excl;
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const int t = lo + k;
                         if (t < hi) {
-                            const float m = tv[k];
-                            const float pre = run + m;
-                            if (m > 0.f) {
+                            const double m = tv[k];
+                            const double pre = run + m;
+                            if (m > 0.0) {
                                 lastp = t;
                                 before_last = run;
                                 if (found < 0 && pre > tp) {
@@ -555,7 +566,7 @@ __global__ void __launch_bounds__(DNT, 1) draw_kernel(const __grid_constant__ DP
                     }
                     const unsigned hit = __ballot_sync(0xffffffffu, found >= 0);
                     int ft;
-                    float before_piece;
+                    double before_piece;
                     if (hit) {
                         const int ln = __ffs(hit) - 1;
                         ft = __shfl_sync(0xffffffffu, found, ln);
@@ -568,7 +579,7 @@ __global__ void __launch_bounds__(DNT, 1) draw_kernel(const __grid_constant__ DP
                     }
                     if (ft >= 0)
                         emitted = pick_in_piece<E, AL>(d_cm + (ft / cps) * D_CPP, static_cast<uint32_t>(ft % cps), rank,
-                                                       trow, orow, mode, ft * PE, V, c, bt, bo, tok, ht, tp,
+                                                       trow, orow, mode, ft * PE, V, c, po, tok, ht, tp,
                                                        before_piece, lane);
                 }
             }

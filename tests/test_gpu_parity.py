@@ -1,8 +1,9 @@
 """GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the same seeded inputs.
 
-Small cases span several 256-token tiles, several CTAs of a cluster (forced cluster sizes), a ragged last
-slice, unaligned rows (V odd: element-wise staging instead of bulk copies) and fp32 logits; the five named
-workloads run at full size (the largest checked on a stated sample of sequences through seq_index).
+Small cases span several 2048-logit pieces, forced statistics grids (rows cut into per-warp segments at
+different places), a ragged last piece, unaligned rows (V not a multiple of 8: element-wise loads instead of
+bulk copies) and fp32 logits; the five named workloads run at full size (the largest checked on a stated
+sample of sequences through seq_index).
 """
 import numpy as np
 import pytest
@@ -23,16 +24,13 @@ def _lib():
         pytest.skip("needs a GPU")
     sv.load(build_if_missing=True)
     yield
-    sv.set_cluster_size(0)
     sv.set_stats_grid(0)
 
 
 @pytest.fixture(autouse=True)
-def _auto_cluster():
-    sv.set_cluster_size(0)
+def _auto_grid():
     sv.set_stats_grid(0)
     yield
-    sv.set_cluster_size(0)
     sv.set_stats_grid(0)
 
 
@@ -85,7 +83,7 @@ def test_verify_stats_grid_invariance():
         sv.set_stats_grid(ctas)
         o = sv.verify(g["target"], g["draft"], g["tokens"], g["seeds"])
         torch.cuda.synchronize()
-        assert sv.last_plan()["clusters"] == (ctas or sv.last_plan()["clusters"])
+        assert sv.last_plan()["ctas"] == (ctas or sv.last_plan()["ctas"])
         assert_diag(o, ref)
         assert_chain(o, ref, w.K)
         outs.append(o)
@@ -298,9 +296,8 @@ def test_cactus_named_workload_sampled():
 # ------------------------------------------------------------------------------------------------
 # HedgeSpec counterfactual gamma
 # ------------------------------------------------------------------------------------------------
-@pytest.mark.parametrize("V,C,selected", [(5000, 0, -1), (5000, 0, 1), (33333, 8, 2), (33336, 4, 0)])
-def test_counterfactual_small(V, C, selected):
-    sv.set_cluster_size(C)
+@pytest.mark.parametrize("V,selected", [(5000, -1), (5000, 1), (33333, 2), (33336, 0)])
+def test_counterfactual_small(V, selected):
     w = small(V, B=5, K=4, sigmas=(0.5, 1.0, 2.0, 4.0), selected=max(selected, 0))
     inp = workloads.make(w)
     ref = oracle.counterfactual(host(inp["target"]), host(inp["drafters"]), w.temperature, selected,
@@ -321,6 +318,33 @@ def test_counterfactual_small(V, C, selected):
         torch.cuda.synchronize()
         assert_diag(v, ref)
         assert_chain(v, ref, w.K)
+
+
+@pytest.mark.parametrize("V,dtype,sigmas,B,K,selected", [
+    (140000, "bf16", (0.5, 1.5, 3.0), 3, 2, 1),      # 69 pieces a row: pieces past the tensor-memory share
+    (70000, "fp32", (1.0, 2.0, 4.0), 3, 2, -1),      # fp32 pieces of 1024 logits, also past the share
+    (1000, "fp32", (0.5, 2.0), 4, 5, 0),             # one piece a row: 15 of 16 warps idle
+    (20001, "bf16", (0.5, 1.0, 2.0, 3.0, 6.0), 2, 3, 4),   # element-wise loads (V not a multiple of 8)
+    (128256, "bf16", (0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0), 24, 5, 2),   # more units than CTAs
+])
+def test_counterfactual_shapes(V, dtype, sigmas, B, K, selected):
+    """The gamma kernel across row lengths, element types and unit counts: every CTA run starting inside a
+    position (its own copy of the target row's statistics), rows longer than the tensor-memory share,
+    one-piece rows and the element-wise path."""
+    w = small(V, B=B, K=K, dtype=dtype, sigmas=sigmas, selected=max(selected, 0))
+    inp = workloads.make(w)
+    ref = oracle.counterfactual(host(inp["target"]), host(inp["drafters"]), w.temperature, selected,
+                                inp["tokens"].numpy(), inp["seeds"].numpy().astype(np.uint64))
+    g = to_device(inp)
+    out = sv.counterfactual_gamma(g["target"], g["drafters"], w.temperature, selected, g["tokens"], g["seeds"])
+    torch.cuda.synchronize()
+    assert sv.read_status(out["workspace"]) == 0
+    gam = out["gamma"].cpu().numpy()
+    assert np.abs(gam - ref["gamma"]).max() <= PROB_TOL
+    assert np.abs(out["loss"].cpu().numpy() - (1 - ref["gamma"])).max() <= PROB_TOL
+    if selected >= 0:
+        assert_diag(out, ref)
+        assert_chain(out, ref, w.K)
 
 
 def test_counterfactual_named_full():

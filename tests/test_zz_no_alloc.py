@@ -35,7 +35,7 @@ def _static_call(lib, inp, w, stream):
 @pytest.mark.parametrize("name,B", [("sps_llama3_b64_k5", 16), ("tiny_sps_v1000", 8)])
 def test_static_scratch_matches_workspace_entry(name, B):
     lib = sv.load()
-    lib.spec_debug_set_cluster_size(0)
+    lib.spec_debug_set_stats_grid(0)
     w = workloads.WORKLOADS[name].scaled(B=B)
     stream = torch.cuda.current_stream()
     for call in range(2):   # two calls in a row: the second reuses the region the first one left behind
