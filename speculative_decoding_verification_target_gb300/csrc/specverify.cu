@@ -260,6 +260,8 @@ spec_status run_gamma(const Call& a, bool aligned) {
     const int pe = G_PIECE_BYTES / eb;
     g.np = (a.V + pe - 1) / pe;
     g.U = static_cast<long long>(a.B) * a.K * (a.N + 1) + (chain ? a.B : 0);
+    if (g.U >= (1LL << 31))
+        return fail(SPEC_ERR_UNSUPPORTED, "B (K (N + 1) + 1) = %lld rows exceed the gamma kernel's 2^31 row index", g.U);
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

@@ -38,7 +38,7 @@ struct CgParams {
     const unsigned char* drafters;   // [N, B, K, V]
     int B, K, V, N;
     int np;                          // pieces per row
-    long long U;                     // units in all
+    long long U;                     // units in all (< 2^31)
     int G;                           // CTAs
     float c;                         // log2(e) / temperature
     int tma;                         // 1: rows 16-byte aligned and V a multiple of 8 -> bulk copies
@@ -51,41 +51,68 @@ struct CgParams {
 // row_ms layout (the one draw_kernel reads): target row (b, j) at b (K + 1) + j for j <= K, then the rows
 // of drafter `selected` at B (K + 1) + b K + j.
 
-struct GUnit {
-    const unsigned char* row;   // the row pass 1 reads
-    const unsigned char* trow;  // the target row of the position (pass 2 of a D unit)
-    int kind;                   // 0: T unit of (b, j); 1: D unit of drafter i at (b, j); 2: bonus row (b, K)
-    int b, j, i;
-};
+// A CTA's run of units, walked in order with no division per step. Unit u < B K (N + 1) is position
+// (b, j) = divmod(u / (N + 1), K) with k = u mod (N + 1): k = 0 the T unit, else the D unit of drafter k - 1;
+// unit u >= B K (N + 1) is the bonus row of sequence u - B K (N + 1). A run that starts inside a position
+// (k > 0) is preceded by that position's T unit.
+struct UnitSeq {
+    int b, j, k;       // position and unit within it (k = N + 1 marks the bonus row of sequence b)
+    int t;             // index in the run
 
-__device__ __forceinline__ GUnit g_unit(const CgParams& p, long long u, size_t row_bytes) {
-    GUnit r;
-    const long long nd = static_cast<long long>(p.B) * p.K * (p.N + 1);
-    if (u < nd) {
-        const long long item = u / (p.N + 1);
-        const int k = static_cast<int>(u - item * (p.N + 1));
-        r.b = static_cast<int>(item / p.K);
-        r.j = static_cast<int>(item - static_cast<long long>(r.b) * p.K);
-        r.trow = p.target + (static_cast<size_t>(r.b) * (p.K + 1) + r.j) * row_bytes;
-        if (k == 0) {
-            r.kind = 0;
-            r.i = -1;
-            r.row = r.trow;
+    __device__ void set(const CgParams& p, int u) {
+        const int nd = p.B * p.K * (p.N + 1);
+        if (u < nd) {
+            const int item = u / (p.N + 1);
+            k = u - item * (p.N + 1);
+            b = item / p.K;
+            j = item - b * p.K;
         } else {
-            r.kind = 1;
-            r.i = k - 1;
-            r.row = p.drafters + ((static_cast<size_t>(r.i) * p.B + r.b) * p.K + r.j) * row_bytes;
+            b = u - nd;
+            j = p.K;
+            k = p.N + 1;
         }
-    } else {
-        r.kind = 2;
-        r.b = static_cast<int>(u - nd);
-        r.j = p.K;
-        r.i = -1;
-        r.trow = p.target + (static_cast<size_t>(r.b) * (p.K + 1) + p.K) * row_bytes;
-        r.row = r.trow;
     }
-    return r;
-}
+    // the run starting at unit u0; true when it starts inside a position (its T unit is inserted first)
+    __device__ bool start(const CgParams& p, int u0) {
+        t = 0;
+        set(p, u0);
+        const bool pre = k > 0 && k <= p.N;
+        if (pre) k = 0;
+        return pre;
+    }
+    __device__ void next(const CgParams& p, bool pre, int u0) {
+        ++t;
+        if (t == 1 && pre) {
+            set(p, u0);
+            return;
+        }
+        if (k == p.N + 1) {   // bonus rows follow one another
+            ++b;
+            return;
+        }
+        if (++k == p.N + 1) {
+            k = 0;
+            if (++j == p.K) {
+                j = 0;
+                if (++b == p.B) {   // past the last position: the bonus rows
+                    b = 0;
+                    j = p.K;
+                    k = p.N + 1;
+                }
+            }
+        }
+    }
+    __device__ int kind(const CgParams& p) const { return k == 0 ? 0 : (k == p.N + 1 ? 2 : 1); }
+    __device__ int drafter() const { return k - 1; }
+    __device__ const unsigned char* trow(const CgParams& p, size_t row_bytes) const {
+        return p.target + (static_cast<size_t>(b) * (p.K + 1) + j) * row_bytes;
+    }
+    // the row pass 1 reads
+    __device__ const unsigned char* row(const CgParams& p, size_t row_bytes) const {
+        if (k == 0 || k == p.N + 1) return trow(p, row_bytes);
+        return p.drafters + ((static_cast<size_t>(k - 1) * p.B + b) * p.K + j) * row_bytes;
+    }
+};
 
 // ---------------------------------------- tensor memory ----------------------------------------
 // A warp may address only the 32 lanes of its quarter (warp index mod 4). Each thread stores / loads 32
@@ -137,17 +164,49 @@ struct GPiece<Bf16> {
 #pragma unroll
         for (int q = 0; q < NCH; ++q) r[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
     }
-    // one chunk from global memory through the read-only path without L1 allocation, normal L2 policy
-    // (target rows are read again by the position's next drafters). Chunks at or past n_el are -inf.
-    __device__ static Bf16::Raw ld_keep(const unsigned char* row, int e0, int n_el) {
+    // one chunk from global memory through the read-only path, no L1 allocation, L2 eviction policy `pol`;
+    // chunks at or past n_el are -inf (ld_full: the chunk is known to be in range)
+    __device__ static Bf16::Raw ld_keep(const unsigned char* row, int e0, int n_el, uint64_t pol) {
         uint4 v = Bf16::ninf();
         const uint4* ptr = reinterpret_cast<const uint4*>(row) + e0 / CHUNK;
         asm volatile(
             "{\n\t.reg .pred q;\n\tsetp.lt.s32 q, %4, %5;\n\t"
-            "@q ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%6];\n\t}"
+            "@q ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%6], %7;\n\t}"
             : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w)
-            : "r"(e0), "r"(n_el), "l"(ptr));
+            : "r"(e0), "r"(n_el), "l"(ptr), "l"(pol));
         return v;
+    }
+    __device__ static Bf16::Raw ld_full(const unsigned char* row, int e0, uint64_t pol) {
+        uint4 v;
+        const uint4* ptr = reinterpret_cast<const uint4*>(row) + e0 / CHUNK;
+        asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                     : "l"(ptr), "l"(pol));
+        return v;
+    }
+    // the piece's 32 words to / from this thread's lane, columns [taddr, taddr + 32)
+    __device__ static void tmem_st(uint32_t taddr, const Bf16::Raw (&r)[NCH]) {
+        asm volatile(
+            "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+            "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+            "r"(r[0].x), "r"(r[0].y), "r"(r[0].z), "r"(r[0].w), "r"(r[1].x), "r"(r[1].y), "r"(r[1].z), "r"(r[1].w),
+            "r"(r[2].x), "r"(r[2].y), "r"(r[2].z), "r"(r[2].w), "r"(r[3].x), "r"(r[3].y), "r"(r[3].z), "r"(r[3].w),
+            "r"(r[4].x), "r"(r[4].y), "r"(r[4].z), "r"(r[4].w), "r"(r[5].x), "r"(r[5].y), "r"(r[5].z), "r"(r[5].w),
+            "r"(r[6].x), "r"(r[6].y), "r"(r[6].z), "r"(r[6].w), "r"(r[7].x), "r"(r[7].y), "r"(r[7].z), "r"(r[7].w)
+            : "memory");
+    }
+    __device__ static void tmem_ld(uint32_t taddr, Bf16::Raw (&r)[NCH]) {
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+            "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+            "tcgen05.wait::ld.sync.aligned;"
+            : "=r"(r[0].x), "=r"(r[0].y), "=r"(r[0].z), "=r"(r[0].w), "=r"(r[1].x), "=r"(r[1].y), "=r"(r[1].z),
+              "=r"(r[1].w), "=r"(r[2].x), "=r"(r[2].y), "=r"(r[2].z), "=r"(r[2].w), "=r"(r[3].x), "=r"(r[3].y),
+              "=r"(r[3].z), "=r"(r[3].w), "=r"(r[4].x), "=r"(r[4].y), "=r"(r[4].z), "=r"(r[4].w), "=r"(r[5].x),
+              "=r"(r[5].y), "=r"(r[5].z), "=r"(r[5].w), "=r"(r[6].x), "=r"(r[6].y), "=r"(r[6].z), "=r"(r[6].w),
+              "=r"(r[7].x), "=r"(r[7].y), "=r"(r[7].z), "=r"(r[7].w)
+            : "r"(taddr)
+            : "memory");
     }
 };
 template <>
@@ -175,15 +234,35 @@ struct GPiece<F32> {
                                  __uint_as_float(w[8 * q + 6]), __uint_as_float(w[8 * q + 7]));
         }
     }
-    __device__ static F32::Raw ld_keep(const unsigned char* row, int e0, int n_el) {
+    __device__ static void tmem_st(uint32_t taddr, const F32::Raw (&r)[NCH]) {
+        uint32_t w[32];
+        to_words(r, w);
+        tmem_st32(taddr, w);
+    }
+    __device__ static void tmem_ld(uint32_t taddr, F32::Raw (&r)[NCH]) {
+        uint32_t w[32];
+        tmem_ld32(taddr, w);
+        from_words(w, r);
+    }
+    __device__ static F32::Raw ld_keep(const unsigned char* row, int e0, int n_el, uint64_t pol) {
         F32::Raw v = F32::ninf();
         const float* ptr = reinterpret_cast<const float*>(row) + e0;
         asm volatile(
             "{\n\t.reg .pred q;\n\tsetp.lt.s32 q, %8, %9;\n\t"
-            "@q ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%10];\n\t"
-            "@q ld.global.nc.L1::no_allocate.v4.f32 {%4, %5, %6, %7}, [%10+16];\n\t}"
+            "@q ld.global.nc.L1::no_allocate.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%10], %11;\n\t"
+            "@q ld.global.nc.L1::no_allocate.L2::cache_hint.v4.f32 {%4, %5, %6, %7}, [%10+16], %11;\n\t}"
             : "+f"(v.a.x), "+f"(v.a.y), "+f"(v.a.z), "+f"(v.a.w), "+f"(v.b.x), "+f"(v.b.y), "+f"(v.b.z), "+f"(v.b.w)
-            : "r"(e0), "r"(n_el), "l"(ptr));
+            : "r"(e0), "r"(n_el), "l"(ptr), "l"(pol));
+        return v;
+    }
+    __device__ static F32::Raw ld_full(const unsigned char* row, int e0, uint64_t pol) {
+        F32::Raw v;
+        const float* ptr = reinterpret_cast<const float*>(row) + e0;
+        asm volatile(
+            "ld.global.nc.L1::no_allocate.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%8], %9;\n\t"
+            "ld.global.nc.L1::no_allocate.L2::cache_hint.v4.f32 {%4, %5, %6, %7}, [%8+16], %9;"
+            : "=f"(v.a.x), "=f"(v.a.y), "=f"(v.a.z), "=f"(v.a.w), "=f"(v.b.x), "=f"(v.b.y), "=f"(v.b.z), "=f"(v.b.w)
+            : "l"(ptr), "l"(pol));
         return v;
     }
 };
@@ -246,60 +325,99 @@ __global__ void __launch_bounds__(GNT, 1) gamma_kernel(const __grid_constant__ C
     // this warp's columns: lanes 32 (warp mod 4) .. + 31, columns 128 (warp / 4) .. + 127
     const uint32_t twarp = tbase + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + static_cast<uint32_t>((warp >> 2) * G_CAP * 32);
 
-    // this CTA's run of units
-    const long long u0 = static_cast<long long>(blockIdx.x) * p.U / p.G;
-    const long long u1 = static_cast<long long>(blockIdx.x + 1) * p.U / p.G;
-    const long long nd = static_cast<long long>(p.B) * p.K * (p.N + 1);
-    const bool pre = u0 < nd && (u0 % (p.N + 1)) != 0;
-    const long long S = (u1 - u0) + (pre ? 1 : 0);
-    auto unit_of = [&](long long t) -> GUnit {
-        const long long u = pre ? (t == 0 ? u0 - u0 % (p.N + 1) : u0 + t - 1) : u0 + t;
-        return g_unit(p, u, row_bytes);
-    };
+    // this CTA's run of units (the host checks that U fits in 31 bits)
+    const int u0 = static_cast<int>(static_cast<long long>(blockIdx.x) * p.U / p.G);
+    const int u1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * p.U / p.G);
+    UnitSeq first;
+    const bool pre = first.start(p, u0);
+    const int S = (u1 - u0) + (pre ? 1 : 0);
     const int nmine = warp < np ? (np - 1 - warp) / GW + 1 : 0;   // pieces warp, warp + 16, ... of a row
 
-    // ---- ring of pass-1 pieces (bulk copies), the issue walker runs G_R pieces ahead ----
-    const uint64_t pol_first = policy_evict_first(), pol_normal = policy_evict_normal();
-    long long it_t = 0;
+    // ---- ring of pass-1 pieces: the issue walker runs G_R bulk copies ahead of use. Pass 2 reads the target
+    // piece (and a drafter piece past the tensor-memory share) straight from L2 into registers. ----
+    const uint64_t pol_first = policy_evict_first(), pol_normal = policy_evict_normal(), pol_last = policy_evict_last();
+    UnitSeq iu = first;   // the walker's unit
     int it_k = 0;
-    GUnit it_u = unit_of(0);
-    const long long total = S * nmine;
+    const unsigned char* it_row = iu.row(p, row_bytes);
+    int it_kind = iu.kind(p);
+    const long long total = p.tma ? static_cast<long long>(S) * nmine : 0;
     long long issued = 0, copies = 0;
     int islot = 0;
     bool issuing = true;
     auto issue = [&]() {
+        if (issued >= total) return;
         const int pc = warp + GW * it_k;
         const int len = min(PEG, V - pc * PEG);
         if (lane == 0 && issuing) {
             fence_proxy_async_shared();   // the warp's reads of this slot come before the copy refilling it
             const uint32_t bytes = static_cast<uint32_t>(len) * E::BYTES;
             mbar_arrive_expect_tx(&full[islot], bytes);
-            // evict-first where this is the logits' last read; target rows and re-read drafter pieces stay
-            const bool last = it_u.kind == 2 || (it_u.kind == 1 && it_k < G_CAP);
-            bulk_load(ring + static_cast<size_t>(islot) * G_PIECE_BYTES, it_u.row + static_cast<size_t>(pc) * G_PIECE_BYTES,
-                      bytes, &full[islot], last ? pol_first : pol_normal);
+            // evict-first where this is the logits' last read (bonus rows, drafter pieces parked in tensor
+            // memory); evict-last for a position's target row, which its drafters' pass 2 reads again
+            const uint64_t pol = it_kind == 0 ? pol_last : ((it_kind == 2 || it_k < G_CAP) ? pol_first : pol_normal);
+            bulk_load(ring + static_cast<size_t>(islot) * G_PIECE_BYTES, it_row + static_cast<size_t>(pc) * G_PIECE_BYTES,
+                      bytes, &full[islot], pol);
             ++copies;
         }
         ++issued;
         if (++islot == G_R) islot = 0;
         if (++it_k == nmine) {
             it_k = 0;
-            if (++it_t < S) it_u = unit_of(it_t);
+            iu.next(p, pre, u0);
+            if (iu.t < S) {
+                it_row = iu.row(p, row_bytes);
+                it_kind = iu.kind(p);
+            }
         }
     };
-    if (p.tma)
-        for (int q = 0; q < G_R && issued < total; ++q) issue();
+    for (int q = 0; q < G_R; ++q) issue();
     int cslot = 0;
     uint32_t cpar = 0;
     bool ok = true;
+    // the next piece of the ring into registers (chunks past len are -inf), then its slot is refilled
+    auto take = [&](Raw (&r)[NCH], int len) {
+        if (ok) ok = mbar_wait_bounded(&full[cslot], cpar, p.status, STATUS_TIMEOUT, WAIT_LIMIT_NS);
+        if (lane == 0 && !ok) issuing = false;
+        const unsigned char* slot = ring + static_cast<size_t>(cslot) * G_PIECE_BYTES;
+        if (len == PEG) {
+#pragma unroll
+            for (int q = 0; q < NCH; ++q) r[q] = E::lds(slot, lane + 32 * q);
+        } else {
+            const int nch = (len + CHUNK - 1) / CHUNK;
+#pragma unroll
+            for (int q = 0; q < NCH; ++q) {
+                const int kk = lane + 32 * q;
+                r[q] = kk < nch ? E::lds(slot, kk) : E::ninf();
+            }
+        }
+        __syncwarp();
+        if (++cslot == G_R) {
+            cslot = 0;
+            cpar ^= 1u;
+        }
+        issue();
+    };
+    // element-wise loads of a piece (rows of any alignment; the unit geometry is recomputed here, off the
+    // bulk-copy path)
+    auto gather = [&](Raw (&r)[NCH], const unsigned char* row, size_t poff, int len) {
+        const unsigned char* piece = row + poff;
+#pragma unroll
+        for (int q = 0; q < NCH; ++q) r[q] = E::template gload<false>(piece, (lane + 32 * q) * CHUNK, len);
+    };
 
-    GUnit prev = it_u;   // unit s - 1 (valid from step 1 on)
+    int prev_kind = -1;                   // kind of unit s - 1
+    size_t prev_gidx = 0;                 // its gamma index when it is a D unit
+    const unsigned char* prev_trow = nullptr;   // its rows (pass 2 of a D unit)
+    const unsigned char* prev_row = nullptr;
+    bool prev_last = false;               // it is its position's last drafter
     float pend_bt = 0.f, pend_bd = 0.f;   // log2 offsets of unit s - 1 when it is a D unit
     float bt_item = 0.f;                  // log2 offset of the latest T unit's row
-    for (long long s = 0; s <= S; ++s) {
+    UnitSeq cu = first;   // the consumer's unit (unit s)
+    for (int s = 0; s <= S; ++s) {
         const bool has1 = s < S;
-        const GUnit cur = has1 ? unit_of(s) : prev;
-        const bool has2 = s >= 1 && prev.kind == 1;
+        const int kind1 = has1 ? cu.kind(p) : -1;
+        const unsigned char* cur_row = p.tma ? nullptr : cu.row(p, row_bytes);
+        const bool has2 = prev_kind == 1;
         float m = NINF, sm = 0.f;
         float2 acc = make_float2(0.f, 0.f);
         for (int k = 0; k < nmine; ++k) {
@@ -309,59 +427,41 @@ __global__ void __launch_bounds__(GNT, 1) gamma_kernel(const __grid_constant__ C
             if (has2) {   // pass 2 of unit s - 1: the target piece from L2, the drafter piece from tensor memory
                 Raw rt[NCH], rd[NCH];
                 if (p.tma) {
+                    // the target row stays in L2 for the position's next drafter; the last one lets it go
+                    const uint64_t tpol = prev_last ? pol_first : pol_last;
+                    const unsigned char* tp = prev_trow + poff;
+                    if (len == PEG) {
 #pragma unroll
-                    for (int q = 0; q < NCH; ++q) rt[q] = GPiece<E>::ld_keep(prev.trow + poff, (lane + 32 * q) * CHUNK, len);
+                        for (int q = 0; q < NCH; ++q) rt[q] = GPiece<E>::ld_full(tp, (lane + 32 * q) * CHUNK, tpol);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < NCH; ++q) rt[q] = GPiece<E>::ld_keep(tp, (lane + 32 * q) * CHUNK, len, tpol);
+                    }
                 } else {
-#pragma unroll
-                    for (int q = 0; q < NCH; ++q) rt[q] = E::template gload<false>(prev.trow + poff, (lane + 32 * q) * CHUNK, len);
+                    gather(rt, prev_trow, poff, len);
                 }
                 if (k < G_CAP) {
-                    uint32_t w[32];
-                    tmem_ld32(twarp + 32 * k, w);
-                    GPiece<E>::from_words(w, rd);
+                    GPiece<E>::tmem_ld(twarp + 32 * k, rd);
                 } else if (p.tma) {
 #pragma unroll
-                    for (int q = 0; q < NCH; ++q) rd[q] = E::template gload<true>(prev.row + poff, (lane + 32 * q) * CHUNK, len);
+                    for (int q = 0; q < NCH; ++q) rd[q] = E::template gload<true>(prev_row + poff, (lane + 32 * q) * CHUNK, len);
                 } else {
-#pragma unroll
-                    for (int q = 0; q < NCH; ++q) rd[q] = E::template gload<false>(prev.row + poff, (lane + 32 * q) * CHUNK, len);
+                    gather(rd, prev_row, poff, len);
                 }
                 g_overlap<E>(rt, rd, c, pend_bt, pend_bd, acc);
             }
             if (has1) {   // pass 1 of unit s
                 Raw r1[NCH];
-                if (p.tma) {
-                    if (ok) ok = mbar_wait_bounded(&full[cslot], cpar, p.status, STATUS_TIMEOUT, WAIT_LIMIT_NS);
-                    if (lane == 0 && !ok) issuing = false;
-                    const int nch = (len + CHUNK - 1) / CHUNK;
-                    const unsigned char* slot = ring + static_cast<size_t>(cslot) * G_PIECE_BYTES;
-#pragma unroll
-                    for (int q = 0; q < NCH; ++q) {
-                        const int kk = lane + 32 * q;
-                        r1[q] = kk < nch ? E::lds(slot, kk) : E::ninf();
-                    }
-                    __syncwarp();
-                    if (++cslot == G_R) {
-                        cslot = 0;
-                        cpar ^= 1u;
-                    }
-                    if (issued < total) issue();
-                } else {
-#pragma unroll
-                    for (int q = 0; q < NCH; ++q) r1[q] = E::template gload<false>(cur.row + poff, (lane + 32 * q) * CHUNK, len);
-                }
-                if (cur.kind == 1 && k < G_CAP) {   // park the drafter piece (its columns were read above)
-                    uint32_t w[32];
-                    GPiece<E>::to_words(r1, w);
-                    tmem_st32(twarp + 32 * k, w);
-                }
+                if (p.tma) take(r1, len);
+                else gather(r1, cur_row, poff, len);
+                if (kind1 == 1 && k < G_CAP) GPiece<E>::tmem_st(twarp + 32 * k, r1);   // its columns were read above
                 g_stats<E>(r1, c, m, sm);
             }
         }
         if (has1) {
             const MaxSum w = warp_ms(MaxSum{m, sm}, c);
             if (lane == 0) s_ms[s & 1][warp] = make_float2(w.m, w.s);
-            if (cur.kind == 1) tmem_wait_st();
+            if (kind1 == 1) tmem_wait_st();
         }
         if (has2) {
             const float g = warp_sum(acc.x + acc.y);
@@ -371,30 +471,35 @@ __global__ void __launch_bounds__(GNT, 1) gamma_kernel(const __grid_constant__ C
         if (has2 && warp == GW - 1) {   // gamma of unit s - 1: the 16 partials in warp order
             const float g = warp_sum(lane < GW ? s_g[s & 1][lane] : 0.f);
             if (lane == 0) {
-                const size_t o = (static_cast<size_t>(prev.i) * p.B + prev.b) * p.K + prev.j;
-                p.gamma[o] = g;
-                if (p.loss) p.loss[o] = 1.f - g;
+                p.gamma[prev_gidx] = g;
+                if (p.loss) p.loss[prev_gidx] = 1.f - g;
             }
         }
+        prev_kind = kind1;
         if (has1) {   // the row's (max, sum): the 16 warp pairs merged in warp order, the same in every warp
             const float2 v = lane < GW ? s_ms[s & 1][lane] : make_float2(NINF, 0.f);
             const MaxSum r = warp_ms(MaxSum{v.x, v.y}, c);
             const float beta = beta_of(r, c);
-            if (cur.kind == 1) {
+            if (kind1 == 1) {
+                const int i = cu.drafter();
                 pend_bt = bt_item;
                 pend_bd = beta;
-            } else if (cur.kind == 0) {
+                prev_gidx = (static_cast<size_t>(i) * p.B + cu.b) * p.K + cu.j;
+                prev_trow = cu.trow(p, row_bytes);
+                prev_row = cu.row(p, row_bytes);
+                prev_last = i == p.N - 1;
+            } else if (kind1 == 0) {
                 bt_item = beta;
             }
             if (p.row_ms && warp == 0 && lane == 0) {
                 long long ri = -1;
-                if (cur.kind != 1) ri = static_cast<long long>(cur.b) * (p.K + 1) + cur.j;
-                else if (cur.i == p.selected)
-                    ri = static_cast<long long>(p.B) * (p.K + 1) + static_cast<long long>(cur.b) * p.K + cur.j;
+                if (kind1 != 1) ri = static_cast<long long>(cu.b) * (p.K + 1) + cu.j;
+                else if (cu.drafter() == p.selected)
+                    ri = static_cast<long long>(p.B) * (p.K + 1) + static_cast<long long>(cu.b) * p.K + cu.j;
                 if (ri >= 0) p.row_ms[ri] = make_float2(r.m, r.s);
             }
+            cu.next(p, pre, u0);
         }
-        prev = cur;
     }
 
     // after a failed wait, copies may still be in flight: they must land before the CTA may exit
