@@ -143,11 +143,10 @@ def max_over_ranks(pg, torch, v, device):
 # ------------------------------------------------------------------------------------------------
 # CPU oracle timing (reference arm and cpu_baseline)
 # ------------------------------------------------------------------------------------------------
-# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one row-kernel launch, from an ncu capture of
-# this benchmark's own command (profiles/), keyed by a hash of the kernel sources it was taken with: when the
-# sources change the recorded number no longer applies and the JSON line reports null.
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one call (both kernels), from an ncu capture
+# of this benchmark's own command (profiles/), keyed by a hash of the kernel sources it was taken with: when
+# the sources change the recorded number no longer applies and the JSON line reports null.
 RECORDED_TRAFFIC = {
-    "da891611c878ba80": {"sps_llama3_b64_k5": 261182720 + 4624384},
 }
 
 
@@ -248,8 +247,8 @@ def run_ours(args, w):
     outt = torch.empty((w.B, w.K + 1), dtype=torch.int32, device=dev)
     gam = torch.empty((w.N, w.B, w.K), dtype=torch.float32, device=dev) if kind == "counterfactual" else None
     stream = torch.cuda.current_stream(dev)
-    # kernels per call: the row kernel and the chain-finish kernel, plus the gamma reduction for gamma calls
-    launches_per_call = 3 if kind == "counterfactual" else 2
+    # kernels per call: the statistics pass (gamma kernel for gamma calls) and the chain-and-draw kernel
+    launches_per_call = 2
 
     def call(bt, s=None):
         if kind == "counterfactual":
@@ -354,9 +353,9 @@ def run_ours(args, w):
                    "parallelism": "replicas over sequences" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": RECORDED_TRAFFIC.get(kernel_source_hash(), {}).get(w.name), "peak_kind": peak_kind,
-                     "kernel": "rows_kernel (+ the small chain-finish%s kernel): one whole %s call, graph replay "
-                               "timed with CUDA events on the launching stream, divided by the steps" % (
-                                   " and gamma-reduction" if kind == "counterfactual" else "", kind),
+                     "kernel": "%s + draw_kernel: one whole %s call (both kernels), graph replay timed with CUDA "
+                               "events on the launching stream, divided by the steps" % (
+                                   "gamma_kernel" if kind == "counterfactual" else "stats_kernel", kind),
                      "avg_call_us": avg_call_s * 1e6, "eager_call_us": eager_ms * 1e3,
                      "frac_of_8tbs_nominal": achieved / 8000.0},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

@@ -245,6 +245,65 @@ __device__ __forceinline__ double warp_sum(double v) {
     return v;
 }
 
+// Float-float numbers: an unevaluated sum hi + lo of two floats with |lo| <= ulp(hi) / 2, about 44
+// significant bits, built on the error-free sum of two floats (Knuth's TwoSum; Dekker's FastTwoSum when the
+// first operand is the larger). The intrinsics keep the compiler from contracting or reordering the steps.
+struct FF {
+    float hi, lo;
+};
+__device__ __forceinline__ FF ff_two_sum(float a, float b) {
+    const float s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+    return {s, e};
+}
+__device__ __forceinline__ FF ff_fast_two_sum(float a, float b) {
+    const float s = __fadd_rn(a, b);
+    return {s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+__device__ __forceinline__ FF ff_add(FF a, FF b) {
+    const FF s = ff_two_sum(a.hi, b.hi);
+    return ff_fast_two_sum(s.hi, __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo)));
+}
+__device__ __forceinline__ FF ff_addf(FF a, float b) {
+    const FF s = ff_two_sum(a.hi, b);
+    return ff_fast_two_sum(s.hi, __fadd_rn(s.lo, a.lo));
+}
+__device__ __forceinline__ FF ff_sub(FF a, FF b) { return ff_add(a, FF{-b.hi, -b.lo}); }
+// a * u for a float u (the product's rounding error recovered with one fused multiply-add)
+__device__ __forceinline__ FF ff_mulf(FF a, float u) {
+    const float p = __fmul_rn(a.hi, u);
+    const float e = __fmaf_rn(a.lo, u, __fmaf_rn(a.hi, u, -p));
+    return ff_fast_two_sum(p, e);
+}
+__device__ __forceinline__ bool ff_gt(FF a, FF b) { return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo); }
+__device__ __forceinline__ FF ff_shfl(FF v, int src) {
+    return {__shfl_sync(0xffffffffu, v.hi, src), __shfl_sync(0xffffffffu, v.lo, src)};
+}
+__device__ __forceinline__ FF ff_shfl_up(FF v, int d) {
+    return {__shfl_up_sync(0xffffffffu, v.hi, d), __shfl_up_sync(0xffffffffu, v.lo, d)};
+}
+__device__ __forceinline__ FF warp_sum(FF v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v = ff_add(v, FF{__shfl_xor_sync(0xffffffffu, v.hi, o), __shfl_xor_sync(0xffffffffu, v.lo, o)});
+    return v;
+}
+// Inclusive scan across the warp (Hillis-Steele, fixed association order).
+__device__ __forceinline__ FF warp_incl_scan_ff(FF v, int lane) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const FF y = ff_shfl_up(v, o);
+        if (lane >= o) v = ff_add(v, y);
+    }
+    return v;
+}
+__device__ __forceinline__ float2 ld_cluster_f32x2(uint32_t addr) {
+    float2 v;
+    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+    return v;
+}
+
 // Online (max, sum of 2^((x - max) c)) pair; s == 0 marks an empty set (every logit -inf).
 struct MaxSum {
     float m, s;

@@ -252,49 +252,51 @@ __device__ __forceinline__ void piece_chunk_masses(int mode, const typename E::R
     }
 }
 
-// A float (double) of the shared memory of CTA `owner` of this cluster (this CTA's own when owner == self).
+// A float (float-float) of the shared memory of CTA `owner` of this cluster (this CTA's own when owner == self).
 __device__ __forceinline__ float cluster_f32(const float* local, uint32_t owner, uint32_t self) {
     return owner == self ? *local : ld_cluster_f32(map_to_rank(smem_addr(local), owner));
 }
-__device__ __forceinline__ double cluster_f64(const double* local, uint32_t owner, uint32_t self) {
-    return owner == self ? *local : ld_cluster_f64(map_to_rank(smem_addr(local), owner));
+__device__ __forceinline__ FF cluster_ff(const float2* local, uint32_t owner, uint32_t self) {
+    const float2 v = owner == self ? *local : ld_cluster_f32x2(map_to_rank(smem_addr(local), owner));
+    return {v.x, v.y};
 }
 
 // Inverse CDF inside piece ft of the row (warp-collective): the chunk whose running mass (from `before`,
-// accumulated in fp64 like every sum above the chunk) first exceeds tp, from the chunk masses its CTA kept (chunks 8 l .. 8 l + 7 to lane l), then the element
+// accumulated in float-float like every sum above the chunk) first exceeds tp, from the chunk masses its CTA kept (chunks 8 l .. 8 l + 7 to lane l), then the element
 // inside that chunk from its recomputed values. When rounding leaves no chunk above tp, the last chunk with
 // positive mass; inside the chunk, the last positive element likewise. -1 if the piece has no mass.
 template <class E, bool AL>
 __device__ int pick_in_piece(const float* cm_slot, uint32_t owner, uint32_t self, const unsigned char* trow,
                              const unsigned char* orow, int mode, int e_begin, int V, float c, PairOff o,
-                             int tok, float ht, double tp, double before, int lane) {
+                             int tok, float ht, FF tp, FF before, int lane) {
     const int nch = (min(PE, V - e_begin) + CHUNK - 1) / CHUNK;
     float cv[8];
-    double loc = 0.0;
+    FF loc = {0.f, 0.f};
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
         const int k = 8 * lane + q;
         cv[q] = k < nch ? cluster_f32(cm_slot + k, owner, self) : 0.f;
-        loc += static_cast<double>(cv[q]);
+        loc = ff_addf(loc, cv[q]);
     }
-    const double incl = warp_incl_scan(loc, lane);
-    const unsigned over = __ballot_sync(0xffffffffu, loc > 0.0 && before + incl > tp);
-    const unsigned posm = __ballot_sync(0xffffffffu, loc > 0.0);
+    const FF incl = warp_incl_scan_ff(loc, lane);
+    const FF end = ff_add(before, incl);
+    const unsigned over = __ballot_sync(0xffffffffu, loc.hi > 0.f && ff_gt(end, tp));
+    const unsigned posm = __ballot_sync(0xffffffffu, loc.hi > 0.f);
     if (!posm) return -1;
     const int ln = over ? __ffs(over) - 1 : 31 - __clz(posm);
     int chunk = -1;
-    double bchunk = 0.0;
+    FF bchunk = {0.f, 0.f};
     if (lane == ln) {
-        double a = before + incl - loc;
+        FF a = ff_sub(end, loc);
         int pk = -1, lp = -1;
-        double bpk = 0.0, blp = 0.0;
+        FF bpk = {0.f, 0.f}, blp = {0.f, 0.f};
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-            const double a2 = a + cv[q];
+            const FF a2 = ff_addf(a, cv[q]);
             if (cv[q] > 0.f) {
                 lp = q;
                 blp = a;
-                if (pk < 0 && a2 > tp) {
+                if (pk < 0 && ff_gt(a2, tp)) {
                     pk = q;
                     bpk = a;
                 }
@@ -305,21 +307,21 @@ __device__ int pick_in_piece(const float* cm_slot, uint32_t owner, uint32_t self
         bchunk = pk >= 0 ? bpk : blp;
     }
     chunk = __shfl_sync(0xffffffffu, chunk, ln);
-    bchunk = __shfl_sync(0xffffffffu, bchunk, ln);
+    bchunk = ff_shfl(bchunk, ln);
     const int e0 = e_begin + chunk * CHUNK;
     const typename E::Raw rt = E::template gload<AL>(trow, e0, V);
     const typename E::Raw ro = mode == 1 ? E::template gload<AL>(orow, e0, V) : rt;
     const int et = (tok >= e0 && tok < e0 + CHUNK) ? tok - e0 : -1;
     float v[8], ovl = 0.f;
     chunk_values<E>(mode, rt, ro, c, o, et, ht, v, ovl);
-    double a = bchunk;
+    FF a = bchunk;
     int pick = -1, lp = -1;
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-        a += v[q];
+        a = ff_addf(a, v[q]);
         if (v[q] > 0.f) {
             lp = q;
-            if (pick < 0 && a > tp) pick = q;
+            if (pick < 0 && ff_gt(a, tp)) pick = q;
         }
     }
     return pick >= 0 ? e0 + pick : (lp >= 0 ? e0 + lp : -1);
@@ -340,7 +342,7 @@ __global__ void __launch_bounds__(DNT, 1) draw_kernel(const __grid_constant__ DP
     __shared__ float s_nmt[D_MAX_K + 1], s_ltp[D_MAX_K + 1], s_lt[D_MAX_K], s_nmo[D_MAX_K], s_lo[D_MAX_K];
     __shared__ float s_xt[D_MAX_K], s_xd[D_MAX_K];
     __shared__ int s_tok[D_MAX_K];
-    __shared__ double s_tiles[D_MAX_PIECES];  // piece masses (fp64 sums of chunk masses); entry pc by CTA pc % cps
+    __shared__ float2 s_tiles[D_MAX_PIECES];  // piece masses (float-float sums of chunk masses); entry pc by CTA pc % cps
     __shared__ int s_L;
     const float NINF = __uint_as_float(0xFF800000u);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -501,36 +503,36 @@ __global__ void __launch_bounds__(DNT, 1) draw_kernel(const __grid_constant__ DP
             const int et = (tok >= pc * PE && tok < pc * PE + PE) ? tok - pc * PE : -1;
             float cm[PCH];
             piece_chunk_masses<E>(mode, rt, ro, lane, c, po, et, ht, cm);
-            double loc = 0.0;
+            FF loc = {0.f, 0.f};
 #pragma unroll
             for (int q = 0; q < PCH; ++q) {
                 d_cm[i * D_CPP + lane + 32 * q] = cm[q];
-                loc += static_cast<double>(cm[q]);
+                loc = ff_addf(loc, cm[q]);
             }
-            const double m = warp_sum(loc);
-            if (lane == 0) s_tiles[pc] = m;
+            const FF m = warp_sum(loc);
+            if (lane == 0) s_tiles[pc] = make_float2(m.hi, m.lo);
         }
         cluster_sync_all();   // every CTA's masses are in place and visible to the cluster
         if (rank == 0 && warp == 0 && !idle) {
             // piece masses in vocabulary order (np <= 4 * 32: lane l owns pieces seg l .. seg l + seg - 1)
             const int seg = (np + 31) / 32;
             const int lo = min(np, lane * seg), hi = min(np, lo + seg);
-            double tv[4];
-            double local = 0.0;
+            FF tv[4];
+            FF local = {0.f, 0.f};
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int t = lo + k;
-                tv[k] = t < hi ? cluster_f64(&s_tiles[t], static_cast<uint32_t>(t % cps), rank) : 0.0;
-                local += tv[k];
+                tv[k] = t < hi ? cluster_ff(&s_tiles[t], static_cast<uint32_t>(t % cps), rank) : FF{0.f, 0.f};
+                local = ff_add(local, tv[k]);
             }
-            const double incl = warp_incl_scan(local, lane);
-            double excl = __shfl_up_sync(0xffffffffu, incl, 1);
-            if (lane == 0) excl = 0.0;
-            const double Z = __shfl_sync(0xffffffffu, incl, 31);
-            if (p.diag && j < K && lane == 0) p.diag[(static_cast<size_t>(b) * K + j) * 4 + 2] = static_cast<float>(Z);
+            const FF incl = warp_incl_scan_ff(local, lane);
+            FF excl = ff_shfl_up(incl, 1);
+            if (lane == 0) excl = FF{0.f, 0.f};
+            const FF Z = ff_shfl(incl, 31);
+            if (p.diag && j < K && lane == 0) p.diag[(static_cast<size_t>(b) * K + j) * 4 + 2] = Z.hi + Z.lo;
             if (j == L) {
                 const float u = philox_uniform(seed, static_cast<uint32_t>(b), static_cast<uint32_t>(L), 1u);
-                if (mode == 1 && !(Z > 0.0)) {
+                if (mode == 1 && !(Z.hi > 0.f)) {
                     // the residual rounded to zero mass: draw from h over the whole row instead
                     double all = 0.0;
                     for (int e0 = lane * CHUNK; e0 < V; e0 += 32 * CHUNK) {
@@ -542,21 +544,21 @@ __global__ void __launch_bounds__(DNT, 1) draw_kernel(const __grid_constant__ DP
                     const double tp = static_cast<double>(u) * warp_sum(all);
                     emitted = scan_pick<E, AL>(c, trow, trow, 2, 0, V, po, tok, ht, tp, 0.0, lane);
                 } else {
-                    const double tp = static_cast<double>(u) * Z;
+                    const FF tp = ff_mulf(Z, u);
                     // first piece whose prefix exceeds tp (else the last piece with mass)
                     int found = -1, lastp = -1;
-                    double before_found = 0.0, before_last = 0.0;
-                    double run = excl;
+                    FF before_found = {0.f, 0.f}, before_last = {0.f, 0.f};
+                    FF run = excl;
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const int t = lo + k;
                         if (t < hi) {
-                            const double m = tv[k];
-                            const double pre = run + m;
-                            if (m > 0.0) {
+                            const FF m = tv[k];
+                            const FF pre = ff_add(run, m);
+                            if (m.hi > 0.f) {
                                 lastp = t;
                                 before_last = run;
-                                if (found < 0 && pre > tp) {
+                                if (found < 0 && ff_gt(pre, tp)) {
                                     found = t;
                                     before_found = run;
                                 }
@@ -566,16 +568,16 @@ __global__ void __launch_bounds__(DNT, 1) draw_kernel(const __grid_constant__ DP
                     }
                     const unsigned hit = __ballot_sync(0xffffffffu, found >= 0);
                     int ft;
-                    double before_piece;
+                    FF before_piece;
                     if (hit) {
                         const int ln = __ffs(hit) - 1;
                         ft = __shfl_sync(0xffffffffu, found, ln);
-                        before_piece = __shfl_sync(0xffffffffu, before_found, ln);
+                        before_piece = ff_shfl(before_found, ln);
                     } else {
                         const unsigned any = __ballot_sync(0xffffffffu, lastp >= 0);
                         const int ln = any ? 31 - __clz(any) : 0;
                         ft = __shfl_sync(0xffffffffu, lastp, ln);
-                        before_piece = __shfl_sync(0xffffffffu, before_last, ln);
+                        before_piece = ff_shfl(before_last, ln);
                     }
                     if (ft >= 0)
                         emitted = pick_in_piece<E, AL>(d_cm + (ft / cps) * D_CPP, static_cast<uint32_t>(ft % cps), rank,

@@ -72,8 +72,8 @@ def test_verify_deterministic():
 
 
 def test_verify_stats_grid_invariance():
-    """The statistics grid only changes how rows are cut into per-warp segments (summation order): every
-    grid meets the oracle bar, and the probabilities agree within the tolerance."""
+    """The statistics grid only changes where the rows are cut into per-warp segments (summation order):
+    every grid meets the oracle bar, and the probabilities agree within the tolerance."""
     w = small(50000, B=8, K=3)
     inp = workloads.make(w)
     ref = oracle_verify(inp)
@@ -83,9 +83,11 @@ def test_verify_stats_grid_invariance():
         sv.set_stats_grid(ctas)
         o = sv.verify(g["target"], g["draft"], g["tokens"], g["seeds"])
         torch.cuda.synchronize()
-        assert sv.last_plan()["ctas"] == (ctas or sv.last_plan()["ctas"])
+        if ctas:
+            assert 1 <= sv.last_plan()["ctas"] <= ctas
         assert_diag(o, ref)
         assert_chain(o, ref, w.K)
+        assert sv.read_status(o["workspace"]) == 0
         outs.append(o)
     for o in outs[1:]:
         assert torch.allclose(o["diag"], outs[0]["diag"], atol=PROB_TOL, rtol=0)
