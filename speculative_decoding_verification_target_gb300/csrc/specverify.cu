@@ -225,6 +225,20 @@ spec_status run_chain(const Call& a, bool aligned) {
     if (ctas > need) ctas = static_cast<int>(need);
     s.G = ctas * SW;
     s.part = reinterpret_cast<float2*>(ws + wl.part_off);
+    // L2 kept for the draw: the rows of the first positions, up to 64 MB (whole positions while they fit,
+    // else position 0 of the first sequences)
+    {
+        const size_t budget = size_t(64) << 20;
+        const size_t pair = 2 * static_cast<size_t>(a.V) * eb;
+        s.K = a.K;
+        const size_t per_position = pair * static_cast<size_t>(a.B);
+        s.keep_j = static_cast<int>(std::min<size_t>(a.K, budget / per_position));
+        s.keep_b = a.B;
+        if (s.keep_j == 0) {
+            s.keep_j = 1;
+            s.keep_b = static_cast<int>(budget / pair);
+        }
+    }
     s.status = reinterpret_cast<unsigned*>(ws);
     g_last_plan[0] = 0;
     g_last_plan[1] = R;

@@ -63,6 +63,9 @@ struct SParams {
     float c;                       // log2(e) / temperature
     int tma;                       // 1: rows 16-byte aligned and V a multiple of CHUNK -> bulk copies
     int R;                         // ring slots per warp
+    int K;                         // draft positions per sequence
+    int keep_j, keep_b;            // rows (b, j) with j < keep_j and b < keep_b are kept in L2 (evict-last)
+                                   // for the draw kernel, which re-reads the row pair of the first reject
     float2* part;                  // (max, sum) of segment (g, r) at entry g + r
     unsigned* status;
 };
@@ -131,11 +134,22 @@ __global__ void __launch_bounds__(SNT, 1) stats_kernel(const __grid_constant__ S
         fence_mbarrier_init_cluster();
     }
     __syncwarp();
-    const uint64_t pol = policy_evict_first();   // every logit is read once here
+    // Every logit is read once here (evict-first), except the rows of the first draft positions: the draw
+    // kernel re-reads the row pair at the sequence's first reject, most often position 0, right after this
+    // grid, and finds them in L2 (evict-last; its own read demotes them).
+    const uint64_t pol_first = policy_evict_first(), pol_last = policy_evict_last();
+    auto row_policy = [&](long long r) -> uint64_t {
+        const long long kp = r < p.rows_a_n ? p.K + 1 : p.K;
+        const long long rr = r < p.rows_a_n ? r : r - p.rows_a_n;
+        const long long b = rr / kp, j = rr - b * kp;
+        return (j < p.keep_j && b < p.keep_b) ? pol_last : pol_first;
+    };
+    uint64_t ipol = 0;
 
     // the issue walker runs R pieces ahead of consumption
     long long irow = row;
     int ipc = pc;
+    ipol = row_policy(irow);
     int islot = 0;
     long long issued = 0;   // pieces the walker has passed
     long long copies = 0;   // lane 0: bulk copies actually started (slot k % R for copy k)
@@ -148,7 +162,7 @@ __global__ void __launch_bounds__(SNT, 1) stats_kernel(const __grid_constant__ S
             const uint32_t bytes = static_cast<uint32_t>(len) * eb;
             mbar_arrive_expect_tx(&full[islot], bytes);
             bulk_load(ring + static_cast<size_t>(islot) * slot_bytes,
-                      s_row<E>(p, irow, row_bytes) + static_cast<size_t>(ipc) * PE * eb, bytes, &full[islot], pol);
+                      s_row<E>(p, irow, row_bytes) + static_cast<size_t>(ipc) * PE * eb, bytes, &full[islot], ipol);
             ++copies;
         }
         ++issued;
@@ -156,6 +170,7 @@ __global__ void __launch_bounds__(SNT, 1) stats_kernel(const __grid_constant__ S
         if (++ipc == p.np) {
             ipc = 0;
             ++irow;
+            ipol = row_policy(irow);
         }
     };
     for (int q = 0; q < R && issued < cnt; ++q) issue();
@@ -342,7 +357,7 @@ __global__ void __launch_bounds__(DNT, 1) draw_kernel(const __grid_constant__ DP
     __shared__ float s_nmt[D_MAX_K + 1], s_ltp[D_MAX_K + 1], s_lt[D_MAX_K], s_nmo[D_MAX_K], s_lo[D_MAX_K];
     __shared__ float s_xt[D_MAX_K], s_xd[D_MAX_K];
     __shared__ int s_tok[D_MAX_K];
-    __shared__ float2 s_tiles[D_MAX_PIECES];  // piece masses (float-float sums of chunk masses); entry pc by CTA pc % cps
+    __shared__ float2 s_tiles[D_MAX_PIECES];  // piece masses (float-float sums of chunk masses), gathered in CTA 0
     __shared__ int s_L;
     const float NINF = __uint_as_float(0xFF800000u);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -510,7 +525,11 @@ __global__ void __launch_bounds__(DNT, 1) draw_kernel(const __grid_constant__ DP
                 loc = ff_addf(loc, cm[q]);
             }
             const FF m = warp_sum(loc);
-            if (lane == 0) s_tiles[pc] = make_float2(m.hi, m.lo);
+            // the piece mass goes straight to CTA 0, which makes the draw
+            if (lane == 0) {
+                if (rank == 0) s_tiles[pc] = make_float2(m.hi, m.lo);
+                else st_cluster_f32x2(map_to_rank(smem_addr(&s_tiles[pc]), 0), m.hi, m.lo);
+            }
         }
         cluster_sync_all();   // every CTA's masses are in place and visible to the cluster
         if (rank == 0 && warp == 0 && !idle) {
@@ -522,7 +541,7 @@ __global__ void __launch_bounds__(DNT, 1) draw_kernel(const __grid_constant__ DP
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int t = lo + k;
-                tv[k] = t < hi ? cluster_ff(&s_tiles[t], static_cast<uint32_t>(t % cps), rank) : FF{0.f, 0.f};
+                tv[k] = t < hi ? FF{s_tiles[t].x, s_tiles[t].y} : FF{0.f, 0.f};
                 local = ff_add(local, tv[k]);
             }
             const FF incl = warp_incl_scan_ff(local, lane);
