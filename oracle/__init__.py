@@ -68,6 +68,14 @@ def _load():
     lib.spec_oracle_verify.restype = i32
     lib.spec_oracle_cactus.argtypes = [i32, P, P, P, P, P, i32, i32, i32, f64, f64, P, P, P, P, P, P, i32]
     lib.spec_oracle_cactus.restype = i32
+    lib.spec_oracle_cactus_ex.argtypes = [i32, P, P, P, P, P, i32, i32, i32, f64, f64, i32, P, P, P, P, P, P, i32]
+    lib.spec_oracle_cactus_ex.restype = i32
+    lib.spec_oracle_cactus_kl.argtypes = [f64, f64]
+    lib.spec_oracle_cactus_kl.restype = f64
+    lib.spec_oracle_cactus_gamma_kl.argtypes = [f64, f64]
+    lib.spec_oracle_cactus_gamma_kl.restype = f64
+    lib.spec_oracle_cactus_h_mode.argtypes = [P, i32, i32, f64, i32, P]
+    lib.spec_oracle_cactus_h_mode.restype = f64
     lib.spec_oracle_counterfactual.argtypes = [i32, P, P, i32, i32, i32, i32, f64, P, P, i32, P, P, P,
                                                P, P, P, P, P, i32]
     lib.spec_oracle_counterfactual.restype = i32
@@ -133,13 +141,24 @@ def sample_one(h, pd, t: int, r: float, u: float, mutation: int = 0):
     return tok, bool(acc[0]), float(z[0]), float(am[0]), float(cm[0])
 
 
-def cactus_h(pt, n: int, delta: float):
-    """Cactus target distribution for candidate n. Returns (h, gamma_star)."""
+def cactus_h(pt, n: int, delta: float, exact: bool = False):
+    """Cactus target distribution for candidate n (Taylor gamma*, or the root of the divergence constraint
+    with exact=True). Returns (h, gamma_star)."""
     lib = _load()
     pt = np.ascontiguousarray(pt, dtype=np.float64)
     h = np.empty_like(pt)
-    g = lib.spec_oracle_cactus_h(_ptr(pt), pt.size, n, delta, _ptr(h))
+    g = lib.spec_oracle_cactus_h_mode(_ptr(pt), pt.size, n, delta, 1 if exact else 0, _ptr(h))
     return h, g
+
+
+def cactus_kl(q: float, g: float) -> float:
+    """KL(h || target) of the Cactus target with h_n = g for a candidate of target probability q."""
+    return _load().spec_oracle_cactus_kl(q, g)
+
+
+def cactus_gamma_kl(q: float, delta: float) -> float:
+    """gamma* as the root of the divergence constraint (no Taylor step), clamped to [q, 1]."""
+    return _load().spec_oracle_cactus_gamma_kl(q, delta)
 
 
 def _seq_index(seq_index, B):
@@ -173,8 +192,9 @@ def verify(target, draft, tokens, seeds, temperature=1.0, seq_index=None, mutati
     return out
 
 
-def cactus(target, draft, tokens, seeds, delta, temperature=1.0, seq_index=None, nthreads=0):
-    """Cactus constrained acceptance; same layout as verify plus delta."""
+def cactus(target, draft, tokens, seeds, delta, temperature=1.0, seq_index=None, nthreads=0, exact=False):
+    """Cactus constrained acceptance; same layout as verify plus delta (exact=True: gamma* as the root of the
+    divergence constraint instead of its Taylor closed form)."""
     lib = _load()
     target, dt = _logits(target)
     draft, dd = _logits(draft)
@@ -188,8 +208,8 @@ def cactus(target, draft, tokens, seeds, delta, temperature=1.0, seq_index=None,
     out = dict(accept_len=np.zeros(B, np.int32), out_tokens=np.zeros((B, K + 1), np.int32),
                diag=np.zeros((B, K, 4)), gamma_star=np.zeros((B, K)), accept_margin=np.zeros((B, K)),
                cdf_margin=np.zeros(B))
-    rc = lib.spec_oracle_cactus(dt, _ptr(target), _ptr(draft), _ptr(tokens), _ptr(seeds), _ptr(si), B, K, V,
-                                float(temperature), float(delta), _ptr(out["accept_len"]),
+    rc = lib.spec_oracle_cactus_ex(dt, _ptr(target), _ptr(draft), _ptr(tokens), _ptr(seeds), _ptr(si), B, K, V,
+                                float(temperature), float(delta), 1 if exact else 0, _ptr(out["accept_len"]),
                                 _ptr(out["out_tokens"]), _ptr(out["diag"]), _ptr(out["gamma_star"]),
                                 _ptr(out["accept_margin"]), _ptr(out["cdf_margin"]), nthreads)
     if rc != 0:

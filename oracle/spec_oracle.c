@@ -16,7 +16,8 @@
  *         Key design 3, loss f_t[i] = 1 - gamma_t[i].
  *  [Cactus] "Cactus: Accelerating Auto-Regressive Decoding with Constrained Acceptance Speculative
  *         Sampling" (Cactus notes): Key design 1 (objective min{h_n/p(n),1}), Key design 2 (closed-form
- *         h), Key design 3 (gamma* Taylor closed form). NOTE: that page writes q for the verifier
+ *         h; gamma* the root of the divergence constraint on [q(n), +inf), clamped to [q(n), 1]), Key
+ *         design 3 (gamma* Taylor closed form, KL divergence). NOTE: that page writes q for the verifier
  *         (target) and p for the draft -- the opposite of [SpS]. This file always says target/draft.
  *  Philox4x32-10: Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3" (SC'11),
  *         the counter-based generator; the pages do not fix a uniform source.
@@ -189,20 +190,61 @@ int spec_oracle_sample_one(const double* h, const double* pd, int V, int t, doub
     return spec_oracle_inverse_cdf(w, V, u * total, cdf_margin);
 }
 
+/* The divergence of the Cactus target from the target row, for candidate probability q = p_target(n) and
+ * h_n = g: with h_i = (1 - g) / (1 - q) p_target(i) for i != n, the sum over i != n factors and
+ * KL(h || p_target) = g ln(g / q) + (1 - g) ln((1 - g) / (1 - q)), with 0 ln 0 = 0. */
+double spec_oracle_cactus_kl(double q, double g)
+{
+    double a = (g > 0.0) ? g * log(g / q) : 0.0;
+    double b = (g < 1.0) ? (1.0 - g) * log((1.0 - g) / (1.0 - q)) : 0.0;
+    return a + b;
+}
+
+/* gamma* without the Taylor step ([Cactus] Key design 2 with the KL divergence of Key design 3): the root
+ * of KL(h || p_target) = delta on [q, +inf), clamped to [q, 1]. The divergence is 0 at g = q and increases
+ * on [q, 1] (its derivative ln(g / q) - ln((1 - g) / (1 - q)) is positive there), so the root is found by
+ * bisection of [q, 1] down to the spacing of doubles. No root below 1 (ln(1/q) <= delta) gives 1; q = 0
+ * gives 0 (every g > 0 has infinite divergence); delta = 0 gives q. */
+double spec_oracle_cactus_gamma_kl(double q, double delta)
+{
+    if (delta <= 0.0 || q <= 0.0) return q;
+    if (q >= 1.0) return 1.0;
+    if (spec_oracle_cactus_kl(q, 1.0) <= delta) return 1.0;
+    double lo = q, hi = 1.0;
+    for (int it = 0; it < 200 && hi - lo > 0.0; it++) {
+        double mid = 0.5 * (lo + hi);
+        if (mid <= lo || mid >= hi) break;
+        if (spec_oracle_cactus_kl(q, mid) <= delta) lo = mid;
+        else hi = mid;
+    }
+    return lo;
+}
+
 /* Cactus target distribution, [Cactus] Key design 2 and 3 (translated: the page's q is the target,
  * its p is the draft). With q = p_target(n) for the candidate n:
- *   gamma* = min(q + sqrt(2 delta q (1 - q)), 1),
+ *   gamma* = min(q + sqrt(2 delta q (1 - q)), 1)  (the Taylor closed form, exact = 0), or the root of
+ *   the divergence constraint (exact = 1, spec_oracle_cactus_gamma_kl),
  *   h_n = gamma*,  h_i = (1 - gamma*) / (1 - q) * p_target(i) for i != n.
  * q = 1 gives gamma* = 1 and the other entries 0. Returns gamma*. */
-double spec_oracle_cactus_h(const double* pt, int V, int n, double delta, double* h)
+double spec_oracle_cactus_h_mode(const double* pt, int V, int n, double delta, int exact, double* h)
 {
     double q = pt[n];
-    double g = q + sqrt(2.0 * delta * q * (1.0 - q));
-    if (g > 1.0) g = 1.0;
+    double g;
+    if (exact) {
+        g = spec_oracle_cactus_gamma_kl(q, delta);
+    } else {
+        g = q + sqrt(2.0 * delta * q * (1.0 - q));
+        if (g > 1.0) g = 1.0;
+    }
     double s = (q < 1.0) ? (1.0 - g) / (1.0 - q) : 0.0;
     for (int i = 0; i < V; i++) h[i] = s * pt[i];
     h[n] = g;
     return g;
+}
+
+double spec_oracle_cactus_h(const double* pt, int V, int n, double delta, double* h)
+{
+    return spec_oracle_cactus_h_mode(pt, V, n, delta, 0, h);
 }
 
 /* ------------------------------------------------------------------------------------------ */
@@ -316,14 +358,15 @@ int spec_oracle_verify(int dtype, const void* target, const void* draft, const i
 }
 
 /* Cactus constrained acceptance over a batch ([Cactus] Key design 1-3 inside the [SpS] §9.1 chain).
- * Same layout as spec_oracle_verify plus delta >= 0 and gamma_star [B, K] (nullable). At each
- * position the target distribution of the chain is h built from the target row and the draft token;
- * the bonus row is the plain target row. diag's first entry is h(t) = gamma*. */
-int spec_oracle_cactus(int dtype, const void* target, const void* draft, const int32_t* tokens,
-                       const uint64_t* seeds, const int32_t* seq_index, int B, int K, int V,
-                       double T, double delta, int32_t* accept_len, int32_t* out_tokens,
-                       double* diag, double* gamma_star, double* accept_margin,
-                       double* cdf_margin, int nthreads)
+ * Same layout as spec_oracle_verify plus delta >= 0, exact (0: the Taylor gamma*, 1: the root of the
+ * divergence constraint) and gamma_star [B, K] (nullable). At each position the target distribution of
+ * the chain is h built from the target row and the draft token; the bonus row is the plain target row.
+ * diag's first entry is h(t) = gamma*. */
+int spec_oracle_cactus_ex(int dtype, const void* target, const void* draft, const int32_t* tokens,
+                          const uint64_t* seeds, const int32_t* seq_index, int B, int K, int V,
+                          double T, double delta, int exact, int32_t* accept_len, int32_t* out_tokens,
+                          double* diag, double* gamma_star, double* accept_margin,
+                          double* cdf_margin, int nthreads)
 {
     if (K < 1 || K > ORACLE_MAX_K || V < 1 || B < 0) return -1;
     int nt = nthreads_or_default(nthreads);
@@ -340,7 +383,7 @@ int spec_oracle_cactus(int dtype, const void* target, const void* draft, const i
             drows[j] = store + (size_t)(K + j) * V;
             load_row(dtype, target, (size_t)b * (K + 1) + j, V, x);
             spec_oracle_softmax(x, V, T, pt);
-            double g = spec_oracle_cactus_h(pt, V, tokens[(size_t)b * K + j], delta, hrows[j]);
+            double g = spec_oracle_cactus_h_mode(pt, V, tokens[(size_t)b * K + j], delta, exact, hrows[j]);
             if (gamma_star) gamma_star[(size_t)b * K + j] = g;
             load_row(dtype, draft, (size_t)b * K + j, V, x);
             spec_oracle_softmax(x, V, T, drows[j]);
@@ -360,6 +403,16 @@ int spec_oracle_cactus(int dtype, const void* target, const void* draft, const i
         free(x);
     }
     return 0;
+}
+
+int spec_oracle_cactus(int dtype, const void* target, const void* draft, const int32_t* tokens,
+                       const uint64_t* seeds, const int32_t* seq_index, int B, int K, int V,
+                       double T, double delta, int32_t* accept_len, int32_t* out_tokens,
+                       double* diag, double* gamma_star, double* accept_margin,
+                       double* cdf_margin, int nthreads)
+{
+    return spec_oracle_cactus_ex(dtype, target, draft, tokens, seeds, seq_index, B, K, V, T, delta, 0, accept_len,
+                                 out_tokens, diag, gamma_star, accept_margin, cdf_margin, nthreads);
 }
 
 /* HedgeSpec counterfactual evaluation ([Hedge] Key design 1): for every drafter i, sequence b and

@@ -491,3 +491,77 @@ def test_cactus_batched_chi2():
     c = np.bincount(out["out_tokens"][:, 0], minlength=V)
     assert _chi2_p(c, direct) > 1e-6
     assert _chi2_p(c, pt) < 1e-6        # lossy by design for delta > 0
+
+
+# ----------------------------------------------------------------------------------------------
+# Cactus gamma* as the root of the divergence constraint (no Taylor step)
+# ----------------------------------------------------------------------------------------------
+def test_cactus_exact_root_meets_the_constraint():
+    """[Cactus] Key design 2: gamma* is the root of D_KL(h || target) = delta on [q(n), 1] (clamped). The
+    divergence is recomputed here from the whole distribution h, not from the oracle's two-term form."""
+    rng = np.random.default_rng(50)
+    for _ in range(400):
+        V = int(rng.integers(2, 40))
+        pt = special.softmax(rng.normal(0, rng.uniform(0.2, 5), V))
+        n = int(rng.integers(0, V))
+        delta = float(rng.choice([1e-4, 1e-2, 0.1, 0.5, 0.75, 1.0, 3.0]))
+        h, gs = oracle.cactus_h(pt, n, delta, exact=True)
+        q = pt[n]
+        assert q <= gs <= 1.0
+        assert h.sum() == pytest.approx(1.0, abs=1e-12) and h[n] == gs
+        if np.log(1.0 / q) > delta:      # a root below 1 exists
+            assert _kl(h, pt) == pytest.approx(delta, rel=1e-9, abs=1e-12)
+        else:
+            assert gs == 1.0
+        assert oracle.cactus_kl(q, gs) == pytest.approx(_kl(h, pt), rel=1e-9, abs=1e-13)
+
+
+def test_cactus_exact_root_against_taylor():
+    """Corollary 6 of the page: where the Taylor gamma* is at most 0.5 it meets KL <= delta, so it lies at or
+    below the root; as delta -> 0 the two agree to first order (the Taylor step drops an O(delta) term)."""
+    rng = np.random.default_rng(51)
+    for _ in range(2000):
+        q = float(np.exp(rng.uniform(np.log(1e-6), np.log(0.999))))
+        delta = float(np.exp(rng.uniform(np.log(1e-8), np.log(3.0))))
+        ex = oracle.cactus_gamma_kl(q, delta)
+        ty = min(q + np.sqrt(2 * delta * q * (1 - q)), 1.0)
+        if ty <= 0.5:
+            assert ty <= ex + 1e-15
+        if delta <= 1e-6:
+            assert abs(ex - ty) <= 10 * delta
+    for q in (1e-4, 0.2, 0.6, 0.97):
+        assert oracle.cactus_gamma_kl(q, 0.0) == q
+        gs = [oracle.cactus_gamma_kl(q, d) for d in (1e-5, 1e-3, 0.1, 0.5, 2.0)]
+        assert all(a <= b for a, b in zip(gs, gs[1:]))        # monotone in delta
+    assert oracle.cactus_gamma_kl(0.0, 0.5) == 0.0             # q = 0: every g > 0 has infinite divergence
+    assert oracle.cactus_gamma_kl(1.0, 0.5) == 1.0
+
+
+@pytest.mark.parametrize("delta", [0.2, 1.0])
+def test_cactus_exact_root_law(delta):
+    """The chain with the exact gamma* produces the law its acceptance rule states (exact enumeration), and
+    the batched oracle reports the root as gamma*."""
+    rng = np.random.default_rng(60 + int(10 * delta))
+    V = 5
+    pt = special.softmax(rng.normal(0, 1.5, V))
+    pd = special.softmax(np.log(pt) + rng.normal(0, 1.0, V))
+    hs = [oracle.cactus_h(pt, n, delta, exact=True)[0] for n in range(V)]
+    law = output_law(None, pd, h_of=lambda t: hs[t])
+    direct = np.zeros(V)
+    for n in range(V):
+        h = hs[n]
+        a = min(1.0, h[n] / pd[n])
+        direct[n] += pd[n] * a
+        res = np.maximum(h - pd, 0.0)
+        if a < 1.0:
+            direct += pd[n] * (1 - a) * res / res.sum()
+    assert law == pytest.approx(direct, abs=2e-6)
+    B, K = 8, 3
+    tgt = rng.normal(0, 2, (B, K + 1, 40)).astype(np.float32)
+    drf = (tgt[:, :K] + rng.normal(0, 1, (B, K, 40))).astype(np.float32)
+    tok = rng.integers(0, 40, (B, K)).astype(np.int32)
+    out = oracle.cactus(tgt, drf, tok, np.arange(B, dtype=np.uint64), delta, exact=True)
+    for b in range(B):
+        for j in range(K):
+            q = special.softmax(tgt[b, j].astype(np.float64))[tok[b, j]]
+            assert out["gamma_star"][b, j] == pytest.approx(oracle.cactus_gamma_kl(q, delta), abs=1e-12)
