@@ -113,6 +113,19 @@ spec_status spec_cactus_verify(const void* target_logits, const void* draft_logi
                                float* diag, float* gamma_star, void* workspace, size_t workspace_bytes,
                                void* stream);
 
+/* Cactus with gamma* as the exact root of its divergence constraint ("Cactus ...", Key design 2: gamma* is
+ * the root of D_KL(h || p_target) = delta on [q(n), +inf), clamped to [q(n), 1]; Key design 3 chooses the
+ * KL divergence and then replaces the root by its second-order Taylor closed form, which spec_cactus_verify
+ * uses). With h_n = g and the other tokens scaled by (1 - g) / (1 - q(n)) the divergence is
+ * g ln(g / q(n)) + (1 - g) ln((1 - g) / (1 - q(n))); the root is found per position by a bracketed Newton
+ * iteration in fp32. Same arguments, layout, outputs and errors as spec_cactus_verify; delta = 0 again gives
+ * outputs bit-identical to spec_verify, and ln(1 / q(n)) <= delta gives gamma* = 1. */
+spec_status spec_cactus_kl_verify(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                                  const int32_t* draft_tokens, const uint64_t* seeds, int B, int K, int V,
+                                  float temperature, float delta, int32_t* accept_len, int32_t* out_tokens,
+                                  float* diag, float* gamma_star, void* workspace, size_t workspace_bytes,
+                                  void* stream);
+
 /* spec_verify for callers that cannot allocate device memory: same inputs, outputs and semantics, but no
  * workspace argument. Some callers run where allocation is not allowed or not possible: inside a memory
  * budget fixed in advance, under an allocator that must not grow, or from code that has no allocator at all.
@@ -144,8 +157,8 @@ spec_status spec_clear_status(void* workspace, void* stream);
 /* Thread-local message describing the last non-OK status returned on this thread. */
 const char* spec_last_error(void);
 
-/* Tuning and test hook: forces the number of CTAs of the statistics pass of spec_verify, spec_verify_cactus
- * and spec_verify_static (1 to 1024; 0 restores the automatic choice, every SM once). The grid fixes how
+/* Tuning and test hook: forces the number of CTAs of the statistics pass of spec_verify, spec_cactus_verify,
+ * spec_cactus_kl_verify and spec_verify_static (1 to 1024; 0 restores the automatic choice, every SM once). The grid fixes how
  * the rows are cut into per-warp segments, so results depend on it only through floating-point summation
  * order. Process-wide, not thread-safe. Returns 0, or -1 for an unsupported value. */
 int spec_debug_set_stats_grid(int ctas);

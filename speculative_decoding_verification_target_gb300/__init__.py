@@ -19,7 +19,7 @@ from . import _build
 
 SPEC_OK, SPEC_ERR_INVALID, SPEC_ERR_CUDA, SPEC_ERR_UNSUPPORTED = 0, 1, 2, 3
 STATUS_BAD_TOKEN, STATUS_TIMEOUT = 1, 2
-EXPORTS = ("spec_workspace_size", "spec_verify", "spec_counterfactual_gamma", "spec_cactus_verify",
+EXPORTS = ("spec_workspace_size", "spec_verify", "spec_counterfactual_gamma", "spec_cactus_verify", "spec_cactus_kl_verify",
            "spec_read_status", "spec_clear_status", "spec_last_error",
            "spec_debug_last_plan", "spec_verify_static", "spec_debug_set_stats_grid")
 
@@ -56,6 +56,8 @@ def load(build_if_missing: bool = False):
     lib.spec_counterfactual_gamma.restype = I
     lib.spec_cactus_verify.argtypes = [P, P, I, P, P, I, I, I, F, F, P, P, P, P, P, Z, P]
     lib.spec_cactus_verify.restype = I
+    lib.spec_cactus_kl_verify.argtypes = [P, P, I, P, P, I, I, I, F, F, P, P, P, P, P, Z, P]
+    lib.spec_cactus_kl_verify.restype = I
     lib.spec_read_status.argtypes = [P, P, P]
     lib.spec_read_status.restype = I
     lib.spec_clear_status.argtypes = [P, P]
@@ -167,8 +169,9 @@ def verify(target, draft, tokens, seeds, temperature=1.0, *, accept_len=None, ou
 
 
 def cactus_verify(target, draft, tokens, seeds, delta, temperature=1.0, *, accept_len=None, out_tokens=None,
-                  diag=None, gamma_star=None, want_diag=True, workspace=None, stream=None):
-    """Cactus constrained acceptance with divergence budget delta; same layout as verify."""
+                  diag=None, gamma_star=None, want_diag=True, workspace=None, stream=None, exact_kl=False):
+    """Cactus constrained acceptance with divergence budget delta; same layout as verify. exact_kl=True uses
+    gamma* as the root of the KL constraint (spec_cactus_kl_verify) instead of its Taylor closed form."""
     B, K1, V = target.shape
     K = K1 - 1
     _need(target, "target")
@@ -179,9 +182,10 @@ def cactus_verify(target, draft, tokens, seeds, delta, temperature=1.0, *, accep
     if gamma_star is None:
         gamma_star = torch.empty((B, K), dtype=torch.float32, device=target.device)
     ws = workspace if workspace is not None else new_workspace(B, K, V, 1, target.device)
-    _check(load().spec_cactus_verify(_p(target), _p(draft), _dtype_code(target), _p(tokens), _p(seeds), B, K, V,
-                                     float(temperature), float(delta), _p(accept_len), _p(out_tokens), _p(diag),
-                                     _p(gamma_star), _p(ws), ws.numel(), _stream(stream)))
+    fn = load().spec_cactus_kl_verify if exact_kl else load().spec_cactus_verify
+    _check(fn(_p(target), _p(draft), _dtype_code(target), _p(tokens), _p(seeds), B, K, V, float(temperature),
+              float(delta), _p(accept_len), _p(out_tokens), _p(diag), _p(gamma_star), _p(ws), ws.numel(),
+              _stream(stream)))
     return dict(accept_len=accept_len, out_tokens=out_tokens, diag=diag, gamma_star=gamma_star, workspace=ws)
 
 

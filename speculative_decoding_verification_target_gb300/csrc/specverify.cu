@@ -443,7 +443,7 @@ spec_status spec_counterfactual_gamma(const void* target_logits, const void* dra
     return run(a);
 }
 
-spec_status spec_cactus_verify(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+static spec_status cactus_call(int mode, const void* target_logits, const void* draft_logits, spec_dtype dtype,
                                const int32_t* draft_tokens, const uint64_t* seeds, int B, int K, int V,
                                float temperature, float delta, int32_t* accept_len, int32_t* out_tokens, float* diag,
                                float* gamma_star, void* workspace, size_t workspace_bytes, void* stream) {
@@ -467,7 +467,7 @@ spec_status spec_cactus_verify(const void* target_logits, const void* draft_logi
     a.selected = 0;
     a.temperature = temperature;
     a.delta = delta;
-    a.cactus = 1;
+    a.cactus = mode;
     a.accept_len = accept_len;
     a.out_tokens = out_tokens;
     a.diag = diag;
@@ -476,6 +476,23 @@ spec_status spec_cactus_verify(const void* target_logits, const void* draft_logi
     a.workspace_bytes = workspace_bytes;
     a.stream = static_cast<cudaStream_t>(stream);
     return run(a);
+}
+
+spec_status spec_cactus_verify(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                               const int32_t* draft_tokens, const uint64_t* seeds, int B, int K, int V,
+                               float temperature, float delta, int32_t* accept_len, int32_t* out_tokens, float* diag,
+                               float* gamma_star, void* workspace, size_t workspace_bytes, void* stream) {
+    return cactus_call(1, target_logits, draft_logits, dtype, draft_tokens, seeds, B, K, V, temperature, delta,
+                       accept_len, out_tokens, diag, gamma_star, workspace, workspace_bytes, stream);
+}
+
+spec_status spec_cactus_kl_verify(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                                  const int32_t* draft_tokens, const uint64_t* seeds, int B, int K, int V,
+                                  float temperature, float delta, int32_t* accept_len, int32_t* out_tokens,
+                                  float* diag, float* gamma_star, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+    return cactus_call(2, target_logits, draft_logits, dtype, draft_tokens, seeds, B, K, V, temperature, delta,
+                       accept_len, out_tokens, diag, gamma_star, workspace, workspace_bytes, stream);
 }
 
 spec_status spec_verify_static(const void* target_logits, const void* draft_logits, spec_dtype dtype,

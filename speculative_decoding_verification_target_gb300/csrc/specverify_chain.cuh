@@ -223,7 +223,7 @@ struct DParams {
     int cps;                       // CTAs per sequence, the cluster size (piece pc belongs to CTA pc % cps)
     int tma;                       // 1: pieces come through a per-warp shared-memory slot by bulk copies
     float c, delta;
-    int cactus;
+    int cactus;                    // 0: standard, 1: Cactus (Taylor gamma*), 2: Cactus (root of the KL constraint)
     int32_t* accept_len;           // [B]
     int32_t* out_tokens;           // [B, K+1]
     float* diag;                   // [B, K, 4] or null
@@ -436,7 +436,8 @@ __global__ void __launch_bounds__(DNT, 1) draw_kernel(const __grid_constant__ DP
                 float ht = s_ht[j], lt = s_ltp[j];
                 if (p.cactus) {
                     float log2s;
-                    cactus_scalars(s_ht[j], p.delta, ht, log2s);
+                    if (p.cactus == 2) cactus_scalars_kl(s_ht[j], p.delta, ht, log2s);
+                    else cactus_scalars(s_ht[j], p.delta, ht, log2s);
                     lt = s_ltp[j] + log2s;
                 }
                 s_ht[j] = ht;

@@ -199,6 +199,46 @@ __device__ __forceinline__ void cactus_scalars(float q, float delta, float& gsta
     log2s = log2f(s);
 }
 
+// The same scalars with gamma* the root of the divergence constraint instead of its Taylor closed form
+// ([Cactus] Key design 2 with the KL divergence of Key design 3): with h_n = g and the other tokens scaled
+// by (1 - g) / (1 - q), KL(h || p_target) = g ln(g / q) + (1 - g) ln((1 - g) / (1 - q)) =: F(g). F(q) = 0,
+// F increases and is convex on [q, 1], so Newton's method inside the bracket [q, 1] (a bisection step
+// whenever Newton leaves it) finds the root of F(g) = delta. No root below 1 (ln(1/q) <= delta) gives
+// gamma* = 1; delta = 0 or q = 0 gives gamma* = q exactly.
+__device__ __forceinline__ float cactus_kl_f(float q, float g) {
+    const float a = g > 0.f ? g * logf(g / q) : 0.f;
+    const float b = g < 1.f ? (1.f - g) * logf((1.f - g) / (1.f - q)) : 0.f;
+    return a + b;
+}
+__device__ __forceinline__ void cactus_scalars_kl(float q, float delta, float& gstar, float& log2s) {
+    float gs;
+    if (!(delta > 0.f) || !(q > 0.f)) {
+        gs = q;
+    } else if (!(q < 1.f) || cactus_kl_f(q, 1.f) <= delta) {
+        gs = 1.f;
+    } else {
+        float lo = q, hi = 1.f;
+        float g = fminf(q + sqrtf(2.f * delta * q * (1.f - q)), 0.5f * (q + 1.f));   // the Taylor start
+        for (int it = 0; it < 64; ++it) {
+            const float f = cactus_kl_f(q, g) - delta;
+            if (f > 0.f) hi = g;
+            else lo = g;
+            const float d = logf(g / q) - logf((1.f - g) / (1.f - q));   // F'(g) > 0 inside (q, 1)
+            float gn = g - f / d;
+            if (!(gn > lo && gn < hi)) gn = 0.5f * (lo + hi);
+            if (fabsf(gn - g) <= 1e-7f * g || hi - lo <= 1e-7f * hi) {
+                g = gn;
+                break;
+            }
+            g = gn;
+        }
+        gs = g;
+    }
+    const float s = q < 1.f ? __fdiv_rn(1.f - gs, 1.f - q) : 0.f;
+    gstar = gs;
+    log2s = log2f(s);
+}
+
 // ------------------------------------------------------------------------------------------------
 // per-chunk arithmetic
 // ------------------------------------------------------------------------------------------------

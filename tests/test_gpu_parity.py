@@ -279,6 +279,58 @@ def test_cactus_delta_zero_bit_identical_to_verify():
     assert torch.equal(a["diag"], c["diag"])
 
 
+# ------------------------------------------------------------------------------------------------
+# Cactus with gamma* as the exact root of its divergence constraint
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("delta", [0.0, 0.05, 0.75, 1.0, 3.0])
+@pytest.mark.parametrize("V,dtype", [(3000, "bf16"), (40000, "bf16"), (1000, "fp32")])
+def test_cactus_kl_small(delta, V, dtype):
+    w = small(V, B=8, K=5, sigma=2.0, dtype=dtype, T=0.8)
+    inp = workloads.make(w)
+    ref = oracle.cactus(host(inp["target"]), host(inp["draft"]), inp["tokens"].numpy(),
+                        inp["seeds"].numpy().astype(np.uint64), delta, w.temperature, exact=True)
+    g = to_device(inp)
+    out = sv.cactus_verify(g["target"], g["draft"], g["tokens"], g["seeds"], delta, w.temperature, exact_kl=True)
+    torch.cuda.synchronize()
+    assert np.abs(out["gamma_star"].cpu().numpy() - ref["gamma_star"]).max() <= PROB_TOL
+    assert_diag(out, ref)
+    assert_chain(out, ref, w.K)
+    assert sv.read_status(out["workspace"]) == 0
+
+
+def test_cactus_kl_delta_zero_bit_identical_to_verify():
+    w = small(151936, B=6, K=4, sigma=2.0)
+    g = to_device(workloads.make(w))
+    a = sv.verify(g["target"], g["draft"], g["tokens"], g["seeds"])
+    c = sv.cactus_verify(g["target"], g["draft"], g["tokens"], g["seeds"], 0.0, exact_kl=True)
+    torch.cuda.synchronize()
+    for k in ("accept_len", "out_tokens", "diag"):
+        assert torch.equal(a[k], c[k])
+
+
+def test_cactus_kl_named_workload_sampled():
+    """Config 4's shapes with the exact root, every 8th sequence against the oracle; the root never falls
+    below the Taylor value where that one is at most 0.5 (the page's Corollary 6)."""
+    w = workloads.WORKLOADS["cactus_qwen_b128_m20"]
+    inp = workloads.make(w, device="cuda")
+    sel = torch.arange(0, w.B, 8)
+    for delta in w.deltas:
+        out = sv.cactus_verify(inp["target"], inp["draft"], inp["tokens"], inp["seeds"], delta, w.temperature,
+                               exact_kl=True)
+        tay = sv.cactus_verify(inp["target"], inp["draft"], inp["tokens"], inp["seeds"], delta, w.temperature)
+        torch.cuda.synchronize()
+        ref = oracle.cactus(host(inp["target"][sel]), host(inp["draft"][sel]), inp["tokens"][sel].cpu().numpy(),
+                            inp["seeds"][sel].cpu().numpy().astype(np.uint64), delta, w.temperature,
+                            seq_index=sel.numpy(), exact=True)
+        sub = {k: out[k][sel.cuda()] for k in ("accept_len", "out_tokens", "diag")}
+        assert np.abs(out["gamma_star"][sel.cuda()].cpu().numpy() - ref["gamma_star"]).max() <= PROB_TOL
+        assert_diag(sub, ref)
+        assert_chain(sub, ref, w.K)
+        ge, gt = out["gamma_star"], tay["gamma_star"]
+        low = gt <= 0.5
+        assert torch.all(ge[low] >= gt[low] - 1e-6)
+
+
 def test_cactus_named_workload_sampled():
     w = workloads.WORKLOADS["cactus_qwen_b128_m20"]
     inp = workloads.make(w, device="cuda")
