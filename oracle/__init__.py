@@ -66,6 +66,8 @@ def _load():
     lib.spec_oracle_cactus_h.restype = f64
     lib.spec_oracle_verify.argtypes = [i32, P, P, P, P, P, i32, i32, i32, f64, i32, P, P, P, P, P, i32]
     lib.spec_oracle_verify.restype = i32
+    lib.spec_oracle_greedy.argtypes = [i32, P, P, i32, i32, i32, P, P, i32]
+    lib.spec_oracle_greedy.restype = i32
     lib.spec_oracle_cactus.argtypes = [i32, P, P, P, P, P, i32, i32, i32, f64, f64, P, P, P, P, P, P, i32]
     lib.spec_oracle_cactus.restype = i32
     lib.spec_oracle_cactus_ex.argtypes = [i32, P, P, P, P, P, i32, i32, i32, f64, f64, i32, P, P, P, P, P, P, i32]
@@ -189,6 +191,22 @@ def verify(target, draft, tokens, seeds, temperature=1.0, seq_index=None, mutati
                                 _ptr(out["cdf_margin"]), nthreads)
     if rc != 0:
         raise ValueError("oracle verify rejected its arguments")
+    return out
+
+
+def greedy(target, tokens, nthreads=0):
+    """Greedy verification (temperature 0): accept a draft token iff it is the target row's argmax (smallest
+    index among ties); emit the argmax of the first rejecting row, or of row K. target [B,K+1,V]."""
+    lib = _load()
+    target, dt = _logits(target)
+    B, K1, V = target.shape
+    K = K1 - 1
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    out = dict(accept_len=np.zeros(B, np.int32), out_tokens=np.zeros((B, K + 1), np.int32))
+    rc = lib.spec_oracle_greedy(dt, _ptr(target), _ptr(tokens), B, K, V, _ptr(out["accept_len"]),
+                                _ptr(out["out_tokens"]), nthreads)
+    if rc != 0:
+        raise ValueError("oracle greedy rejected its arguments")
     return out
 
 

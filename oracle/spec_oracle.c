@@ -415,6 +415,48 @@ int spec_oracle_cactus(int dtype, const void* target, const void* draft, const i
                                  out_tokens, diag, gamma_star, accept_margin, cdf_margin, nthreads);
 }
 
+/* Greedy verification: [SpS] §5.1 and the §9.1 chain with the temperature taken to 0. Both rows become
+ * one-hot at their largest logit (the smallest index among equal largest logits: the pages fix no tie
+ * rule), so p(t) / q(t) is 1 when the draft token t is the target's argmax and 0 otherwise, whatever the
+ * uniform: accept iff t = argmax of target row j. At the first reject the residual (p - q)+ is the one-hot
+ * p itself, or empty when the draft row has the same argmax, in which case the row is drawn from p; either
+ * way the emitted token is the argmax of target row L. All K accepted: the argmax of target row K. The
+ * draft logits and the uniforms drop out. Outputs as spec_oracle_verify's accept_len and out_tokens. */
+static int argmax_row(const double* x, int V)
+{
+    int a = 0;
+    for (int i = 1; i < V; i++)
+        if (x[i] > x[a]) a = i;
+    return a;
+}
+
+int spec_oracle_greedy(int dtype, const void* target, const int32_t* tokens, int B, int K, int V,
+                       int32_t* accept_len, int32_t* out_tokens, int nthreads)
+{
+    if (K < 1 || K > ORACLE_MAX_K || V < 1 || B < 0) return -1;
+    int nt = nthreads_or_default(nthreads);
+#pragma omp parallel for schedule(dynamic) num_threads(nt)
+    for (int b = 0; b < B; b++) {
+        double* x = (double*)malloc(sizeof(double) * (size_t)V);
+        int L = K;
+        for (int j = 0; j <= K; j++) {
+            load_row(dtype, target, (size_t)b * (K + 1) + j, V, x);
+            int a = argmax_row(x, V);
+            if (j < K && tokens[(size_t)b * K + j] == a) {
+                out_tokens[(size_t)b * (K + 1) + j] = a;
+                continue;
+            }
+            L = j;
+            out_tokens[(size_t)b * (K + 1) + j] = a;
+            break;
+        }
+        for (int j = L + 1; j <= K; j++) out_tokens[(size_t)b * (K + 1) + j] = -1;
+        accept_len[b] = L;
+        free(x);
+    }
+    return 0;
+}
+
 /* HedgeSpec counterfactual evaluation ([Hedge] Key design 1): for every drafter i, sequence b and
  * level j < K, gamma[i,b,j] = sum_x min(p_target(x), q_i(x)), the acceptance probability of
  * drafter i at that level ([SpS] §6.3: P(accept) = sum_x min(p, q) = 1 - TV). tv[i,b,j] =

@@ -565,3 +565,65 @@ def test_cactus_exact_root_law(delta):
         for j in range(K):
             q = special.softmax(tgt[b, j].astype(np.float64))[tok[b, j]]
             assert out["gamma_star"][b, j] == pytest.approx(oracle.cactus_gamma_kl(q, delta), abs=1e-12)
+
+
+# ----------------------------------------------------------------------------------------------
+# greedy verification (temperature 0)
+# ----------------------------------------------------------------------------------------------
+def _greedy_case(rng, B=24, K=5, V=60, ties=False):
+    tgt = rng.normal(0, 2, (B, K + 1, V)).astype(np.float32)
+    if ties:   # round to a coarse grid so that rows have several equal largest logits
+        tgt = np.round(tgt * 2) / 2
+    drf = (tgt[:, :K] + rng.normal(0, 1, (B, K, V))).astype(np.float32)
+    am = tgt.argmax(axis=2)
+    # drafts: the target's argmax most of the time, another token otherwise
+    tok = np.where(rng.random((B, K)) < 0.7, am[:, :K], rng.integers(0, V, (B, K))).astype(np.int32)
+    return tgt, drf, tok
+
+
+def test_greedy_is_the_chain_on_one_hot_rows():
+    """The greedy result equals [SpS] §5.1 / §9.1 run on one-hot target and draft rows (logit 0 at the
+    argmax, -inf elsewhere), for any seeds: the uniforms and the draft rows drop out."""
+    rng = np.random.default_rng(70)
+    for ties in (False, True):
+        tgt, drf, tok = _greedy_case(rng, ties=ties)
+        g = oracle.greedy(tgt, tok)
+        am_t = tgt.argmax(axis=2)                # numpy: first index of the largest value
+        am_d = drf.argmax(axis=2)
+        oh_t = np.full(tgt.shape, -np.inf, dtype=np.float32)
+        oh_d = np.full(drf.shape, -np.inf, dtype=np.float32)
+        np.put_along_axis(oh_t, am_t[..., None], 0.0, axis=2)
+        np.put_along_axis(oh_d, am_d[..., None], 0.0, axis=2)
+        for seed0 in (0, 999):
+            seeds = np.arange(len(tok), dtype=np.uint64) + seed0
+            v = oracle.verify(oh_t, oh_d, tok, seeds)
+            assert np.array_equal(v["accept_len"], g["accept_len"])
+            assert np.array_equal(v["out_tokens"], g["out_tokens"])
+
+
+def test_greedy_is_the_low_temperature_limit():
+    """With greedy drafts (each draft token the argmax of its draft row) and no ties, the general algorithm
+    at T = 1e-3 gives the greedy outputs: q(t) -> 1 and p(t) -> 1 or 0 as T -> 0. (For a token that is the
+    argmax of neither row the ratio p(t)/q(t) has no such limit, which is why greedy is defined on the
+    one-hot rows.)"""
+    rng = np.random.default_rng(71)
+    tgt, drf, _ = _greedy_case(rng, B=40)
+    tok = drf.argmax(axis=2).astype(np.int32)
+    g = oracle.greedy(tgt, tok)
+    v = oracle.verify(tgt, drf, tok, np.arange(40, dtype=np.uint64) + 5, temperature=1e-3)
+    assert np.array_equal(v["accept_len"], g["accept_len"])
+    assert np.array_equal(v["out_tokens"], g["out_tokens"])
+    assert 0 < g["accept_len"].mean() < 5
+
+
+def test_greedy_chain_structure():
+    rng = np.random.default_rng(72)
+    tgt, _, tok = _greedy_case(rng, B=50, ties=True)
+    g = oracle.greedy(tgt, tok)
+    am = tgt.argmax(axis=2)
+    for b in range(50):
+        L = g["accept_len"][b]
+        assert np.array_equal(g["out_tokens"][b, :L], tok[b, :L]) and np.all(tok[b, :L] == am[b, :L])
+        assert L == 5 or tok[b, L] != am[b, L]
+        assert g["out_tokens"][b, L] == am[b, L]
+        assert np.all(g["out_tokens"][b, L + 1:] == -1)
