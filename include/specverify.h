@@ -126,6 +126,20 @@ spec_status spec_cactus_kl_verify(const void* target_logits, const void* draft_l
                                   float* diag, float* gamma_star, void* workspace, size_t workspace_bytes,
                                   void* stream);
 
+/* Greedy verification: [SpS] §5.1 and the §9.1 chain at temperature 0, where the target and draft rows are
+ * one-hot at their largest logit ("Speculative Decoding 为什么是 Lossless 的", §8 Q4: sampling transforms are
+ * folded into p and q before the ratio). Then p(t) / q(t) is 1 when the draft token t is the argmax of
+ * target row j and 0 otherwise, so draft j is accepted iff it is that argmax; the first rejecting row (or row
+ * K when all K are accepted) emits its argmax. Ties among equal largest logits go to the smallest index (the
+ * pages fix no rule). The draft logits and the uniforms drop out, so only the target rows are read.
+ * target_logits: [B, K+1, V]; draft_tokens int32 [B, K]; outputs accept_len [B] and out_tokens [B, K+1]
+ * (-1 padded) as spec_verify. A draft token outside [0, V) is a reject and sets SPEC_STATUS_BAD_TOKEN. A row
+ * whose logits are all -inf has argmax 0. Workspace and errors as spec_verify (spec_workspace_size(B, K, V,
+ * 1) bytes). */
+spec_status spec_greedy_verify(const void* target_logits, spec_dtype dtype, const int32_t* draft_tokens, int B,
+                               int K, int V, int32_t* accept_len, int32_t* out_tokens, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
 /* spec_verify for callers that cannot allocate device memory: same inputs, outputs and semantics, but no
  * workspace argument. Some callers run where allocation is not allowed or not possible: inside a memory
  * budget fixed in advance, under an allocator that must not grow, or from code that has no allocator at all.
@@ -166,7 +180,7 @@ int spec_debug_set_stats_grid(int ctas);
 /* Tuning and test hook: the launch plan of the last call made on this thread, as five ints: 0, ring slots
  * per warp, CTAs launched, kernel (0: the statistics pass of spec_verify / spec_cactus_verify /
  * spec_verify_static; 2: the gamma kernel of spec_counterfactual_gamma, which parks rows in tensor
- * memory), pieces per row. out5 is host memory. Returns 0, or -1 for a NULL pointer. */
+ * memory; 3: the argmax pass of spec_greedy_verify), pieces per row. out5 is host memory. Returns 0, or -1 for a NULL pointer. */
 int spec_debug_last_plan(int* out5);
 
 #ifdef __cplusplus

@@ -20,6 +20,7 @@ from . import _build
 SPEC_OK, SPEC_ERR_INVALID, SPEC_ERR_CUDA, SPEC_ERR_UNSUPPORTED = 0, 1, 2, 3
 STATUS_BAD_TOKEN, STATUS_TIMEOUT = 1, 2
 EXPORTS = ("spec_workspace_size", "spec_verify", "spec_counterfactual_gamma", "spec_cactus_verify", "spec_cactus_kl_verify",
+           "spec_greedy_verify",
            "spec_read_status", "spec_clear_status", "spec_last_error",
            "spec_debug_last_plan", "spec_verify_static", "spec_debug_set_stats_grid")
 
@@ -58,6 +59,8 @@ def load(build_if_missing: bool = False):
     lib.spec_cactus_verify.restype = I
     lib.spec_cactus_kl_verify.argtypes = [P, P, I, P, P, I, I, I, F, F, P, P, P, P, P, Z, P]
     lib.spec_cactus_kl_verify.restype = I
+    lib.spec_greedy_verify.argtypes = [P, I, P, I, I, I, P, P, P, Z, P]
+    lib.spec_greedy_verify.restype = I
     lib.spec_read_status.argtypes = [P, P, P]
     lib.spec_read_status.restype = I
     lib.spec_clear_status.argtypes = [P, P]
@@ -187,6 +190,20 @@ def cactus_verify(target, draft, tokens, seeds, delta, temperature=1.0, *, accep
               float(delta), _p(accept_len), _p(out_tokens), _p(diag), _p(gamma_star), _p(ws), ws.numel(),
               _stream(stream)))
     return dict(accept_len=accept_len, out_tokens=out_tokens, diag=diag, gamma_star=gamma_star, workspace=ws)
+
+
+def greedy_verify(target, tokens, *, accept_len=None, out_tokens=None, workspace=None, stream=None):
+    """Greedy (temperature 0) verification: accept a draft token iff it is the target row's argmax; emit the
+    argmax of the first rejecting row (or of row K). target [B,K+1,V], tokens [B,K]."""
+    B, K1, V = target.shape
+    K = K1 - 1
+    _need(target, "target")
+    _need(tokens, "tokens", torch.int32, (B, K))
+    accept_len, out_tokens, _ = _outputs(B, K, target.device, accept_len, out_tokens, None, False)
+    ws = workspace if workspace is not None else new_workspace(B, K, V, 1, target.device)
+    _check(load().spec_greedy_verify(_p(target), _dtype_code(target), _p(tokens), B, K, V, _p(accept_len),
+                                     _p(out_tokens), _p(ws), ws.numel(), _stream(stream)))
+    return dict(accept_len=accept_len, out_tokens=out_tokens, workspace=ws)
 
 
 def counterfactual_gamma(target, drafters, temperature=1.0, selected=-1, tokens=None, seeds=None, *, gamma=None,

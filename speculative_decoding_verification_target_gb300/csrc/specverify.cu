@@ -257,6 +257,81 @@ spec_status run_chain(const Call& a, bool aligned) {
     return launch_draw(a, aligned, static_cast<const unsigned char*>(a.others), s.part, nullptr, s.P, s.G, s.status);
 }
 
+// Greedy verification: the statistics pass in its argmax mode over the target rows, then one warp per
+// sequence for the chain.
+spec_status run_greedy(const void* target, spec_dtype dtype, const int32_t* tokens, int B, int K, int V,
+                       int32_t* accept_len, int32_t* out_tokens, void* workspace, cudaStream_t stream) {
+    const int eb = dtype == SPEC_BF16 ? 2 : 4;
+    const bool aligned = (reinterpret_cast<uintptr_t>(target) & 15) == 0 && (static_cast<size_t>(V) * eb) % 16 == 0 &&
+                         V % CHUNK == 0;
+    const WsLayout wl = ws_layout(B, K, V, 1);
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    SParams s = {};
+    s.rows_a = static_cast<const unsigned char*>(target);
+    s.rows_b = nullptr;
+    s.rows_a_n = static_cast<long long>(B) * (K + 1);
+    s.rows_n = s.rows_a_n;
+    s.V = V;
+    s.np = (V + PE - 1) / PE;
+    s.P = s.rows_n * s.np;
+    s.c = 1.f;
+    s.tma = aligned ? 1 : 0;
+    s.K = K;
+    s.keep_j = 0;   // every logit is read once
+    s.keep_b = 0;
+    const size_t slot_bytes = static_cast<size_t>(PE) * eb;
+    int R = S_MAX_R;
+    while (R > 1 && static_cast<size_t>(SW) * R * (slot_bytes + 8) > static_cast<size_t>(SMEM_MAX_PER_CTA)) --R;
+    s.R = R;
+    const size_t smem = s.tma ? static_cast<size_t>(SW) * R * (slot_bytes + 8) : 0;
+    StatsFn sfn = dtype == SPEC_BF16 ? stats_kernel<Bf16, true> : stats_kernel<F32, true>;
+    int ctas = 0;
+    cudaError_t e = stats_ctas(sfn, smem, ctas);
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "occupancy query failed: %s", cudaGetErrorString(e));
+    if (g_stats_grid_override > 0) ctas = g_stats_grid_override;
+    const long long need = (s.P + SW - 1) / SW;
+    if (ctas > need) ctas = static_cast<int>(need);
+    s.G = ctas * SW;
+    s.part = reinterpret_cast<float2*>(ws + wl.part_off);
+    s.status = reinterpret_cast<unsigned*>(ws);
+    g_last_plan[0] = 0;
+    g_last_plan[1] = R;
+    g_last_plan[2] = ctas;
+    g_last_plan[3] = 3;
+    g_last_plan[4] = s.np;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
+    cfg.blockDim = dim3(SNT, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    e = cudaLaunchKernelEx(&cfg, sfn, s);
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "statistics kernel launch failed: %s", cudaGetErrorString(e));
+    GrParams gp = {};
+    gp.part = s.part;
+    gp.P = s.P;
+    gp.G = s.G;
+    gp.np = s.np;
+    gp.tokens = tokens;
+    gp.B = B;
+    gp.K = K;
+    gp.V = V;
+    gp.accept_len = accept_len;
+    gp.out_tokens = out_tokens;
+    gp.status = s.status;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t gc = {};
+    gc.gridDim = dim3(static_cast<unsigned>((B + 7) / 8), 1, 1);
+    gc.blockDim = dim3(256, 1, 1);
+    gc.stream = stream;
+    gc.attrs = at;
+    gc.numAttrs = 1;
+    e = cudaLaunchKernelEx(&gc, greedy_chain_kernel, gp);
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "greedy chain kernel launch failed: %s", cudaGetErrorString(e));
+    return SPEC_OK;
+}
+
 // Counterfactual gamma for N drafters (gamma_kernel, one CTA per SM, rows whole per CTA), followed by the
 // chain and draw of drafter `selected` when one is given.
 spec_status run_gamma(const Call& a, bool aligned) {
@@ -493,6 +568,26 @@ spec_status spec_cactus_kl_verify(const void* target_logits, const void* draft_l
                                   void* stream) {
     return cactus_call(2, target_logits, draft_logits, dtype, draft_tokens, seeds, B, K, V, temperature, delta,
                        accept_len, out_tokens, diag, gamma_star, workspace, workspace_bytes, stream);
+}
+
+spec_status spec_greedy_verify(const void* target_logits, spec_dtype dtype, const int32_t* draft_tokens, int B,
+                               int K, int V, int32_t* accept_len, int32_t* out_tokens, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+    if (dtype != SPEC_BF16 && dtype != SPEC_FP32) return fail(SPEC_ERR_INVALID, "unknown dtype %d", static_cast<int>(dtype));
+    if (B < 0) return fail(SPEC_ERR_INVALID, "B must be >= 0 (got %d)", B);
+    if (K < 1 || K > MAX_K) return fail(SPEC_ERR_INVALID, "K must be in [1, %d] (got %d)", MAX_K, K);
+    if (V < 1 || V > MAX_V) return fail(SPEC_ERR_INVALID, "V must be in [1, %d] (got %d)", MAX_V, V);
+    if (B == 0) return SPEC_OK;
+    if (!target_logits) return fail(SPEC_ERR_INVALID, "target_logits must not be NULL");
+    if (!draft_tokens || !accept_len || !out_tokens)
+        return fail(SPEC_ERR_INVALID, "draft_tokens, accept_len and out_tokens must not be NULL");
+    if (!workspace) return fail(SPEC_ERR_INVALID, "workspace must not be NULL");
+    if (reinterpret_cast<uintptr_t>(workspace) % 16) return fail(SPEC_ERR_INVALID, "workspace must be 16-byte aligned");
+    const size_t need = spec_workspace_size(B, K, V, 1);
+    if (workspace_bytes < need)
+        return fail(SPEC_ERR_INVALID, "workspace too small: %zu bytes, need %zu", workspace_bytes, need);
+    return run_greedy(target_logits, dtype, draft_tokens, B, K, V, accept_len, out_tokens, workspace,
+                      static_cast<cudaStream_t>(stream));
 }
 
 spec_status spec_verify_static(const void* target_logits, const void* draft_logits, spec_dtype dtype,

@@ -76,7 +76,44 @@ __device__ __forceinline__ const unsigned char* s_row(const SParams& p, long lon
                           : p.rows_b + static_cast<size_t>(r - p.rows_a_n) * row_bytes;
 }
 
+// Greedy mode of the statistics pass: folds a piece into the lane's running (largest logit m, its index).
+// The lane's elements come in increasing index order (chunk lane + 32 q, q ascending, inside a piece;
+// pieces ascending along the warp's run), so a strictly larger value is the only reason to move the
+// index: the lane keeps the first occurrence. The piece is rescanned only when its bf16x2 maximum beats m.
 template <class E>
+__device__ __forceinline__ void piece_argmax(const typename E::Raw (&r)[PCH], int e_piece, int lane, float& m,
+                                             int& idx) {
+    typename E::Max mm = E::max_init();
+#pragma unroll
+    for (int q = 0; q < PCH; ++q) mm = E::max_acc(mm, r[q]);
+    const float pm = E::max_fin(mm);
+    if (pm > m) {
+        int found = -1;
+#pragma unroll
+        for (int q = 0; q < PCH; ++q)
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const float2 v = E::pair(r[q], w);
+                const int e = e_piece + (lane + 32 * q) * CHUNK + 2 * w;
+                if (found < 0 && v.x == pm) found = e;
+                if (found < 0 && v.y == pm) found = e + 1;
+            }
+        m = pm;
+        idx = found;
+    }
+}
+
+// Warp merge of the lanes' (m, idx): the largest value, and the smallest index among the lanes holding it.
+__device__ __forceinline__ void warp_argmax(float& m, int& idx) {
+    const float M = warp_max(m);
+    unsigned cand = (m == M && idx >= 0) ? static_cast<unsigned>(idx) : 0xFFFFFFFFu;
+    unsigned r;
+    asm volatile("redux.sync.min.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(cand));
+    m = M;
+    idx = r == 0xFFFFFFFFu ? -1 : static_cast<int>(r);
+}
+
+template <class E, bool ARGMAX = false>
 __global__ void __launch_bounds__(SNT, 1) stats_kernel(const __grid_constant__ SParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     using Raw = typename E::Raw;
@@ -98,12 +135,20 @@ __global__ void __launch_bounds__(SNT, 1) stats_kernel(const __grid_constant__ S
     long long row = start / p.np;
     int pc = static_cast<int>(start - row * p.np);
     float m = NINF, s = 0.f;
+    int amax = -1;   // greedy mode: index of m in the row (-1: none yet)
 
     auto fold = [&](Raw (&r)[PCH], long long t) {
-        piece_stats<E>(r, c, m, s);
+        if constexpr (ARGMAX) piece_argmax<E>(r, pc * PE, lane, m, amax);
+        else piece_stats<E>(r, c, m, s);
         if (pc == p.np - 1 || t == cnt - 1) {   // the run leaves row `row` here: store the segment
-            const MaxSum a = warp_ms(MaxSum{m, s}, c);
-            if (lane == 0) p.part[g + row] = make_float2(a.m, a.s);
+            if constexpr (ARGMAX) {
+                warp_argmax(m, amax);
+                if (lane == 0) p.part[g + row] = make_float2(m, __int_as_float(amax));
+                amax = -1;
+            } else {
+                const MaxSum a = warp_ms(MaxSum{m, s}, c);
+                if (lane == 0) p.part[g + row] = make_float2(a.m, a.s);
+            }
             m = NINF;
             s = 0.f;
         }
@@ -625,6 +670,71 @@ __global__ void __launch_bounds__(DNT, 1) draw_kernel(const __grid_constant__ DP
         }
         if (lane == 0) p.accept_len[b] = L;
     }
+}
+
+// ------------------------------------------------------------------------------------------------
+// greedy chain
+// ------------------------------------------------------------------------------------------------
+struct GrParams {
+    const float2* part;            // the greedy statistics pass's segments: (largest logit, its index)
+    long long P;                   // pieces of that pass
+    int G;                         // its warps
+    int np;                        // pieces per row
+    const int32_t* tokens;         // [B, K]
+    int B, K, V;
+    int32_t* accept_len;           // [B]
+    int32_t* out_tokens;           // [B, K+1]
+    unsigned* status;
+};
+
+// One warp per sequence: the argmax of target rows (b, 0..K) from their segments (in piece order, so the
+// first segment holding the largest value holds its first index), then the chain: accept draft j iff it
+// is row j's argmax; emit the argmax of the first rejecting row, or of row K.
+__global__ void __launch_bounds__(256) greedy_chain_kernel(const __grid_constant__ GrParams p) {
+    const int lane = threadIdx.x & 31;
+    const int b = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int K = p.K;
+    // draft tokens are inputs: read before waiting for the statistics grid
+    const int tokv = (b < p.B && lane < K) ? __ldg(p.tokens + static_cast<size_t>(b) * K + lane) : 0;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (b >= p.B) return;
+    const Split sp(p.P, p.G);
+    int L = K, emit = -1;
+    for (int j = 0; j <= K; ++j) {
+        const long long r = static_cast<long long>(b) * (K + 1) + j;
+        const long long g0 = sp.warp_of(r * p.np), g1 = sp.warp_of(r * p.np + p.np - 1);
+        // segments in index order: lane-strided walk keeping (largest, first index), then the warp merge
+        float m = __uint_as_float(0xFF800000u);
+        int idx = -1;
+        for (long long gg = g0 + lane; gg <= g1; gg += 32) {
+            const float2 v = p.part[gg + r];
+            const int vi = __float_as_int(v.y);
+            if (v.x > m || (v.x == m && vi >= 0 && (idx < 0 || vi < idx))) {
+                m = v.x;
+                idx = vi;
+            }
+        }
+        warp_argmax(m, idx);
+        const int am = idx >= 0 ? idx : 0;   // a row with every logit -inf: index 0
+        int t = __shfl_sync(0xffffffffu, tokv, j < K ? j : 0);
+        if (j < K && (t < 0 || t >= p.V)) {
+            if (lane == 0) atomicOr(p.status, STATUS_BAD_TOKEN);
+            t = -1;
+        }
+        if (j == K || t != am) {
+            L = j;
+            emit = am;
+            break;
+        }
+    }
+    for (int j = lane; j <= K; j += 32) {
+        int v;
+        if (j < L) v = __ldg(p.tokens + static_cast<size_t>(b) * K + j);
+        else if (j == L) v = emit;
+        else v = -1;
+        p.out_tokens[static_cast<size_t>(b) * (K + 1) + j] = v;
+    }
+    if (lane == 0) p.accept_len[b] = L;
 }
 
 }  // namespace specv

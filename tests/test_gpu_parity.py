@@ -514,3 +514,69 @@ def test_full_batch_near_ties(name, delta):
                                         inp["seeds"], want_diag=False)
         torch.cuda.synchronize()
         assert_chain(fused, ref, w.K)
+
+
+# ------------------------------------------------------------------------------------------------
+# greedy verification (temperature 0)
+# ------------------------------------------------------------------------------------------------
+def _greedy_tokens(inp, frac=0.7, seed=5):
+    """Draft tokens: the target's argmax with probability frac (so chains get long), else the draft's."""
+    gen = torch.Generator().manual_seed(seed)
+    t = inp["target"].float().cpu()
+    d = inp["draft"].float().cpu()
+    K = d.shape[1]
+    am_t = t[:, :K].argmax(dim=2)
+    am_d = d.argmax(dim=2)
+    pick = torch.rand(am_t.shape, generator=gen) < frac
+    return torch.where(pick, am_t, am_d).to(torch.int32)
+
+
+@pytest.mark.parametrize("V,dtype,C", [(1000, "fp32", 0), (3000, "bf16", 0), (4099, "bf16", 3), (20001, "bf16", 0),
+                                       (128256, "bf16", 0), (151936, "bf16", 7), (65536, "fp32", 0)])
+def test_greedy_small(V, dtype, C):
+    sv.set_stats_grid(C)
+    w = small(V, B=9, K=5, dtype=dtype)
+    inp = workloads.make(w)
+    tok = _greedy_tokens(inp)
+    ref = oracle.greedy(host(inp["target"]), tok.numpy())
+    g = to_device(inp)
+    out = sv.greedy_verify(g["target"], tok.cuda())
+    torch.cuda.synchronize()
+    assert np.array_equal(out["accept_len"].cpu().numpy(), ref["accept_len"])
+    assert np.array_equal(out["out_tokens"].cpu().numpy(), ref["out_tokens"])
+    assert sv.read_status(out["workspace"]) == 0
+    assert ref["accept_len"].max() > 0      # the chains pass accepted positions too
+
+
+def test_greedy_ties_masked_rows_and_bad_tokens():
+    """Rows with several equal largest logits (the smallest index wins), rows of -inf (argmax 0) and draft
+    tokens outside [0, V) (a reject, with the status bit)."""
+    B, K, V = 12, 4, 9000
+    gen = torch.Generator().manual_seed(9)
+    tgt = torch.round(torch.randn((B, K + 1, V), generator=gen) * 2) / 2   # coarse grid: many ties
+    tgt[:, :, 100] = tgt.max() + 1.0                                          # a tie at 100 and 7000
+    tgt[:, :, 7000] = tgt[:, :, 100]
+    tgt[3, 1] = float("-inf")                                                 # a fully masked row
+    tgt = tgt.to(torch.bfloat16)
+    tok = torch.full((B, K), 100, dtype=torch.int32)
+    tok[5, 2] = V + 3
+    tok[6, 0] = -1
+    ref = oracle.greedy(host(tgt), tok.numpy())
+    out = sv.greedy_verify(tgt.cuda(), tok.cuda())
+    torch.cuda.synchronize()
+    assert np.array_equal(out["accept_len"].cpu().numpy(), ref["accept_len"])
+    assert np.array_equal(out["out_tokens"].cpu().numpy(), ref["out_tokens"])
+    assert out["accept_len"][3].item() == 1 and out["out_tokens"][3, 1].item() == 0
+    assert sv.read_status(out["workspace"]) & sv.STATUS_BAD_TOKEN
+
+
+def test_greedy_named_workload_full():
+    w = workloads.WORKLOADS["sps_llama3_b64_k5"]
+    inp = workloads.make(w, device="cuda")
+    tok = _greedy_tokens(inp)
+    ref = oracle.greedy(host(inp["target"]), tok.numpy())
+    out = sv.greedy_verify(inp["target"], tok.cuda())
+    torch.cuda.synchronize()
+    assert np.array_equal(out["accept_len"].cpu().numpy(), ref["accept_len"])
+    assert np.array_equal(out["out_tokens"].cpu().numpy(), ref["out_tokens"])
+    assert 0 < ref["accept_len"].mean() < w.K
