@@ -68,6 +68,8 @@ def _load():
     lib.spec_oracle_verify.restype = i32
     lib.spec_oracle_greedy.argtypes = [i32, P, P, i32, i32, i32, P, P, i32]
     lib.spec_oracle_greedy.restype = i32
+    lib.spec_oracle_accept_length.argtypes = [P, i32, i32, i32, P, P]
+    lib.spec_oracle_accept_length.restype = None
     lib.spec_oracle_cactus.argtypes = [i32, P, P, P, P, P, i32, i32, i32, f64, f64, P, P, P, P, P, P, i32]
     lib.spec_oracle_cactus.restype = i32
     lib.spec_oracle_cactus_ex.argtypes = [i32, P, P, P, P, P, i32, i32, i32, f64, f64, i32, P, P, P, P, P, P, i32]
@@ -208,6 +210,18 @@ def greedy(target, tokens, nthreads=0):
     if rc != 0:
         raise ValueError("oracle greedy rejected its arguments")
     return out
+
+
+def accept_length(gamma):
+    """HedgeSpec accept-length estimate and loss from gamma [N, B, K] (reading: 1 + sum_k prod_{j<=k} gamma_j;
+    the page's display is missing). Returns (est [N, B], loss [N, B])."""
+    lib = _load()
+    g = np.ascontiguousarray(gamma, dtype=np.float64)
+    N, B, K = g.shape
+    est = np.empty((N, B))
+    loss = np.empty((N, B))
+    lib.spec_oracle_accept_length(_ptr(g), N, B, K, _ptr(est), _ptr(loss))
+    return est, loss
 
 
 def cactus(target, draft, tokens, seeds, delta, temperature=1.0, seq_index=None, nthreads=0, exact=False):

@@ -457,6 +457,26 @@ int spec_oracle_greedy(int dtype, const void* target, const int32_t* tokens, int
     return 0;
 }
 
+/* HedgeSpec accept-length estimate and its loss ([Hedge] Key design 2 and 3). PARITY UNPINNED against the
+ * page: its estimator display (Theorem 3) and loss display are missing from the text; what survives is that
+ * the estimate lies in [1, K + 1], that gamma_k is the probability of accepting any token at level k, and
+ * that the loss measures the accept length still available up to K + 1. Reading taken: the expected
+ * number of tokens of a chain whose level k is reached and accepted with probability gamma_k given the
+ * levels before it, est = 1 + sum_{k=1..K} prod_{j<=k} gamma_j, and loss = K + 1 - est. gamma [N, B, K],
+ * est and loss [N, B] (loss nullable). */
+void spec_oracle_accept_length(const double* gamma, int N, int B, int K, double* est, double* loss)
+{
+    for (long long r = 0; r < (long long)N * B; r++) {
+        double run = 1.0, total = 1.0;
+        for (int k = 0; k < K; k++) {
+            run *= gamma[r * K + k];
+            total += run;
+        }
+        est[r] = total;
+        if (loss) loss[r] = (double)(K + 1) - total;
+    }
+}
+
 /* HedgeSpec counterfactual evaluation ([Hedge] Key design 1): for every drafter i, sequence b and
  * level j < K, gamma[i,b,j] = sum_x min(p_target(x), q_i(x)), the acceptance probability of
  * drafter i at that level ([SpS] §6.3: P(accept) = sum_x min(p, q) = 1 - TV). tv[i,b,j] =

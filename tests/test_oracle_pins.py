@@ -627,3 +627,57 @@ def test_greedy_chain_structure():
         assert L == 5 or tok[b, L] != am[b, L]
         assert g["out_tokens"][b, L] == am[b, L]
         assert np.all(g["out_tokens"][b, L + 1:] == -1)
+
+
+# ----------------------------------------------------------------------------------------------
+# HedgeSpec accept-length estimate (the page's display is missing: the reading is pinned through its own
+# mathematics, not against the paper's formula)
+# ----------------------------------------------------------------------------------------------
+def test_accept_length_estimate_identities():
+    rng = np.random.default_rng(80)
+    N, B, K = 3, 7, 6
+    g = rng.uniform(0, 1, (N, B, K))
+    est, loss = oracle.accept_length(g)
+    assert np.all((est >= 1.0) & (est <= K + 1))                        # the range the page states
+    assert np.allclose(est + loss, K + 1, atol=1e-14)
+    # constant gamma: the geometric series (1 - gamma^(K+1)) / (1 - gamma)
+    for gv in (0.0, 0.3, 0.9, 1.0):
+        e, _ = oracle.accept_length(np.full((1, 1, K), gv))
+        ref = K + 1 if gv == 1.0 else (1 - gv ** (K + 1)) / (1 - gv)
+        assert e[0, 0] == pytest.approx(ref, abs=1e-13)
+
+
+def test_accept_length_estimate_is_the_chain_expectation():
+    """Exact enumeration: a chain whose level k is accepted with probability gamma_k (given the levels before
+    it) emits 1 + (number of accepted levels) tokens; its expectation is the estimate."""
+    rng = np.random.default_rng(81)
+    K = 5
+    for _ in range(20):
+        g = rng.uniform(0, 1, K)
+        expect = 0.0
+        for outcome in range(2 ** K):
+            bits = [(outcome >> k) & 1 for k in range(K)]
+            p = np.prod([g[k] if bits[k] else 1 - g[k] for k in range(K)])
+            L = next((k for k in range(K) if not bits[k]), K)   # the first reject stops the chain
+            expect += p * (1 + L)
+        e, _ = oracle.accept_length(g[None, None, :])
+        assert e[0, 0] == pytest.approx(expect, abs=1e-12)
+
+
+def test_accept_length_estimate_matches_simulated_chains():
+    """The estimate from the counterfactual gamma of one drafter against the mean length of many simulated
+    speculative-sampling chains over the same rows (different uniforms): within 5 standard errors."""
+    rng = np.random.default_rng(82)
+    K, V, n = 4, 30, 40000
+    pt = [special.softmax(rng.normal(0, 1.5, V)) for _ in range(K + 1)]
+    pd = [special.softmax(np.log(pt[j]) + rng.normal(0, 0.8, V)) for j in range(K)]
+    # gamma at every level: sum_x min(p, q) (the probability of accepting any draft token there)
+    gam = np.array([np.minimum(pt[j], pd[j]).sum() for j in range(K)])
+    est, _ = oracle.accept_length(gam[None, None, :])
+    # independent chains: draft tokens sampled from q at each level, accept with min(1, p/q)
+    toks = np.stack([rng.choice(V, size=n, p=pd[j]) for j in range(K)], axis=1)
+    acc = rng.uniform(0, 1, (n, K)) < np.stack([np.minimum(1, pt[j][toks[:, j]] / pd[j][toks[:, j]])
+                                                for j in range(K)], axis=1)
+    L = np.where(acc.all(axis=1), K, np.argmin(acc, axis=1))
+    m, se = (1 + L).mean(), (1 + L).std() / np.sqrt(n)
+    assert abs(est[0, 0] - m) < 5 * se
