@@ -140,6 +140,18 @@ spec_status spec_greedy_verify(const void* target_logits, spec_dtype dtype, cons
                                int K, int V, int32_t* accept_len, int32_t* out_tokens, void* workspace,
                                size_t workspace_bytes, void* stream);
 
+/* HedgeSpec accept-length estimate and loss from the counterfactual gamma ("Not-a-Bandit ...", Key design
+ * 2: a one-trajectory estimate of a drafter's expected accept length, in [1, K + 1]; Key design 3: the loss
+ * is the accept length still available up to K + 1). The page's displays of both formulas are missing;
+ * the reading taken is est[i, b] = 1 + sum_{k=1..K} prod_{j<=k} gamma[i, b, j] (the expected tokens of a
+ * chain accepting level k with probability gamma_k given the levels before it) and loss[i, b] = K + 1 -
+ * est[i, b]. gamma: device float [N, B, K], as written by spec_counterfactual_gamma; est: device float
+ * [N, B]; loss: nullable device float [N, B]. All levels are used: a caller that censors by the accepted
+ * length passes gamma with the censored levels as it wants them. Asynchronous on `stream`; allocates
+ * nothing. */
+spec_status spec_accept_length_estimate(const float* gamma, int N, int B, int K, float* est, float* loss,
+                                        void* stream);
+
 /* spec_verify for callers that cannot allocate device memory: same inputs, outputs and semantics, but no
  * workspace argument. Some callers run where allocation is not allowed or not possible: inside a memory
  * budget fixed in advance, under an allocator that must not grow, or from code that has no allocator at all.

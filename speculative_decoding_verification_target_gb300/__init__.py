@@ -20,7 +20,7 @@ from . import _build
 SPEC_OK, SPEC_ERR_INVALID, SPEC_ERR_CUDA, SPEC_ERR_UNSUPPORTED = 0, 1, 2, 3
 STATUS_BAD_TOKEN, STATUS_TIMEOUT = 1, 2
 EXPORTS = ("spec_workspace_size", "spec_verify", "spec_counterfactual_gamma", "spec_cactus_verify", "spec_cactus_kl_verify",
-           "spec_greedy_verify",
+           "spec_greedy_verify", "spec_accept_length_estimate",
            "spec_read_status", "spec_clear_status", "spec_last_error",
            "spec_debug_last_plan", "spec_verify_static", "spec_debug_set_stats_grid")
 
@@ -61,6 +61,8 @@ def load(build_if_missing: bool = False):
     lib.spec_cactus_kl_verify.restype = I
     lib.spec_greedy_verify.argtypes = [P, I, P, I, I, I, P, P, P, Z, P]
     lib.spec_greedy_verify.restype = I
+    lib.spec_accept_length_estimate.argtypes = [P, I, I, I, P, P, P]
+    lib.spec_accept_length_estimate.restype = I
     lib.spec_read_status.argtypes = [P, P, P]
     lib.spec_read_status.restype = I
     lib.spec_clear_status.argtypes = [P, P]
@@ -204,6 +206,18 @@ def greedy_verify(target, tokens, *, accept_len=None, out_tokens=None, workspace
     _check(load().spec_greedy_verify(_p(target), _dtype_code(target), _p(tokens), B, K, V, _p(accept_len),
                                      _p(out_tokens), _p(ws), ws.numel(), _stream(stream)))
     return dict(accept_len=accept_len, out_tokens=out_tokens, workspace=ws)
+
+
+def accept_length_estimate(gamma, *, est=None, loss=None, want_loss=True, stream=None):
+    """HedgeSpec accept-length estimate 1 + sum_k prod_{j<=k} gamma_j and loss K + 1 - est from gamma [N,B,K]."""
+    N, B, K = gamma.shape
+    _need(gamma, "gamma", torch.float32, (N, B, K))
+    if est is None:
+        est = torch.empty((N, B), dtype=torch.float32, device=gamma.device)
+    if loss is None and want_loss:
+        loss = torch.empty((N, B), dtype=torch.float32, device=gamma.device)
+    _check(load().spec_accept_length_estimate(_p(gamma), N, B, K, _p(est), _p(loss), _stream(stream)))
+    return dict(est=est, loss=loss)
 
 
 def counterfactual_gamma(target, drafters, temperature=1.0, selected=-1, tokens=None, seeds=None, *, gamma=None,

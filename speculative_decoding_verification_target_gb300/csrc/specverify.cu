@@ -590,6 +590,21 @@ spec_status spec_greedy_verify(const void* target_logits, spec_dtype dtype, cons
                       static_cast<cudaStream_t>(stream));
 }
 
+spec_status spec_accept_length_estimate(const float* gamma, int N, int B, int K, float* est, float* loss,
+                                        void* stream) {
+    if (N < 1 || N > MAX_N) return fail(SPEC_ERR_INVALID, "N must be in [1, %d] (got %d)", MAX_N, N);
+    if (B < 0) return fail(SPEC_ERR_INVALID, "B must be >= 0 (got %d)", B);
+    if (K < 1 || K > MAX_K) return fail(SPEC_ERR_INVALID, "K must be in [1, %d] (got %d)", MAX_K, K);
+    if (B == 0) return SPEC_OK;
+    if (!gamma || !est) return fail(SPEC_ERR_INVALID, "gamma and est must not be NULL");
+    const long long rows = static_cast<long long>(N) * B;
+    accept_length_kernel<<<static_cast<unsigned>((rows + 255) / 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        gamma, rows, K, est, loss);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "accept-length kernel launch failed: %s", cudaGetErrorString(e));
+    return SPEC_OK;
+}
+
 spec_status spec_verify_static(const void* target_logits, const void* draft_logits, spec_dtype dtype,
                                const int32_t* draft_tokens, const uint64_t* seeds, int B, int K, int V,
                                float temperature, int32_t* accept_len, int32_t* out_tokens, float* diag,

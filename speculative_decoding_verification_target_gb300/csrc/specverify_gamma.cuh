@@ -29,7 +29,8 @@ constexpr int GW = 16;                       // warps per CTA
 constexpr int GNT = GW * 32;
 constexpr int G_PIECE_BYTES = 4096;          // one bulk copy: 2048 bf16 or 1024 fp32 logits
 constexpr int G_R = 3;                       // ring slots per warp
-constexpr int G_CAP = 4;                     // pieces a warp parks in tensor memory (32 columns each)
+constexpr int G_CAP = 4;                     // pieces of a warp's tensor-memory share (32 columns each)
+constexpr int G_HALF = G_CAP / 2;            // pieces of one unit parked (the share is double buffered)
 constexpr int G_TMEM_COLS = 512;
 constexpr size_t G_SMEM = static_cast<size_t>(GW) * G_R * G_PIECE_BYTES + static_cast<size_t>(GW) * G_R * 8;
 
@@ -292,8 +293,10 @@ template <class E>
 __global__ void __launch_bounds__(GNT, 1) gamma_kernel(const __grid_constant__ CgParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ uint32_t s_tmem;
-    __shared__ float2 s_ms[2][GW];   // per step parity: the warps' (max, sum) of unit s
-    __shared__ float s_g[2][GW];     // per step parity: the warps' gamma partials of unit s - 1
+    __shared__ float2 s_ms[4][GW];   // per unit u (mod 4): the warps' (max, sum) of its row
+    __shared__ float s_g[4][GW];     // per unit u (mod 4): the warps' gamma partials
+    __shared__ uint64_t s_bar_a[2];  // per unit parity: every warp has stored its (max, sum) of unit u
+    __shared__ uint64_t s_bar_g[2];  // per unit parity: every warp has stored its gamma partial of unit u
     using Raw = typename E::Raw;
     constexpr int NCH = GPiece<E>::NCH;
     constexpr int PEG = G_PIECE_BYTES / E::BYTES;   // logits per piece
@@ -318,12 +321,21 @@ __global__ void __launch_bounds__(GNT, 1) gamma_kernel(const __grid_constant__ C
         for (int q = 0; q < G_R; ++q) mbar_init(&full[q], 1);
         fence_mbarrier_init_cluster();
     }
+    if (threadIdx.x == 0) {
+        for (int q = 0; q < 2; ++q) {
+            mbar_init(&s_bar_a[q], GW);
+            mbar_init(&s_bar_g[q], GW);
+        }
+        fence_mbarrier_init_cluster();
+    }
     tmem_fence_before();
     __syncthreads();
     tmem_fence_after();
     const uint32_t tbase = s_tmem;
-    // this warp's columns: lanes 32 (warp mod 4) .. + 31, columns 128 (warp / 4) .. + 127
+    // this warp's columns: lanes 32 (warp mod 4) .. + 31, columns 128 (warp / 4) .. + 127, as two halves of
+    // G_HALF pieces: unit u parks its first G_HALF pieces in half u mod 2
     const uint32_t twarp = tbase + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + static_cast<uint32_t>((warp >> 2) * G_CAP * 32);
+    auto tcol = [&](int u, int k) -> uint32_t { return twarp + static_cast<uint32_t>(((u & 1) * G_HALF + k) * 32); };
 
     // this CTA's run of units (the host checks that U fits in 31 bits)
     const int u0 = static_cast<int>(static_cast<long long>(blockIdx.x) * p.U / p.G);
@@ -353,8 +365,9 @@ __global__ void __launch_bounds__(GNT, 1) gamma_kernel(const __grid_constant__ C
             const uint32_t bytes = static_cast<uint32_t>(len) * E::BYTES;
             mbar_arrive_expect_tx(&full[islot], bytes);
             // evict-first where this is the logits' last read (bonus rows, drafter pieces parked in tensor
-            // memory); evict-last for a position's target row, which its drafters' pass 2 reads again
-            const uint64_t pol = it_kind == 0 ? pol_last : ((it_kind == 2 || it_k < G_CAP) ? pol_first : pol_normal);
+            // memory); evict-last for a position's target row, which its drafters' pass 2 reads again, and for
+            // the drafter pieces pass 2 re-reads from L2
+            const uint64_t pol = it_kind == 0 ? pol_last : ((it_kind == 2 || it_k < G_HALF) ? pol_first : pol_last);
             bulk_load(ring + static_cast<size_t>(islot) * G_PIECE_BYTES, it_row + static_cast<size_t>(pc) * G_PIECE_BYTES,
                       bytes, &full[islot], pol);
             ++copies;
@@ -405,102 +418,131 @@ __global__ void __launch_bounds__(GNT, 1) gamma_kernel(const __grid_constant__ C
         for (int q = 0; q < NCH; ++q) r[q] = E::template gload<false>(piece, (lane + 32 * q) * CHUNK, len);
     };
 
-    int prev_kind = -1;                   // kind of unit s - 1
-    size_t prev_gidx = 0;                 // its gamma index when it is a D unit
-    const unsigned char* prev_trow = nullptr;   // its rows (pass 2 of a D unit)
-    const unsigned char* prev_row = nullptr;
-    bool prev_last = false;               // it is its position's last drafter
-    float pend_bt = 0.f, pend_bd = 0.f;   // log2 offsets of unit s - 1 when it is a D unit
+    // Step t: pass 1 of unit t, whose (max, sum) pairs are published with an arrival on s_bar_a; then the
+    // wait for every warp's pass 1 of unit t - 1, its row statistics, and (a D unit) its pass 2, published on
+    // s_bar_g; the last warp sums unit t - 2's gamma partials. A warp waits for the others only a whole pass
+    // after it published, so the warps need not run in step. Every unit arrives on both barriers, so a
+    // barrier's phase parity is the unit index / 2 mod 2; a warp can reach unit u + 2's arrival only after
+    // unit u's phase completed, and the shared slots (unit mod 4) are rewritten only after every warp read them.
+    float pend_bt = 0.f, pend_bd = 0.f;   // log2 offsets of the D unit whose pass 2 runs in this step
     float bt_item = 0.f;                  // log2 offset of the latest T unit's row
-    UnitSeq cu = first;   // the consumer's unit (unit s)
-    for (int s = 0; s <= S; ++s) {
-        const bool has1 = s < S;
-        const int kind1 = has1 ? cu.kind(p) : -1;
-        const unsigned char* cur_row = p.tma ? nullptr : cu.row(p, row_bytes);
-        const bool has2 = prev_kind == 1;
-        float m = NINF, sm = 0.f;
-        float2 acc = make_float2(0.f, 0.f);
-        for (int k = 0; k < nmine; ++k) {
-            const int pc = warp + GW * k;
-            const int len = min(PEG, V - pc * PEG);
-            const size_t poff = static_cast<size_t>(pc) * G_PIECE_BYTES;
-            if (has2) {   // pass 2 of unit s - 1: the target piece from L2, the drafter piece from tensor memory
-                Raw rt[NCH], rd[NCH];
-                if (p.tma) {
-                    // the target row stays in L2 for the position's next drafter; the last one lets it go
-                    const uint64_t tpol = prev_last ? pol_first : pol_last;
-                    const unsigned char* tp = prev_trow + poff;
-                    if (len == PEG) {
-#pragma unroll
-                        for (int q = 0; q < NCH; ++q) rt[q] = GPiece<E>::ld_full(tp, (lane + 32 * q) * CHUNK, tpol);
-                    } else {
-#pragma unroll
-                        for (int q = 0; q < NCH; ++q) rt[q] = GPiece<E>::ld_keep(tp, (lane + 32 * q) * CHUNK, len, tpol);
-                    }
-                } else {
-                    gather(rt, prev_trow, poff, len);
-                }
-                if (k < G_CAP) {
-                    GPiece<E>::tmem_ld(twarp + 32 * k, rd);
-                } else if (p.tma) {
-#pragma unroll
-                    for (int q = 0; q < NCH; ++q) rd[q] = E::template gload<true>(prev_row + poff, (lane + 32 * q) * CHUNK, len);
-                } else {
-                    gather(rd, prev_row, poff, len);
-                }
-                g_overlap<E>(rt, rd, c, pend_bt, pend_bd, acc);
-            }
-            if (has1) {   // pass 1 of unit s
+    size_t gidx1 = 0, gidx2 = 0;          // gamma index of units t - 1 and t - 2 (D units)
+    int kind1 = -1, kind2 = -1;           // kinds of units t - 1 and t - 2
+    const unsigned char* prev_trow = nullptr;   // rows of unit t - 1
+    const unsigned char* prev_row = nullptr;
+    bool prev_last = false;
+    bool okb = true;                      // every barrier wait so far succeeded
+    UnitSeq cu = first;                   // unit t
+    UnitSeq pu = first;                   // unit t - 1
+    auto sum_gamma = [&](int u, size_t gidx) {   // the last warp: unit u's 16 partials in warp order
+        if (okb) okb = mbar_wait_bounded(&s_bar_g[u & 1], static_cast<uint32_t>((u >> 1) & 1), p.status, STATUS_TIMEOUT, WAIT_LIMIT_NS);
+        const float g = warp_sum(lane < GW ? s_g[u & 3][lane] : 0.f);
+        if (lane == 0) {
+            p.gamma[gidx] = g;
+            if (p.loss) p.loss[gidx] = 1.f - g;
+        }
+    };
+    for (int t = 0; t <= S; ++t) {
+        const int kind0 = t < S ? cu.kind(p) : -1;
+        // ---- pass 1 of unit t ----
+        if (t < S) {
+            const unsigned char* cur_row = p.tma ? nullptr : cu.row(p, row_bytes);
+            float m = NINF, sm = 0.f;
+            for (int k = 0; k < nmine; ++k) {
+                const int pc = warp + GW * k;
+                const int len = min(PEG, V - pc * PEG);
                 Raw r1[NCH];
                 if (p.tma) take(r1, len);
-                else gather(r1, cur_row, poff, len);
-                if (kind1 == 1 && k < G_CAP) GPiece<E>::tmem_st(twarp + 32 * k, r1);   // its columns were read above
+                else gather(r1, cur_row, static_cast<size_t>(pc) * G_PIECE_BYTES, len);
+                if (kind0 == 1 && k < G_HALF) GPiece<E>::tmem_st(tcol(t, k), r1);
                 g_stats<E>(r1, c, m, sm);
             }
-        }
-        if (has1) {
             const MaxSum w = warp_ms(MaxSum{m, sm}, c);
-            if (lane == 0) s_ms[s & 1][warp] = make_float2(w.m, w.s);
-            if (kind1 == 1) tmem_wait_st();
+            if (lane == 0) s_ms[t & 3][warp] = make_float2(w.m, w.s);
+            if (kind0 == 1) tmem_wait_st();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_bar_a[t & 1]);
         }
-        if (has2) {
-            const float g = warp_sum(acc.x + acc.y);
-            if (lane == 0) s_g[s & 1][warp] = g;
-        }
-        __syncthreads();
-        if (has2 && warp == GW - 1) {   // gamma of unit s - 1: the 16 partials in warp order
-            const float g = warp_sum(lane < GW ? s_g[s & 1][lane] : 0.f);
-            if (lane == 0) {
-                p.gamma[prev_gidx] = g;
-                if (p.loss) p.loss[prev_gidx] = 1.f - g;
-            }
-        }
-        prev_kind = kind1;
-        if (has1) {   // the row's (max, sum): the 16 warp pairs merged in warp order, the same in every warp
-            const float2 v = lane < GW ? s_ms[s & 1][lane] : make_float2(NINF, 0.f);
+        // ---- unit t - 1: its row statistics, then its pass 2 ----
+        if (t >= 1) {
+            const int u = t - 1;
+            if (okb) okb = mbar_wait_bounded(&s_bar_a[u & 1], static_cast<uint32_t>((u >> 1) & 1), p.status, STATUS_TIMEOUT, WAIT_LIMIT_NS);
+            // the row's (max, sum): the 16 warp pairs merged in warp order, the same in every warp
+            const float2 v = lane < GW ? s_ms[u & 3][lane] : make_float2(NINF, 0.f);
             const MaxSum r = warp_ms(MaxSum{v.x, v.y}, c);
             const float beta = beta_of(r, c);
-            if (kind1 == 1) {
-                const int i = cu.drafter();
+            if (kind1 == 0) {
+                bt_item = beta;
+            } else if (kind1 == 1) {
                 pend_bt = bt_item;
                 pend_bd = beta;
-                prev_gidx = (static_cast<size_t>(i) * p.B + cu.b) * p.K + cu.j;
-                prev_trow = cu.trow(p, row_bytes);
-                prev_row = cu.row(p, row_bytes);
-                prev_last = i == p.N - 1;
-            } else if (kind1 == 0) {
-                bt_item = beta;
             }
             if (p.row_ms && warp == 0 && lane == 0) {
                 long long ri = -1;
-                if (kind1 != 1) ri = static_cast<long long>(cu.b) * (p.K + 1) + cu.j;
-                else if (cu.drafter() == p.selected)
-                    ri = static_cast<long long>(p.B) * (p.K + 1) + static_cast<long long>(cu.b) * p.K + cu.j;
+                if (kind1 != 1) ri = static_cast<long long>(pu.b) * (p.K + 1) + pu.j;
+                else if (pu.drafter() == p.selected)
+                    ri = static_cast<long long>(p.B) * (p.K + 1) + static_cast<long long>(pu.b) * p.K + pu.j;
                 if (ri >= 0) p.row_ms[ri] = make_float2(r.m, r.s);
+            }
+            float2 acc = make_float2(0.f, 0.f);
+            if (kind1 == 1) {   // pass 2: the target piece from L2, the drafter piece from tensor memory or L2
+                for (int k = 0; k < nmine; ++k) {
+                    const int pc = warp + GW * k;
+                    const int len = min(PEG, V - pc * PEG);
+                    const size_t poff = static_cast<size_t>(pc) * G_PIECE_BYTES;
+                    Raw rt[NCH], rd[NCH];
+                    if (p.tma) {
+                        // the target row stays in L2 for the position's next drafter; the last one lets it go
+                        const uint64_t tpol = prev_last ? pol_first : pol_last;
+                        const unsigned char* tp = prev_trow + poff;
+                        if (len == PEG) {
+#pragma unroll
+                            for (int q = 0; q < NCH; ++q) rt[q] = GPiece<E>::ld_full(tp, (lane + 32 * q) * CHUNK, tpol);
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < NCH; ++q)
+                                rt[q] = GPiece<E>::ld_keep(tp, (lane + 32 * q) * CHUNK, len, tpol);
+                        }
+                    } else {
+                        gather(rt, prev_trow, poff, len);
+                    }
+                    if (k < G_HALF) {
+                        GPiece<E>::tmem_ld(tcol(u, k), rd);
+                    } else if (p.tma) {
+#pragma unroll
+                        for (int q = 0; q < NCH; ++q)
+                            rd[q] = E::template gload<true>(prev_row + poff, (lane + 32 * q) * CHUNK, len);
+                    } else {
+                        gather(rd, prev_row, poff, len);
+                    }
+                    g_overlap<E>(rt, rd, c, pend_bt, pend_bd, acc);
+                }
+                const float g = warp_sum(acc.x + acc.y);
+                if (lane == 0) s_g[u & 3][warp] = g;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_bar_g[u & 1]);
+        }
+        // ---- unit t - 2's gamma (its partials were published one step ago) ----
+        if (warp == GW - 1 && t >= 2 && kind2 == 1) sum_gamma(t - 2, gidx2);
+        // ---- move the unit window ----
+        kind2 = kind1;
+        gidx2 = gidx1;
+        if (t < S) {
+            kind1 = kind0;
+            pu = cu;
+            if (kind0 == 1) {
+                const int i = cu.drafter();
+                gidx1 = (static_cast<size_t>(i) * p.B + cu.b) * p.K + cu.j;
+                prev_trow = cu.trow(p, row_bytes);
+                prev_row = cu.row(p, row_bytes);
+                prev_last = i == p.N - 1;
             }
             cu.next(p, pre, u0);
         }
     }
+    // unit S - 1's gamma (published in the last step)
+    if (warp == GW - 1 && kind2 == 1 && S >= 1) sum_gamma(S - 1, gidx2);
 
     // after a failed wait, copies may still be in flight: they must land before the CTA may exit
     if (p.tma && lane == 0 && !issuing) {
@@ -513,6 +555,26 @@ __global__ void __launch_bounds__(GNT, 1) gamma_kernel(const __grid_constant__ C
     tmem_fence_after();
     if (warp == 0)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(G_TMEM_COLS) : "memory");
+}
+
+// ------------------------------------------------------------------------------------------------
+// accept-length estimate
+// ------------------------------------------------------------------------------------------------
+// HedgeSpec's accept-length estimate from the counterfactual gamma ("Not-a-Bandit ...", Key design 2 and
+// 3; the page's displays are missing, reading: est = 1 + sum_{k=1..K} prod_{j<=k} gamma_j, loss =
+// K + 1 - est): one thread per (drafter, sequence), gamma [N, B, K] read in order.
+__global__ void __launch_bounds__(256) accept_length_kernel(const float* __restrict__ gamma, long long rows, int K,
+                                                            float* __restrict__ est, float* __restrict__ loss) {
+    const long long r = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (r >= rows) return;
+    const float* g = gamma + r * K;
+    float run = 1.f, total = 1.f;
+    for (int k = 0; k < K; ++k) {
+        run *= __ldg(g + k);
+        total += run;
+    }
+    est[r] = total;
+    if (loss) loss[r] = static_cast<float>(K + 1) - total;
 }
 
 }  // namespace specv

@@ -580,3 +580,26 @@ def test_greedy_named_workload_full():
     assert np.array_equal(out["accept_len"].cpu().numpy(), ref["accept_len"])
     assert np.array_equal(out["out_tokens"].cpu().numpy(), ref["out_tokens"])
     assert 0 < ref["accept_len"].mean() < w.K
+
+
+# ------------------------------------------------------------------------------------------------
+# HedgeSpec accept-length estimate over the counterfactual gamma
+# ------------------------------------------------------------------------------------------------
+def test_accept_length_estimate():
+    """The epilogue on the GPU's own gamma against the oracle's formula (same input), and end to end on the
+    HedgeSpec pool: the estimate from the GPU gamma against the estimate from the oracle's gamma."""
+    w = workloads.WORKLOADS["hedgespec_n7_b32_k5"]
+    inp = workloads.make(w, device="cuda")
+    out = sv.counterfactual_gamma(inp["target"], inp["drafters"], w.temperature, -1)
+    est = sv.accept_length_estimate(out["gamma"])
+    torch.cuda.synchronize()
+    e_ref, l_ref = oracle.accept_length(out["gamma"].cpu().numpy().astype(np.float64))
+    assert np.abs(est["est"].cpu().numpy() - e_ref).max() <= 1e-5
+    assert np.abs(est["loss"].cpu().numpy() - l_ref).max() <= 1e-5
+    ref = oracle.counterfactual(host(inp["target"]), host(inp["drafters"]), w.temperature, -1)
+    e_full, _ = oracle.accept_length(ref["gamma"])
+    assert np.abs(est["est"].cpu().numpy() - e_full).max() <= w.K * PROB_TOL
+    e = est["est"].cpu().numpy()
+    assert np.all((e >= 1) & (e <= w.K + 1))
+    # drafters with less noise are estimated to keep longer chains, on average
+    assert np.all(np.diff(e.mean(axis=1)) < 0)
