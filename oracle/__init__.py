@@ -70,6 +70,10 @@ def _load():
     lib.spec_oracle_greedy.restype = i32
     lib.spec_oracle_accept_length.argtypes = [P, i32, i32, i32, P, P]
     lib.spec_oracle_accept_length.restype = None
+    lib.spec_oracle_normalhedge.argtypes = [P, P, P, i32]
+    lib.spec_oracle_normalhedge.restype = i32
+    lib.spec_oracle_normalhedge_scale.argtypes = [P, i32]
+    lib.spec_oracle_normalhedge_scale.restype = f64
     lib.spec_oracle_cactus.argtypes = [i32, P, P, P, P, P, i32, i32, i32, f64, f64, P, P, P, P, P, P, i32]
     lib.spec_oracle_cactus.restype = i32
     lib.spec_oracle_cactus_ex.argtypes = [i32, P, P, P, P, P, i32, i32, i32, f64, f64, i32, P, P, P, P, P, P, i32]
@@ -222,6 +226,18 @@ def accept_length(gamma):
     loss = np.empty((N, B))
     lib.spec_oracle_accept_length(_ptr(g), N, B, K, _ptr(est), _ptr(loss))
     return est, loss
+
+
+def normalhedge(regret, loss, weights):
+    """One NormalHedge round (Chaudhuri, Freund, Hsu 2009): regret += (weights . loss) - loss, then the new
+    weights. Returns (regret, weights, c) as new arrays (c = 0 when no regret is positive)."""
+    lib = _load()
+    R = np.array(regret, dtype=np.float64)
+    p = np.array(weights, dtype=np.float64)
+    l_ = np.ascontiguousarray(loss, dtype=np.float64)
+    if lib.spec_oracle_normalhedge(_ptr(R), _ptr(l_), _ptr(p), R.size) != 0:
+        raise ValueError("normalhedge: N must be in [1, 64]")
+    return R, p, lib.spec_oracle_normalhedge_scale(_ptr(R), R.size)
 
 
 def cactus(target, draft, tokens, seeds, delta, temperature=1.0, seq_index=None, nthreads=0, exact=False):

@@ -477,6 +477,71 @@ void spec_oracle_accept_length(const double* gamma, int N, int B, int K, double*
     }
 }
 
+/* NormalHedge (Chaudhuri, Freund, Hsu, "A parameter-free hedging algorithm", NIPS 2009), the learner
+ * [Hedge] names for drafter selection (the page states no update rule). One round: the learner played
+ * weights p over N experts and saw losses l; its regret to expert i grows by (sum_j p_j l_j) - l_i. The next
+ * weights are p_i proportional to ([R_i]+ / c) exp([R_i]+^2 / (2 c)), where c > 0 solves
+ * (1/N) sum_i exp([R_i]+^2 / (2 c)) = e; when no regret is positive the weights are uniform. c is found by
+ * bisection on log c, the mean taken as a log-sum-exp so that no term overflows. R, p: in/out [N]. */
+static double nh_log_mean(const double* Rp, int N, double c)
+{
+    double mx = -INFINITY;
+    for (int i = 0; i < N; i++) {
+        double a = Rp[i] * Rp[i] / (2.0 * c);
+        if (a > mx) mx = a;
+    }
+    double s = 0.0;
+    for (int i = 0; i < N; i++) s += exp(Rp[i] * Rp[i] / (2.0 * c) - mx);
+    return mx + log(s / N);
+}
+
+double spec_oracle_normalhedge_scale(const double* R, int N)
+{
+    double Rp[64];
+    int any = 0;
+    for (int i = 0; i < N; i++) {
+        Rp[i] = R[i] > 0.0 ? R[i] : 0.0;
+        if (Rp[i] > 0.0) any = 1;
+    }
+    if (!any) return 0.0;
+    /* log-mean is decreasing in c: above 1 for small c, towards 0 for large c */
+    double lo = -200.0, hi = 200.0;   /* log c */
+    for (int it = 0; it < 400; it++) {
+        double mid = 0.5 * (lo + hi);
+        if (mid <= lo || mid >= hi) break;
+        if (nh_log_mean(Rp, N, exp(mid)) > 1.0) lo = mid;
+        else hi = mid;
+    }
+    return exp(0.5 * (lo + hi));
+}
+
+int spec_oracle_normalhedge(double* R, const double* loss, double* p, int N)
+{
+    if (N < 1 || N > 64) return -1;
+    double lp = 0.0;
+    for (int i = 0; i < N; i++) lp += p[i] * loss[i];
+    for (int i = 0; i < N; i++) R[i] += lp - loss[i];
+    double c = spec_oracle_normalhedge_scale(R, N);
+    if (c == 0.0) {
+        for (int i = 0; i < N; i++) p[i] = 1.0 / N;
+        return 0;
+    }
+    /* weights in log space relative to the largest, then normalised */
+    double lw[64], mx = -INFINITY;
+    for (int i = 0; i < N; i++) {
+        double r = R[i] > 0.0 ? R[i] : 0.0;
+        lw[i] = r > 0.0 ? log(r / c) + r * r / (2.0 * c) : -INFINITY;
+        if (lw[i] > mx) mx = lw[i];
+    }
+    double s = 0.0;
+    for (int i = 0; i < N; i++) {
+        p[i] = lw[i] == -INFINITY ? 0.0 : exp(lw[i] - mx);
+        s += p[i];
+    }
+    for (int i = 0; i < N; i++) p[i] /= s;
+    return 0;
+}
+
 /* HedgeSpec counterfactual evaluation ([Hedge] Key design 1): for every drafter i, sequence b and
  * level j < K, gamma[i,b,j] = sum_x min(p_target(x), q_i(x)), the acceptance probability of
  * drafter i at that level ([SpS] §6.3: P(accept) = sum_x min(p, q) = 1 - TV). tv[i,b,j] =

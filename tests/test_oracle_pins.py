@@ -681,3 +681,44 @@ def test_accept_length_estimate_matches_simulated_chains():
     L = np.where(acc.all(axis=1), K, np.argmin(acc, axis=1))
     m, se = (1 + L).mean(), (1 + L).std() / np.sqrt(n)
     assert abs(est[0, 0] - m) < 5 * se
+
+
+# ----------------------------------------------------------------------------------------------
+# NormalHedge (Chaudhuri, Freund, Hsu 2009), the learner the HedgeSpec notes name
+# ----------------------------------------------------------------------------------------------
+def test_normalhedge_scale_and_weights():
+    rng = np.random.default_rng(90)
+    for _ in range(300):
+        N = int(rng.integers(2, 40))
+        R = rng.normal(0, rng.uniform(0.1, 20), N)
+        p0 = np.full(N, 1.0 / N)
+        Rn, p, c = oracle.normalhedge(R, np.zeros(N), p0)       # zero losses: the regrets stay
+        assert np.array_equal(Rn, R)
+        pos = np.maximum(R, 0)
+        if not np.any(pos > 0):
+            assert c == 0 and np.allclose(p, 1.0 / N)
+            continue
+        # the scale solves mean exp(R+^2 / 2c) = e
+        assert np.mean(np.exp(pos ** 2 / (2 * c))) == pytest.approx(np.e, rel=1e-10)
+        assert p.sum() == pytest.approx(1.0, abs=1e-12) and np.all(p >= 0)
+        assert np.all(p[pos == 0] == 0)                            # no weight without positive regret
+        w = pos / c * np.exp(pos ** 2 / (2 * c))
+        assert np.allclose(p, w / w.sum(), rtol=1e-9, atol=1e-15)
+
+
+def test_normalhedge_regret_update_and_learning():
+    rng = np.random.default_rng(91)
+    N, T = 7, 400
+    R = np.zeros(N)
+    p = np.full(N, 1.0 / N)
+    for t in range(T):
+        loss = rng.uniform(0, 1, N)
+        loss[3] *= 0.5                                   # expert 3 is the best on average
+        lp = p @ loss
+        Rn, pn, _ = oracle.normalhedge(R, loss, p)
+        assert np.allclose(Rn, R + lp - loss, atol=1e-12)
+        # shifting every loss by a constant changes neither the regrets nor the weights
+        Rs, ps, _ = oracle.normalhedge(R, loss + 3.0, p)
+        assert np.allclose(Rs, Rn, atol=1e-9) and np.allclose(ps, pn, atol=1e-9)
+        R, p = Rn, pn
+    assert np.argmax(p) == 3 and p[3] > 0.5
