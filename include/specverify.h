@@ -152,6 +152,17 @@ spec_status spec_greedy_verify(const void* target_logits, spec_dtype dtype, cons
 spec_status spec_accept_length_estimate(const float* gamma, int N, int B, int K, float* est, float* loss,
                                         void* stream);
 
+/* One round of NormalHedge (Chaudhuri, Freund, Hsu, "A parameter-free hedging algorithm", NIPS 2009), the
+ * learner the HedgeSpec notes name for picking the drafter ("Not-a-Bandit ...", Key design 3; the pages
+ * give no update rule). weights: device float [N], the distribution the learner played this round, replaced
+ * by the next one; loss: device float [N], this round's loss per drafter (for example 1 - gamma at a level,
+ * or the accept-length loss); regret: device float [N], the cumulative regret, updated in place by
+ * (weights . loss) - loss. Next weights: p_i proportional to ([R_i]+ / c) exp([R_i]+^2 / (2 c)) with c solving
+ * (1/N) sum_i exp([R_i]+^2 / (2 c)) = e; uniform when no regret is positive. Start from regret 0 and uniform
+ * weights. Delayed feedback (the notes' queue of Joulani et al. 2013) is the caller's: apply rounds in the
+ * order their feedback arrives. 1 <= N <= 64. One warp; asynchronous on `stream`; allocates nothing. */
+spec_status spec_normalhedge_update(float* regret, const float* loss, float* weights, int N, void* stream);
+
 /* spec_verify for callers that cannot allocate device memory: same inputs, outputs and semantics, but no
  * workspace argument. Some callers run where allocation is not allowed or not possible: inside a memory
  * budget fixed in advance, under an allocator that must not grow, or from code that has no allocator at all.

@@ -21,6 +21,7 @@ SPEC_OK, SPEC_ERR_INVALID, SPEC_ERR_CUDA, SPEC_ERR_UNSUPPORTED = 0, 1, 2, 3
 STATUS_BAD_TOKEN, STATUS_TIMEOUT = 1, 2
 EXPORTS = ("spec_workspace_size", "spec_verify", "spec_counterfactual_gamma", "spec_cactus_verify", "spec_cactus_kl_verify",
            "spec_greedy_verify", "spec_accept_length_estimate",
+           "spec_normalhedge_update",
            "spec_read_status", "spec_clear_status", "spec_last_error",
            "spec_debug_last_plan", "spec_verify_static", "spec_debug_set_stats_grid")
 
@@ -63,6 +64,8 @@ def load(build_if_missing: bool = False):
     lib.spec_greedy_verify.restype = I
     lib.spec_accept_length_estimate.argtypes = [P, I, I, I, P, P, P]
     lib.spec_accept_length_estimate.restype = I
+    lib.spec_normalhedge_update.argtypes = [P, P, P, I, P]
+    lib.spec_normalhedge_update.restype = I
     lib.spec_read_status.argtypes = [P, P, P]
     lib.spec_read_status.restype = I
     lib.spec_clear_status.argtypes = [P, P]
@@ -218,6 +221,14 @@ def accept_length_estimate(gamma, *, est=None, loss=None, want_loss=True, stream
         loss = torch.empty((N, B), dtype=torch.float32, device=gamma.device)
     _check(load().spec_accept_length_estimate(_p(gamma), N, B, K, _p(est), _p(loss), _stream(stream)))
     return dict(est=est, loss=loss)
+
+
+def normalhedge_update(regret, loss, weights, stream=None):
+    """One NormalHedge round in place: regret += weights . loss - loss, weights <- the next distribution."""
+    N = regret.shape[0]
+    for t, nm in ((regret, "regret"), (loss, "loss"), (weights, "weights")):
+        _need(t, nm, torch.float32, (N,))
+    _check(load().spec_normalhedge_update(_p(regret), _p(loss), _p(weights), N, _stream(stream)))
 
 
 def counterfactual_gamma(target, drafters, temperature=1.0, selected=-1, tokens=None, seeds=None, *, gamma=None,

@@ -605,6 +605,15 @@ spec_status spec_accept_length_estimate(const float* gamma, int N, int B, int K,
     return SPEC_OK;
 }
 
+spec_status spec_normalhedge_update(float* regret, const float* loss, float* weights, int N, void* stream) {
+    if (N < 1 || N > MAX_N) return fail(SPEC_ERR_INVALID, "N must be in [1, %d] (got %d)", MAX_N, N);
+    if (!regret || !loss || !weights) return fail(SPEC_ERR_INVALID, "regret, loss and weights must not be NULL");
+    normalhedge_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(regret, loss, weights, N);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "NormalHedge kernel launch failed: %s", cudaGetErrorString(e));
+    return SPEC_OK;
+}
+
 spec_status spec_verify_static(const void* target_logits, const void* draft_logits, spec_dtype dtype,
                                const int32_t* draft_tokens, const uint64_t* seeds, int B, int K, int V,
                                float temperature, int32_t* accept_len, int32_t* out_tokens, float* diag,

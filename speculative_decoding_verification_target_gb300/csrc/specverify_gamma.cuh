@@ -577,4 +577,60 @@ __global__ void __launch_bounds__(256) accept_length_kernel(const float* __restr
     if (loss) loss[r] = static_cast<float>(K + 1) - total;
 }
 
+// ------------------------------------------------------------------------------------------------
+// NormalHedge
+// ------------------------------------------------------------------------------------------------
+// One NormalHedge round (Chaudhuri, Freund, Hsu, "A parameter-free hedging algorithm", NIPS 2009), the
+// learner the HedgeSpec notes name for drafter selection ("Not-a-Bandit ...", Key design 3); the pages
+// state no update rule. The learner played weights p over N <= 64 experts and saw losses l: the regret to
+// expert i grows by (p . l) - l_i, and the new weights are p_i proportional to ([R_i]+ / c)
+// exp([R_i]+^2 / (2 c)), where c solves (1/N) sum_i exp([R_i]+^2 / (2 c)) = e (uniform weights when no
+// regret is positive). One warp; lane l holds experts l and l + 32. c lies in [m^2 / (2 ln(N e)), m^2 / 2]
+// for the largest positive regret m (all exponents below 1 above that bracket, the largest alone above
+// e N below it), found by bisection on log c with the mean taken as a log-sum-exp.
+__device__ __forceinline__ float nh_log_mean(float a0, float a1, bool v0, bool v1, int N) {
+    const float NINF = __uint_as_float(0xFF800000u);
+    const float mx = warp_max(fmaxf(v0 ? a0 : NINF, v1 ? a1 : NINF));
+    const float s = warp_sum((v0 ? expf(a0 - mx) : 0.f) + (v1 ? expf(a1 - mx) : 0.f));
+    return mx + logf(s / static_cast<float>(N));
+}
+
+__global__ void __launch_bounds__(32) normalhedge_kernel(float* __restrict__ regret, const float* __restrict__ loss,
+                                                         float* __restrict__ weights, int N) {
+    const int lane = threadIdx.x;
+    const bool v0 = lane < N, v1 = lane + 32 < N;
+    const float p0 = v0 ? weights[lane] : 0.f, p1 = v1 ? weights[lane + 32] : 0.f;
+    const float l0 = v0 ? loss[lane] : 0.f, l1 = v1 ? loss[lane + 32] : 0.f;
+    const float lp = warp_sum(p0 * l0 + p1 * l1);
+    const float r0 = v0 ? regret[lane] + (lp - l0) : 0.f;
+    const float r1 = v1 ? regret[lane + 32] + (lp - l1) : 0.f;
+    if (v0) regret[lane] = r0;
+    if (v1) regret[lane + 32] = r1;
+    const float q0 = fmaxf(r0, 0.f), q1 = fmaxf(r1, 0.f);
+    const float m = warp_max(fmaxf(q0, q1));
+    if (!(m > 0.f)) {
+        const float u = 1.f / static_cast<float>(N);
+        if (v0) weights[lane] = u;
+        if (v1) weights[lane + 32] = u;
+        return;
+    }
+    const float lm2 = 2.f * logf(m);
+    float lo = lm2 - logf(2.f * (logf(static_cast<float>(N)) + 1.f)), hi = lm2 - logf(2.f);
+    for (int it = 0; it < 48; ++it) {
+        const float mid = 0.5f * (lo + hi);
+        const float c = expf(mid);
+        if (nh_log_mean(q0 * q0 / (2.f * c), q1 * q1 / (2.f * c), v0, v1, N) > 1.f) lo = mid;
+        else hi = mid;
+    }
+    const float c = expf(0.5f * (lo + hi));
+    const float NINF = __uint_as_float(0xFF800000u);
+    const float w0 = (v0 && q0 > 0.f) ? logf(q0 / c) + q0 * q0 / (2.f * c) : NINF;
+    const float w1 = (v1 && q1 > 0.f) ? logf(q1 / c) + q1 * q1 / (2.f * c) : NINF;
+    const float mx = warp_max(fmaxf(w0, w1));
+    const float e0 = w0 > NINF ? expf(w0 - mx) : 0.f, e1 = w1 > NINF ? expf(w1 - mx) : 0.f;
+    const float s = warp_sum(e0 + e1);
+    if (v0) weights[lane] = e0 / s;
+    if (v1) weights[lane + 32] = e1 / s;
+}
+
 }  // namespace specv

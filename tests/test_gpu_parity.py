@@ -603,3 +603,37 @@ def test_accept_length_estimate():
     assert np.all((e >= 1) & (e <= w.K + 1))
     # drafters with less noise are estimated to keep longer chains, on average
     assert np.all(np.diff(e.mean(axis=1)) < 0)
+
+
+# ------------------------------------------------------------------------------------------------
+# NormalHedge round
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("N", [1, 7, 21, 33, 64])
+def test_normalhedge_round(N):
+    """Single rounds from random states against the fp64 oracle, then 300 rounds where one drafter has the
+    smaller loss: the GPU learner follows the oracle's and concentrates on it."""
+    rng = np.random.default_rng(100 + N)
+    for _ in range(20):
+        R = rng.normal(0, rng.uniform(0.1, 10), N)
+        p = rng.dirichlet(np.ones(N))
+        loss = rng.uniform(0, 1, N)
+        R_ref, p_ref, _ = oracle.normalhedge(R, loss, p)
+        Rg = torch.tensor(R, dtype=torch.float32, device="cuda")
+        pg = torch.tensor(p, dtype=torch.float32, device="cuda")
+        sv.normalhedge_update(Rg, torch.tensor(loss, dtype=torch.float32, device="cuda"), pg)
+        torch.cuda.synchronize()
+        assert np.abs(Rg.cpu().numpy() - R_ref).max() <= 1e-5 * (1 + np.abs(R_ref).max())
+        assert np.abs(pg.cpu().numpy() - p_ref).max() <= 1e-4
+    R = np.zeros(N)
+    p = np.full(N, 1.0 / N)
+    Rg = torch.zeros(N, device="cuda")
+    pg = torch.full((N,), 1.0 / N, device="cuda")
+    for t in range(300):
+        loss = rng.uniform(0, 1, N)
+        loss[N // 2] *= 0.4
+        R, p, _ = oracle.normalhedge(R, loss, p)
+        sv.normalhedge_update(Rg, torch.tensor(loss, dtype=torch.float32, device="cuda"), pg)
+    torch.cuda.synchronize()
+    assert np.abs(pg.cpu().numpy() - p).max() <= 1e-3
+    if N > 1:
+        assert int(pg.argmax()) == N // 2
