@@ -74,6 +74,10 @@ def _load():
     lib.spec_oracle_normalhedge.restype = i32
     lib.spec_oracle_normalhedge_scale.argtypes = [P, i32]
     lib.spec_oracle_normalhedge_scale.restype = f64
+    lib.spec_oracle_filter_row.argtypes = [P, i32, f64, i32, f64, P, P, P]
+    lib.spec_oracle_filter_row.restype = f64
+    lib.spec_oracle_verify_filtered.argtypes = [i32, P, P, P, P, i32, i32, i32, f64, i32, f64, P, P, P, P, P, P, P]
+    lib.spec_oracle_verify_filtered.restype = i32
     lib.spec_oracle_cactus.argtypes = [i32, P, P, P, P, P, i32, i32, i32, f64, f64, P, P, P, P, P, P, i32]
     lib.spec_oracle_cactus.restype = i32
     lib.spec_oracle_cactus_ex.argtypes = [i32, P, P, P, P, P, i32, i32, i32, f64, f64, i32, P, P, P, P, P, P, i32]
@@ -238,6 +242,44 @@ def normalhedge(regret, loss, weights):
     if lib.spec_oracle_normalhedge(_ptr(R), _ptr(l_), _ptr(p), R.size) != 0:
         raise ValueError("normalhedge: N must be in [1, 64]")
     return R, p, lib.spec_oracle_normalhedge_scale(_ptr(R), R.size)
+
+
+def filter_row(x, temperature=1.0, top_k=0, top_p=1.0):
+    """Standardised-sampling filter of one row of logits: top-k then top-p, ties at a threshold kept.
+    Returns (filtered logits with -inf outside the kept set, threshold, top-p margin)."""
+    lib = _load()
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty_like(x)
+    sc = np.empty_like(x)
+    m = np.zeros(1)
+    thr = lib.spec_oracle_filter_row(_ptr(x), x.size, float(temperature), int(top_k), float(top_p), _ptr(out),
+                                     _ptr(m), _ptr(sc))
+    return out, thr, float(m[0])
+
+
+def verify_filtered(target, draft, tokens, seeds, temperature=1.0, top_k=0, top_p=1.0):
+    """Standard speculative sampling on the standardised rows (every target and draft row filtered by
+    filter_row with the same temperature, top_k and top_p). Adds thr and pmargin [B*(K+1) + B*K] (target
+    rows, then draft rows) to the verify outputs."""
+    lib = _load()
+    target, dt = _logits(target)
+    draft, dd = _logits(draft)
+    assert dt == dd
+    B, K1, V = target.shape
+    K = K1 - 1
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    seeds = np.ascontiguousarray(seeds, dtype=np.uint64)
+    R = B * (2 * K + 1)
+    out = dict(accept_len=np.zeros(B, np.int32), out_tokens=np.zeros((B, K + 1), np.int32),
+               diag=np.zeros((B, K, 4)), accept_margin=np.zeros((B, K)), cdf_margin=np.zeros(B),
+               thr=np.zeros(R), pmargin=np.zeros(R))
+    rc = lib.spec_oracle_verify_filtered(dt, _ptr(target), _ptr(draft), _ptr(tokens), _ptr(seeds), B, K, V,
+                                         float(temperature), int(top_k), float(top_p), _ptr(out["accept_len"]),
+                                         _ptr(out["out_tokens"]), _ptr(out["diag"]), _ptr(out["accept_margin"]),
+                                         _ptr(out["cdf_margin"]), _ptr(out["thr"]), _ptr(out["pmargin"]))
+    if rc != 0:
+        raise ValueError("oracle verify_filtered rejected its arguments")
+    return out
 
 
 def cactus(target, draft, tokens, seeds, delta, temperature=1.0, seq_index=None, nthreads=0, exact=False):

@@ -542,6 +542,97 @@ int spec_oracle_normalhedge(double* R, const double* loss, double* p, int N)
     return 0;
 }
 
+/* Standardised sampling ([SpS] §8 Q4: temperature, top-k and top-p are folded into p and q before the
+ * ratio, the same transforms for the target and the draft row). For one row of logits x at temperature T:
+ * top-k (0 < k < V) keeps the logits at or above the k-th largest; then top-p (0 < top_p < 1) keeps, of what
+ * is left, the logits at or above the value v* at which the mass of the renormalised distribution, summed
+ * from the largest logit down, first reaches top_p. Readings (the pages give neither rule): ties at either
+ * threshold are all kept (the kept set depends on values only), top-k comes before top-p, and the kept
+ * logits keep their values while the others become -inf. Writes the filtered row to out and returns the
+ * threshold (-inf when nothing is filtered); *margin = the smallest distance of a top-p partial sum from
+ * top_p (in the renormalised mass; +inf without top-p), the near-tie measure of the top-p decision. */
+static int cmp_desc(const void* a, const void* b)
+{
+    double x = *(const double*)a, y = *(const double*)b;
+    return (x < y) - (x > y);
+}
+
+double spec_oracle_filter_row(const double* x, int V, double T, int top_k, double top_p, double* out,
+                              double* margin, double* scratch)
+{
+    double thr = -INFINITY;
+    if (margin) *margin = INFINITY;
+    for (int i = 0; i < V; i++) scratch[i] = x[i];
+    qsort(scratch, (size_t)V, sizeof(double), cmp_desc);
+    if (top_k > 0 && top_k < V) thr = scratch[top_k - 1];
+    if (top_p > 0.0 && top_p < 1.0) {
+        double m = scratch[0];
+        double total = 0.0;
+        for (int i = 0; i < V && scratch[i] >= thr; i++) total += exp((scratch[i] - m) / T);
+        double run = 0.0;
+        int i = 0;
+        while (i < V && scratch[i] >= thr) {
+            /* every copy of a value enters together */
+            double v = scratch[i], block = 0.0;
+            int j = i;
+            while (j < V && scratch[j] == v) { block += exp((v - m) / T); j++; }
+            double before = run / total;
+            run += block;
+            double after = run / total;
+            if (margin) {
+                double d1 = fabs(before - top_p), d2 = fabs(after - top_p);
+                if (d1 < *margin) *margin = d1;
+                if (d2 < *margin) *margin = d2;
+            }
+            if (after >= top_p) { thr = v > thr ? v : thr; break; }
+            i = j;
+        }
+    }
+    for (int i = 0; i < V; i++) out[i] = x[i] >= thr ? x[i] : -INFINITY;
+    return thr;
+}
+
+/* spec_oracle_verify on the standardised rows: every target and draft row filtered by
+ * spec_oracle_filter_row (same T, top_k, top_p), then the ordinary chain. thr: nullable [B*(K+1) + B*K]
+ * thresholds (target rows, then draft rows); pmargin: nullable, the same layout, the top-p margins. */
+int spec_oracle_verify_filtered(int dtype, const void* target, const void* draft, const int32_t* tokens,
+                                const uint64_t* seeds, int B, int K, int V, double T, int top_k, double top_p,
+                                int32_t* accept_len, int32_t* out_tokens, double* diag, double* accept_margin,
+                                double* cdf_margin, double* thr, double* pmargin)
+{
+    if (K < 1 || K > ORACLE_MAX_K || V < 1 || B < 0) return -1;
+    double* x = (double*)malloc(sizeof(double) * (size_t)V);
+    double* scratch = (double*)malloc(sizeof(double) * (size_t)V);
+    double* y = (double*)malloc(sizeof(double) * (size_t)V);
+    /* the filtered rows hold input values or -inf, so fp32 stores them exactly */
+    float* ft = (float*)malloc(sizeof(float) * (size_t)B * (K + 1) * V);
+    float* fd = (float*)malloc(sizeof(float) * (size_t)B * K * V);
+    for (long long r = 0; r < (long long)B * (K + 1); r++) {
+        load_row(dtype, target, (size_t)r, V, x);
+        double mg;
+        double t = spec_oracle_filter_row(x, V, T, top_k, top_p, y, &mg, scratch);
+        for (int v = 0; v < V; v++) ft[r * V + v] = (float)y[v];
+        if (thr) thr[r] = t;
+        if (pmargin) pmargin[r] = mg;
+    }
+    for (long long r = 0; r < (long long)B * K; r++) {
+        load_row(dtype, draft, (size_t)r, V, x);
+        double mg;
+        double t = spec_oracle_filter_row(x, V, T, top_k, top_p, y, &mg, scratch);
+        for (int v = 0; v < V; v++) fd[r * V + v] = (float)y[v];
+        if (thr) thr[(long long)B * (K + 1) + r] = t;
+        if (pmargin) pmargin[(long long)B * (K + 1) + r] = mg;
+    }
+    int rc = spec_oracle_verify(ORACLE_FP32, ft, fd, tokens, seeds, NULL, B, K, V, T, 0, accept_len, out_tokens,
+                                diag, accept_margin, cdf_margin, 0);
+    free(fd);
+    free(ft);
+    free(y);
+    free(scratch);
+    free(x);
+    return rc;
+}
+
 /* HedgeSpec counterfactual evaluation ([Hedge] Key design 1): for every drafter i, sequence b and
  * level j < K, gamma[i,b,j] = sum_x min(p_target(x), q_i(x)), the acceptance probability of
  * drafter i at that level ([SpS] §6.3: P(accept) = sum_x min(p, q) = 1 - TV). tv[i,b,j] =

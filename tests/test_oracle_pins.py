@@ -722,3 +722,63 @@ def test_normalhedge_regret_update_and_learning():
         assert np.allclose(Rs, Rn, atol=1e-9) and np.allclose(ps, pn, atol=1e-9)
         R, p = Rn, pn
     assert np.argmax(p) == 3 and p[3] > 0.5
+
+
+# ----------------------------------------------------------------------------------------------
+# standardised sampling: top-k / top-p folded into both rows
+# ----------------------------------------------------------------------------------------------
+def test_filter_row_top_k_and_top_p_sets():
+    """The kept set, checked by its defining properties: it is an upper set of values; top-k keeps at least
+    k and fewer than k strictly above its threshold; top-p's kept mass (renormalised over the top-k set)
+    reaches top_p, and dropping its smallest value would fall below top_p."""
+    rng = np.random.default_rng(110)
+    for _ in range(300):
+        V = int(rng.integers(2, 80))
+        x = np.round(rng.normal(0, 2, V) * rng.choice([1, 4]), 0) / 2    # coarse: ties are common
+        T = float(rng.choice([0.5, 1.0, 2.0]))
+        k = int(rng.choice([0, 1, 3, V // 2, V - 1, V]))
+        tp = float(rng.choice([1.0, 0.9, 0.5, 0.1, 1e-9]))
+        y, thr, _ = oracle.filter_row(x, T, k, tp)
+        kept = np.isfinite(y)
+        assert np.array_equal(y[kept], x[kept])
+        assert kept.any()
+        if kept.sum() < V:
+            assert x[kept].min() > x[~kept].max()                      # an upper set
+        xk = x.copy()
+        if 0 < k < V:
+            tk = np.sort(x)[::-1][k - 1]
+            assert (x >= tk).sum() >= k and (x > tk).sum() < k
+            xk = np.where(x >= tk, x, -np.inf)
+        if 0 < tp < 1:
+            p = special.softmax(xk / T)
+            vals = np.unique(x[kept])
+            assert p[kept].sum() >= tp - 1e-12
+            if len(vals) > 1:
+                assert p[kept & (x > vals[0])].sum() < tp + 1e-12   # minimal: the smallest kept value is needed
+        if k in (0, V) and tp == 1.0:
+            assert kept.all() and thr == -np.inf
+
+
+def test_verify_filtered_reductions_and_law():
+    """No filter is the plain chain; top_k = 1 is greedy (both rows one-hot); the chain on standardised rows
+    is lossless for the standardised target (exact law by enumeration)."""
+    rng = np.random.default_rng(111)
+    B, K, V = 12, 4, 50
+    tgt = rng.normal(0, 2, (B, K + 1, V)).astype(np.float32)
+    drf = (tgt[:, :K] + rng.normal(0, 1, (B, K, V))).astype(np.float32)
+    tok = np.stack([[rng.choice(V, p=special.softmax(drf[b, j])) for j in range(K)] for b in range(B)]).astype(np.int32)
+    seeds = np.arange(B, dtype=np.uint64) + 3
+    a = oracle.verify(tgt, drf, tok, seeds, 0.8)
+    f = oracle.verify_filtered(tgt, drf, tok, seeds, 0.8, 0, 1.0)
+    for key in ("accept_len", "out_tokens", "diag"):
+        assert np.array_equal(a[key], f[key]), key
+    g = oracle.greedy(tgt, drf.argmax(axis=2).astype(np.int32))
+    f1 = oracle.verify_filtered(tgt, drf, drf.argmax(axis=2).astype(np.int32), seeds, 0.8, 1, 1.0)
+    assert np.array_equal(g["accept_len"], f1["accept_len"]) and np.array_equal(g["out_tokens"], f1["out_tokens"])
+    # the law of one step on standardised rows is the standardised target
+    x_t = rng.normal(0, 1.5, 6)
+    x_d = x_t + rng.normal(0, 1, 6)
+    pt = special.softmax(oracle.filter_row(x_t, 1.0, 4, 0.8)[0])
+    pd = special.softmax(oracle.filter_row(x_d, 1.0, 4, 0.8)[0])
+    law = output_law(pt, pd)
+    assert law == pytest.approx(pt, abs=2e-6)
