@@ -163,6 +163,26 @@ spec_status spec_accept_length_estimate(const float* gamma, int N, int B, int K,
  * order their feedback arrives. 1 <= N <= 64. One warp; asynchronous on `stream`; allocates nothing. */
 spec_status spec_normalhedge_update(float* regret, const float* loss, float* weights, int N, void* stream);
 
+/* Bytes of workspace spec_verify_filtered needs: the spec_verify workspace, one float per row and a filtered
+ * copy of every target and draft row (the same size as the logits). 0 for invalid sizes or dtype. */
+size_t spec_filter_workspace_size(int B, int K, int V, spec_dtype dtype);
+
+/* spec_verify with standardised sampling ("Speculative Decoding 为什么是 Lossless 的", §8 Q4: temperature,
+ * top-k and top-p are folded into p and q, the same transforms on the target and the draft row, before the
+ * ratio). Each target and draft row keeps the logits at or above its threshold: top_k (0 or >= V: none)
+ * keeps the values at or above the k-th largest, then top_p (1: none) keeps, of those, the values at or
+ * above the one at which the renormalised mass summed from the largest logit down first reaches top_p. The
+ * other logits become -inf, and the chain is spec_verify's on the filtered rows. Readings (the pages give
+ * neither rule): ties at a threshold are all kept, top-k comes before top-p. Same arguments, outputs and
+ * errors as spec_verify, plus top_k >= 0 and top_p in (0, 1]; the workspace must hold
+ * spec_filter_workspace_size(B, K, V, dtype) bytes (its first 16 bytes zeroed once, as for spec_verify). The
+ * thresholds come from radix selection with fp32 mass sums: a top-p decision within about 1e-6 of the mass
+ * boundary may differ from an exact-arithmetic one. */
+spec_status spec_verify_filtered(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                                 const int32_t* draft_tokens, const uint64_t* seeds, int B, int K, int V,
+                                 float temperature, int top_k, float top_p, int32_t* accept_len, int32_t* out_tokens,
+                                 float* diag, void* workspace, size_t workspace_bytes, void* stream);
+
 /* spec_verify for callers that cannot allocate device memory: same inputs, outputs and semantics, but no
  * workspace argument. Some callers run where allocation is not allowed or not possible: inside a memory
  * budget fixed in advance, under an allocator that must not grow, or from code that has no allocator at all.

@@ -549,8 +549,9 @@ int spec_oracle_normalhedge(double* R, const double* loss, double* p, int N)
  * from the largest logit down, first reaches top_p. Readings (the pages give neither rule): ties at either
  * threshold are all kept (the kept set depends on values only), top-k comes before top-p, and the kept
  * logits keep their values while the others become -inf. Writes the filtered row to out and returns the
- * threshold (-inf when nothing is filtered); *margin = the smallest distance of a top-p partial sum from
- * top_p (in the renormalised mass; +inf without top-p), the near-tie measure of the top-p decision. */
+ * threshold (-inf when nothing is filtered); *margin = the distance from top_p of the partial sums just
+ * before and after the block of values that crosses it (in the renormalised mass; +inf without top-p),
+ * the near-tie measure of the top-p decision. */
 static int cmp_desc(const void* a, const void* b)
 {
     double x = *(const double*)a, y = *(const double*)b;
@@ -579,12 +580,11 @@ double spec_oracle_filter_row(const double* x, int V, double T, int top_k, doubl
             double before = run / total;
             run += block;
             double after = run / total;
-            if (margin) {
-                double d1 = fabs(before - top_p), d2 = fabs(after - top_p);
-                if (d1 < *margin) *margin = d1;
-                if (d2 < *margin) *margin = d2;
+            if (after >= top_p) {   /* the crossing block: its distances from top_p are the decision's margin */
+                if (margin) *margin = fmin(fabs(before - top_p), fabs(after - top_p));
+                thr = v > thr ? v : thr;
+                break;
             }
-            if (after >= top_p) { thr = v > thr ? v : thr; break; }
             i = j;
         }
     }

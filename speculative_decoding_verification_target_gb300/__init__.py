@@ -21,7 +21,7 @@ SPEC_OK, SPEC_ERR_INVALID, SPEC_ERR_CUDA, SPEC_ERR_UNSUPPORTED = 0, 1, 2, 3
 STATUS_BAD_TOKEN, STATUS_TIMEOUT = 1, 2
 EXPORTS = ("spec_workspace_size", "spec_verify", "spec_counterfactual_gamma", "spec_cactus_verify", "spec_cactus_kl_verify",
            "spec_greedy_verify", "spec_accept_length_estimate",
-           "spec_normalhedge_update",
+           "spec_normalhedge_update", "spec_filter_workspace_size", "spec_verify_filtered",
            "spec_read_status", "spec_clear_status", "spec_last_error",
            "spec_debug_last_plan", "spec_verify_static", "spec_debug_set_stats_grid")
 
@@ -66,6 +66,10 @@ def load(build_if_missing: bool = False):
     lib.spec_accept_length_estimate.restype = I
     lib.spec_normalhedge_update.argtypes = [P, P, P, I, P]
     lib.spec_normalhedge_update.restype = I
+    lib.spec_filter_workspace_size.argtypes = [I, I, I, I]
+    lib.spec_filter_workspace_size.restype = Z
+    lib.spec_verify_filtered.argtypes = [P, P, I, P, P, I, I, I, F, I, F, P, P, P, P, Z, P]
+    lib.spec_verify_filtered.restype = I
     lib.spec_read_status.argtypes = [P, P, P]
     lib.spec_read_status.restype = I
     lib.spec_clear_status.argtypes = [P, P]
@@ -229,6 +233,27 @@ def normalhedge_update(regret, loss, weights, stream=None):
     for t, nm in ((regret, "regret"), (loss, "loss"), (weights, "weights")):
         _need(t, nm, torch.float32, (N,))
     _check(load().spec_normalhedge_update(_p(regret), _p(loss), _p(weights), N, _stream(stream)))
+
+
+def verify_filtered(target, draft, tokens, seeds, temperature=1.0, top_k=0, top_p=1.0, *, accept_len=None,
+                    out_tokens=None, diag=None, want_diag=True, workspace=None, stream=None):
+    """Standard speculative sampling on standardised rows: top-k then top-p folded into the target and the
+    draft row alike (ties at a threshold kept). Same layout and outputs as verify."""
+    B, K1, V = target.shape
+    K = K1 - 1
+    _need(target, "target")
+    _need(draft, "draft", target.dtype, (B, K, V))
+    _need(tokens, "tokens", torch.int32, (B, K))
+    _need(seeds, "seeds", None, (B,))
+    accept_len, out_tokens, diag = _outputs(B, K, target.device, accept_len, out_tokens, diag, want_diag)
+    lib = load()
+    if workspace is None:
+        n = lib.spec_filter_workspace_size(B, K, V, _dtype_code(target))
+        workspace = torch.zeros(n, dtype=torch.uint8, device=target.device)
+    _check(lib.spec_verify_filtered(_p(target), _p(draft), _dtype_code(target), _p(tokens), _p(seeds), B, K, V,
+                                    float(temperature), int(top_k), float(top_p), _p(accept_len), _p(out_tokens),
+                                    _p(diag), _p(workspace), workspace.numel(), _stream(stream)))
+    return dict(accept_len=accept_len, out_tokens=out_tokens, diag=diag, workspace=workspace)
 
 
 def counterfactual_gamma(target, drafters, temperature=1.0, selected=-1, tokens=None, seeds=None, *, gamma=None,

@@ -8,6 +8,7 @@
 #include <mutex>
 
 #include "specverify.h"
+#include "specverify_filter.cuh"
 #include "specverify_gamma.cuh"
 
 namespace specv {
@@ -49,6 +50,22 @@ WsLayout ws_layout(int B, int K, int V, int N) {
     w.total = w.part_off + static_cast<size_t>(std::min(pieces, gmax) + srows) * sizeof(float2);
     w.total = (w.total + 15) / 16 * 16;
     return w;
+}
+
+// Workspace of spec_verify_filtered: [the verify workspace][row thresholds][filtered target rows][filtered
+// draft rows], each region 256-byte aligned.
+struct FilterLayout {
+    size_t thr_off, ta_off, tb_off, total;
+};
+FilterLayout filter_layout(int B, int K, int V, int eb) {
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    FilterLayout f;
+    const size_t rows = static_cast<size_t>(B) * (2 * K + 1);
+    f.thr_off = up(ws_layout(B, K, V, 1).total);
+    f.ta_off = up(f.thr_off + rows * sizeof(float));
+    f.tb_off = up(f.ta_off + static_cast<size_t>(B) * (K + 1) * V * eb);
+    f.total = up(f.tb_off + static_cast<size_t>(B) * K * V * eb);
+    return f;
 }
 
 struct Call {
@@ -384,6 +401,40 @@ spec_status run_gamma(const Call& a, bool aligned) {
     return launch_draw(a, aligned, draft, nullptr, g.row_ms, 0, 0, g.status);
 }
 
+// Standardised sampling: the per-row thresholds, the filtered copies in the workspace, then the chain on them.
+spec_status run_filtered(const Call& a, int top_k, float top_p) {
+    const int eb = a.dtype == SPEC_BF16 ? 2 : 4;
+    const FilterLayout fl = filter_layout(a.B, a.K, a.V, eb);
+    unsigned char* ws = static_cast<unsigned char*>(a.workspace);
+    FParams f = {};
+    f.rows_a = static_cast<const unsigned char*>(a.target);
+    f.rows_b = static_cast<const unsigned char*>(a.others);
+    f.rows_a_n = static_cast<long long>(a.B) * (a.K + 1);
+    f.rows_n = f.rows_a_n + static_cast<long long>(a.B) * a.K;
+    f.V = a.V;
+    f.c = static_cast<float>(1.4426950408889634 / static_cast<double>(a.temperature));
+    f.top_k = top_k;
+    f.top_p = top_p;
+    f.thr = reinterpret_cast<float*>(ws + fl.thr_off);
+    f.out_a = ws + fl.ta_off;
+    f.out_b = ws + fl.tb_off;
+    if (a.dtype == SPEC_BF16) threshold_kernel<Bf16><<<static_cast<unsigned>(f.rows_n), FT_NT, 0, a.stream>>>(f);
+    else threshold_kernel<F32><<<static_cast<unsigned>(f.rows_n), FT_NT, 0, a.stream>>>(f);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "threshold kernel launch failed: %s", cudaGetErrorString(e));
+    const long long elems = f.rows_n * static_cast<long long>(a.V);
+    const unsigned mblocks = static_cast<unsigned>(std::min<long long>((elems + 255) / 256, 152LL * 64));
+    if (a.dtype == SPEC_BF16) mask_kernel<Bf16><<<mblocks, 256, 0, a.stream>>>(f);
+    else mask_kernel<F32><<<mblocks, 256, 0, a.stream>>>(f);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "mask kernel launch failed: %s", cudaGetErrorString(e));
+    Call c = a;
+    c.target = f.out_a;
+    c.others = f.out_b;
+    const bool aligned = (static_cast<size_t>(a.V) * eb) % 16 == 0 && a.V % CHUNK == 0;
+    return run_chain(c, aligned);
+}
+
 spec_status run(const Call& a) {
     if (a.B == 0) return SPEC_OK;
     const int eb = a.dtype == SPEC_BF16 ? 2 : 4;
@@ -612,6 +663,46 @@ spec_status spec_normalhedge_update(float* regret, const float* loss, float* wei
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "NormalHedge kernel launch failed: %s", cudaGetErrorString(e));
     return SPEC_OK;
+}
+
+size_t spec_filter_workspace_size(int B, int K, int V, spec_dtype dtype) {
+    if (B < 0 || K < 0 || V < 1 || (dtype != SPEC_BF16 && dtype != SPEC_FP32)) return 0;
+    return filter_layout(B, K, V, dtype == SPEC_BF16 ? 2 : 4).total;
+}
+
+spec_status spec_verify_filtered(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                                 const int32_t* draft_tokens, const uint64_t* seeds, int B, int K, int V,
+                                 float temperature, int top_k, float top_p, int32_t* accept_len, int32_t* out_tokens,
+                                 float* diag, void* workspace, size_t workspace_bytes, void* stream) {
+    spec_status s = check_common(target_logits, draft_logits, dtype, B, K, V, 1, temperature, workspace, workspace_bytes);
+    if (s != SPEC_OK || B == 0) return s;
+    if (top_k < 0) return fail(SPEC_ERR_INVALID, "top_k must be >= 0 (got %d)", top_k);
+    if (std::isnan(top_p) || !(top_p > 0.f) || top_p > 1.f)
+        return fail(SPEC_ERR_INVALID, "top_p must be in (0, 1] (got %g)", static_cast<double>(top_p));
+    if (!draft_tokens || !seeds || !accept_len || !out_tokens)
+        return fail(SPEC_ERR_INVALID, "draft_tokens, seeds, accept_len and out_tokens must not be NULL");
+    const size_t need = spec_filter_workspace_size(B, K, V, dtype);
+    if (workspace_bytes < need)
+        return fail(SPEC_ERR_INVALID, "workspace too small for the filtered rows: %zu bytes, need %zu", workspace_bytes, need);
+    Call a = {};
+    a.target = target_logits;
+    a.others = draft_logits;
+    a.dtype = dtype;
+    a.tokens = draft_tokens;
+    a.seeds = seeds;
+    a.B = B;
+    a.K = K;
+    a.V = V;
+    a.N = 1;
+    a.selected = 0;
+    a.temperature = temperature;
+    a.accept_len = accept_len;
+    a.out_tokens = out_tokens;
+    a.diag = diag;
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+    a.stream = static_cast<cudaStream_t>(stream);
+    return run_filtered(a, top_k, top_p);
 }
 
 spec_status spec_verify_static(const void* target_logits, const void* draft_logits, spec_dtype dtype,

@@ -637,3 +637,36 @@ def test_normalhedge_round(N):
     assert np.abs(pg.cpu().numpy() - p).max() <= 1e-3
     if N > 1:
         assert int(pg.argmax()) == N // 2
+
+
+# ------------------------------------------------------------------------------------------------
+# standardised sampling: top-k / top-p on both rows
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("V,dtype,top_k,top_p", [
+    (3000, "bf16", 50, 1.0), (3000, "bf16", 0, 0.9), (3000, "bf16", 200, 0.8), (20001, "bf16", 7, 0.95),
+    (1000, "fp32", 40, 0.9), (1000, "fp32", 0, 0.5), (128256, "bf16", 1000, 0.9), (151936, "bf16", 0, 0.99),
+])
+def test_verify_filtered_small(V, dtype, top_k, top_p):
+    w = small(V, B=8, K=4, dtype=dtype, T=0.9, sigma=1.0)
+    inp = workloads.make(w)
+    ref = oracle.verify_filtered(host(inp["target"]), host(inp["draft"]), inp["tokens"].numpy(),
+                                 inp["seeds"].numpy().astype(np.uint64), w.temperature, top_k, top_p)
+    g = to_device(inp)
+    out = sv.verify_filtered(g["target"], g["draft"], g["tokens"], g["seeds"], w.temperature, top_k, top_p)
+    torch.cuda.synchronize()
+    # A top-p threshold can land one value off the oracle's when the mass boundary falls within fp32
+    # resolution of a partial sum; that moves p(t), Z and the CDF by about one element's mass, which the
+    # bar's tolerance and near-tie rules cover.
+    assert_diag(out, ref)
+    assert_chain(out, ref, w.K)
+    assert sv.read_status(out["workspace"]) == 0
+
+
+def test_verify_filtered_without_filters_is_verify():
+    w = small(50000, B=6, K=4)
+    g = to_device(workloads.make(w))
+    a = sv.verify(g["target"], g["draft"], g["tokens"], g["seeds"], w.temperature)
+    f = sv.verify_filtered(g["target"], g["draft"], g["tokens"], g["seeds"], w.temperature, 0, 1.0)
+    torch.cuda.synchronize()
+    for k in ("accept_len", "out_tokens", "diag"):
+        assert torch.equal(a[k], f[k])
