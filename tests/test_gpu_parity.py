@@ -504,11 +504,16 @@ def test_full_batch_near_ties(name, delta):
     if delta is None:
         ref = oracle.verify(host(inp["target"]), host(draft), tok, seeds, w.temperature)
         out = sv.verify(inp["target"], draft, inp["tokens"], inp["seeds"], w.temperature)
+        lean = sv.verify(inp["target"], draft, inp["tokens"], inp["seeds"], w.temperature, want_diag=False)
     else:
         ref = oracle.cactus(host(inp["target"]), host(draft), tok, seeds, delta, w.temperature)
         out = sv.cactus_verify(inp["target"], draft, inp["tokens"], inp["seeds"], delta, w.temperature)
+        lean = sv.cactus_verify(inp["target"], draft, inp["tokens"], inp["seeds"], delta, w.temperature,
+                                want_diag=False)
     torch.cuda.synchronize()
     assert_chain(out, ref, w.K)
+    # the launch the benchmark times (no diag: one draw pass over the row pair of each sequence's draw)
+    assert_chain(lean, ref, w.K)
     if w.N > 1:
         fused = sv.counterfactual_gamma(inp["target"], inp["drafters"], w.temperature, w.selected, inp["tokens"],
                                         inp["seeds"], want_diag=False)
