@@ -147,7 +147,7 @@ def max_over_ranks(pg, torch, v, device):
 # of this benchmark's own command (profiles/), keyed by a hash of the kernel sources it was taken with: when
 # the sources change the recorded number no longer applies and the JSON line reports null.
 RECORDED_TRAFFIC = {
-    "b0411a502ab13c60": {"sps_llama3_b64_k5": 214573824, "hedgespec_n7_b32_k5": 373081600 + 3232768 + 16285440},
+    "d5abaa3cee4fa96e": {"sps_llama3_b64_k5": 214817664, "hedgespec_n7_b32_k5": 373320960 + 3263744 + 16286720},
 }
 
 
