@@ -694,8 +694,10 @@ __global__ void __launch_bounds__(256) greedy_chain_kernel(const __grid_constant
     const int lane = threadIdx.x & 31;
     const int b = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int K = p.K;
-    // draft tokens are inputs: read before waiting for the statistics grid
-    const int tokv = (b < p.B && lane < K) ? __ldg(p.tokens + static_cast<size_t>(b) * K + lane) : 0;
+    // draft tokens are inputs, read before waiting for the statistics grid: position lane in tokv0,
+    // position lane + 32 in tokv1 (K <= 64)
+    const int tokv0 = (b < p.B && lane < K) ? __ldg(p.tokens + static_cast<size_t>(b) * K + lane) : 0;
+    const int tokv1 = (b < p.B && lane + 32 < K) ? __ldg(p.tokens + static_cast<size_t>(b) * K + lane + 32) : 0;
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (b >= p.B) return;
     const Split sp(p.P, p.G);
@@ -716,7 +718,7 @@ __global__ void __launch_bounds__(256) greedy_chain_kernel(const __grid_constant
         }
         warp_argmax(m, idx);
         const int am = idx >= 0 ? idx : 0;   // a row with every logit -inf: index 0
-        int t = __shfl_sync(0xffffffffu, tokv, j < K ? j : 0);
+        int t = __shfl_sync(0xffffffffu, j < 32 ? tokv0 : tokv1, j & 31);
         if (j < K && (t < 0 || t >= p.V)) {
             if (lane == 0) atomicOr(p.status, STATUS_BAD_TOKEN);
             t = -1;
