@@ -128,3 +128,17 @@ def test_accept_length_at_max_N_and_K():
     e_ref, l_ref = oracle.accept_length(gam.numpy().astype(np.float64))
     assert np.abs(est["est"].cpu().numpy() - e_ref).max() <= 1e-4
     assert np.abs(est["loss"].cpu().numpy() - l_ref).max() <= 1e-4
+
+
+def test_filtered_at_max_K_and_V():
+    """Top-k then top-p on both rows of every position, K = 64 over V = 262144."""
+    w = small(V_MAX, B=2, K=K_MAX, sigma=0.5, T=0.9)
+    inp = workloads.make(w)
+    ref = oracle.verify_filtered(host(inp["target"]), host(inp["draft"]), inp["tokens"].numpy(),
+                                 inp["seeds"].numpy().astype(np.uint64), w.temperature, 5000, 0.9)
+    g = to_device(inp)
+    out = sv.verify_filtered(g["target"], g["draft"], g["tokens"], g["seeds"], w.temperature, 5000, 0.9)
+    torch.cuda.synchronize()
+    assert_diag(out, ref)
+    assert_chain(out, ref, w.K)
+    assert sv.read_status(out["workspace"]) == 0
