@@ -330,13 +330,55 @@ def run_ours(args, w):
         e2e_step()
     e1.record(stream)
     barrier(pg, torch)
+    e2e_serial_ms = max_over_ranks(pg, torch, e0.elapsed_time(e1), dev)
+
+    # The same steps pipelined: step i + 1's inputs are copied into a second device buffer on a copy stream
+    # while step i computes (every step still copies its own inputs in and its results out).
+    dev_in2 = [dev_in, {k: torch.empty_like(hb[k]) for k in host_in}]
+    cstream = torch.cuda.Stream(dev)
+    copied = [torch.cuda.Event(), torch.cuda.Event()]
+    consumed = [torch.cuda.Event(), torch.cuda.Event()]
+
+    def copy_in(j):
+        with torch.cuda.stream(cstream):
+            if j >= 2:
+                cstream.wait_event(consumed[j % 2])
+            for k in host_in:
+                dev_in2[j % 2][k].copy_(host_in[k], non_blocking=True)
+            copied[j % 2].record(cstream)
+
+    def e2e_pipelined(n):
+        cstream.wait_stream(stream)
+        copy_in(0)
+        for i in range(n):
+            if i + 1 < n:
+                copy_in(i + 1)
+            stream.wait_event(copied[i % 2])
+            call(dev_in2[i % 2], stream)
+            consumed[i % 2].record(stream)
+            host_out["accept_len"].copy_(acc, non_blocking=True)
+            host_out["out_tokens"].copy_(outt, non_blocking=True)
+            if gam is not None:
+                host_out["gamma"].copy_(gam, non_blocking=True)
+
+    e2e_pipelined(2)
+    torch.cuda.synchronize(dev)
+    barrier(pg, torch)
+    e0.record(stream)
+    e2e_pipelined(e2e_steps)
+    e1.record(stream)
+    barrier(pg, torch)
     e2e_ms = max_over_ranks(pg, torch, e0.elapsed_time(e1), dev)
 
     if rank != 0:
         return 0
     positions = w.positions * world
     value = positions * args.steps / (elapsed_ms / 1e3)
-    e2e_value = positions * e2e_steps / (e2e_ms / 1e3)
+    # e2e reports the faster of the two ways to run the steps: pipelined for calls whose copy dominates,
+    # serial for latency-bound ones (the stream and event bookkeeping costs more than it hides there)
+    pipelined = e2e_ms <= e2e_serial_ms
+    e2e_best_ms = e2e_ms if pipelined else e2e_serial_ms
+    e2e_value = positions * e2e_steps / (e2e_best_ms / 1e3)
     peak, peak_kind = peaks()
     avg_call_s = elapsed_ms / args.steps / 1e3
     achieved = batch_bytes / avg_call_s / 1e9
@@ -360,7 +402,11 @@ def run_ours(args, w):
                      "avg_call_us": avg_call_s * 1e6, "eager_call_us": eager_ms * 1e3,
                      "frac_of_8tbs_nominal": achieved / 8000.0},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms / e2e_steps},
+                "ms_per_step": e2e_best_ms / e2e_steps,
+                "mode": "pipelined: step i + 1's host-to-device copy overlaps step i's call (two device buffers)"
+                        if pipelined else "serial: copy in, call, copy out, one step after another",
+                "pipelined_value": positions * e2e_steps / (e2e_ms / 1e3),
+                "serial_value": positions * e2e_steps / (e2e_serial_ms / 1e3)},
         "gpu_launches": launches_per_call * args.steps,
         "clocks": clocks.summary(),
         "device_status": status,
