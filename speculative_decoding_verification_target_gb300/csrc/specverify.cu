@@ -175,8 +175,9 @@ spec_status launch_draw(const Call& a, bool aligned, const unsigned char* draft,
     d.status = status;
     // CTAs per sequence: the largest power of two up to D_MAX_CPS that keeps the grid within one CTA per SM
     int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "device query failed: %s", cudaGetErrorString(e));
     int cps = 1;
     while (cps < D_MAX_CPS && static_cast<long long>(a.B) * cps * 2 <= sms) cps *= 2;
     d.cps = cps;
@@ -189,7 +190,7 @@ spec_status launch_draw(const Call& a, bool aligned, const unsigned char* draft,
     using DrawFn = void (*)(const DParams);
     DrawFn dfn = a.dtype == SPEC_BF16 ? (aligned ? draw_kernel<Bf16, true> : draw_kernel<Bf16, false>)
                                       : (aligned ? draw_kernel<F32, true> : draw_kernel<F32, false>);
-    cudaError_t e = draw_smem_ceiling(dfn, dev);
+    e = draw_smem_ceiling(dfn, dev);
     if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "draw kernel attribute failed: %s", cudaGetErrorString(e));
     // its CTAs start as the grid before it frees SMs and wait for it (griddepcontrol.wait) after reading
     // their inputs
@@ -422,8 +423,13 @@ spec_status run_filtered(const Call& a, int top_k, float top_p) {
     else threshold_kernel<F32><<<static_cast<unsigned>(f.rows_n), FT_NT, 0, a.stream>>>(f);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "threshold kernel launch failed: %s", cudaGetErrorString(e));
+    // grid-stride copy: up to 64 CTAs of 256 threads per SM
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "device query failed: %s", cudaGetErrorString(e));
     const long long elems = f.rows_n * static_cast<long long>(a.V);
-    const unsigned mblocks = static_cast<unsigned>(std::min<long long>((elems + 255) / 256, 152LL * 64));
+    const unsigned mblocks = static_cast<unsigned>(std::min<long long>((elems + 255) / 256, 64LL * sms));
     if (a.dtype == SPEC_BF16) mask_kernel<Bf16><<<mblocks, 256, 0, a.stream>>>(f);
     else mask_kernel<F32><<<mblocks, 256, 0, a.stream>>>(f);
     e = cudaGetLastError();
