@@ -7,19 +7,21 @@
 // the second visit on chip:
 //   - a CTA owns a contiguous run of "units" in the order T(b, j), D_0(b, j), ..., D_{N-1}(b, j) for every
 //     position, then the bonus target rows T(b, K) when a chain is verified as well. A T unit computes the
-//     target row's normaliser; a D unit computes the drafter row's normaliser and then its gamma. A CTA
-//     whose run starts inside a position first computes that position's T unit itself;
+//     target row's normaliser; a D unit computes the drafter row's normaliser and then its gamma. The runs
+//     hold equal numbers of units. A CTA whose run starts inside a position first computes that position's
+//     T unit itself;
 //   - a whole row is split over the CTA's 16 warps (warp w takes pieces w, w + 16, ...), so the normaliser
-//     of a row is complete once every warp has passed one CTA barrier: no exchange between CTAs;
+//     of a row is complete once every warp has published its pair: no exchange between CTAs;
 //   - pass 1 streams the pieces of unit s from HBM through a private ring of bulk-copy slots per warp.
-//     Each warp parks the raw logits of its first four drafter pieces in tensor memory (its 32 lanes x
-//     128 columns of the CTA's 512-column allocation: 16 KB, so a row of up to 64 x 4 KB is held whole);
-//   - pass 2 of unit s - 1 runs in the same step, piece by piece ahead of pass 1 of unit s: it reads the
-//     parked drafter piece back from tensor memory (the columns are then free for unit s), reads the target
-//     piece from L2 (the CTA keeps one target row hot while it walks that position's drafters) and adds
-//     sum 2^min(log2 p_target, log2 q_i). Pieces past the tensor-memory share are re-read from L2.
-// One CTA barrier per step merges the 16 warps' (max, sum) pairs of unit s and their gamma partials of
-// unit s - 1, each in a fixed order, so the result does not depend on timing.
+//     Each warp parks the raw logits of its first two drafter pieces in tensor memory, in one of two halves
+//     of its 32 lanes x 128 columns (unit s uses half s mod 2);
+//   - pass 2 of unit s - 1 runs in the same step, after pass 1 of unit s: it reads the parked drafter
+//     pieces back from tensor memory, reads the target piece from L2 (the CTA keeps one target row hot
+//     while it walks that position's drafters) and adds sum 2^min(log2 p_target, log2 q_i). Pieces past the
+//     tensor-memory share are re-read from L2.
+// The warps publish their (max, sum) of a unit and their gamma partials of a unit with mbarrier arrivals,
+// and wait for the other warps' a whole pass later; each merge runs in warp order, so the result does not
+// depend on timing.
 #pragma once
 #include "specverify_chain.cuh"
 
