@@ -20,10 +20,10 @@
 // g or r (or both) grows at every step, so the entries are distinct, and there are at most
 // min(G, pieces) + rows - 1 of them. There is no barrier and no exchange between warps.
 //
-// draw_kernel: one CTA per sequence. Its warps merge the segments of the sequence's 2K + 1 rows (in
-// ascending warp order), evaluate p(t) and q(t) at the draft tokens, run the chain (with the Cactus h when
-// asked), then compute the residual (or bonus) mass of every piece of row L in parallel, prefix-sum those
-// masses, and find the drawn token with one scan of the chosen piece. The per-element arithmetic is the
+// draw_kernel: one cluster of CTAs per sequence. Its warps merge the segments of the sequence's 2K + 1 rows
+// (in ascending warp order), evaluate p(t) and q(t) at the draft tokens, run the chain (with the Cactus h
+// when asked), then compute the residual (or bonus) mass of every piece of row L in parallel across the
+// cluster, prefix-sum those masses in CTA 0, and find the drawn token with one scan of the chosen piece. The per-element arithmetic is the
 // one of the inverse-CDF scan (chunk_mass / chunk_values / scan_pick), so every probability of the draw is
 // computed the same way wherever it is needed.
 #pragma once
