@@ -124,3 +124,29 @@ def test_static_scratch_entry_refuses_oversized_calls_without_a_gpu(lib):
     rc = lib.spec_verify_static(good, good, 0, good, good, 2, 0, 1000, ctypes.c_float(1.0), good, good, None, None,
                                 None)
     assert rc == 1
+
+
+def test_no_cpu_fallback(lib, tmp_path):
+    """The product path has no CPU route: host tensors are refused before any call, and a missing library
+    makes loading fail loudly instead of computing anything elsewhere."""
+    import torch
+    import speculative_decoding_verification_target_gb300 as sv
+    B, K, V = 2, 3, 64
+    t = torch.zeros((B, K + 1, V), dtype=torch.float32)
+    d = torch.zeros((B, K, V), dtype=torch.float32)
+    tok = torch.zeros((B, K), dtype=torch.int32)
+    seeds = torch.zeros(B, dtype=torch.int64)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        sv.verify(t, d, tok, seeds)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        sv.cactus_verify(t, d, tok, seeds, 0.5)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        sv.greedy_verify(t, tok)
+    saved_path, saved_lib = sv._build.LIB, sv._lib
+    try:
+        sv._build.LIB = str(tmp_path / "missing" / "libspecverify.so")
+        sv._lib = None
+        with pytest.raises(ImportError, match="no CPU fallback"):
+            sv.load()
+    finally:
+        sv._build.LIB, sv._lib = saved_path, saved_lib
