@@ -74,6 +74,8 @@ def _load():
     lib.spec_oracle_normalhedge.restype = i32
     lib.spec_oracle_normalhedge_scale.argtypes = [P, i32]
     lib.spec_oracle_normalhedge_scale.restype = f64
+    lib.spec_oracle_hedge_feedback.argtypes = [P, P, i32, i32, i32, i32, i32, P, P]
+    lib.spec_oracle_hedge_feedback.restype = i32
     lib.spec_oracle_filter_row.argtypes = [P, i32, f64, i32, f64, P, P, P]
     lib.spec_oracle_filter_row.restype = f64
     lib.spec_oracle_verify_filtered.argtypes = [i32, P, P, P, P, i32, i32, i32, f64, i32, f64, P, P, P, P, P, P, P]
@@ -173,6 +175,12 @@ def cactus_gamma_kl(q: float, delta: float) -> float:
     return _load().spec_oracle_cactus_gamma_kl(q, delta)
 
 
+def _t32(temperature):
+    """A temperature or a divergence budget as the C ABI of the CUDA path receives it (a 32-bit float), so
+    that both sides compute with the same number."""
+    return float(np.float32(temperature))
+
+
 def _seq_index(seq_index, B):
     if seq_index is None:
         return None
@@ -196,7 +204,7 @@ def verify(target, draft, tokens, seeds, temperature=1.0, seq_index=None, mutati
     out = dict(accept_len=np.zeros(B, np.int32), out_tokens=np.zeros((B, K + 1), np.int32),
                diag=np.zeros((B, K, 4)), accept_margin=np.zeros((B, K)), cdf_margin=np.zeros(B))
     rc = lib.spec_oracle_verify(dt, _ptr(target), _ptr(draft), _ptr(tokens), _ptr(seeds), _ptr(si), B, K, V,
-                                float(temperature), mutation, _ptr(out["accept_len"]),
+                                _t32(temperature), mutation, _ptr(out["accept_len"]),
                                 _ptr(out["out_tokens"]), _ptr(out["diag"]), _ptr(out["accept_margin"]),
                                 _ptr(out["cdf_margin"]), nthreads)
     if rc != 0:
@@ -244,6 +252,23 @@ def normalhedge(regret, loss, weights):
     return R, p, lib.spec_oracle_normalhedge_scale(_ptr(R), R.size)
 
 
+def hedge_feedback(gamma, accept_len, objective=0):
+    """NormalHedge under delayed, censored feedback, one learner per sequence (reading of the HedgeSpec notes'
+    Key design 3; see spec_oracle_hedge_feedback). gamma [T, N, B, K] (the counterfactual gamma of T rounds),
+    accept_len [T, B]; objective 0: loss 1 - gamma per revealed level, 1: the accept-length loss over a window
+    of K revealed levels. Returns (weights [T, B, N] after each round, applied [T, B])."""
+    lib = _load()
+    g = np.ascontiguousarray(gamma, dtype=np.float64)
+    T, N, B, K = g.shape
+    L = np.ascontiguousarray(accept_len, dtype=np.int32)
+    assert L.shape == (T, B)
+    w = np.zeros((T, B, N))
+    a = np.zeros((T, B), np.int32)
+    if lib.spec_oracle_hedge_feedback(_ptr(g), _ptr(L), T, N, B, K, int(objective), _ptr(w), _ptr(a)) != 0:
+        raise ValueError("hedge_feedback rejected its arguments")
+    return w, a
+
+
 def filter_row(x, temperature=1.0, top_k=0, top_p=1.0):
     """Standardised-sampling filter of one row of logits: top-k then top-p, ties at a threshold kept.
     Returns (filtered logits with -inf outside the kept set, threshold, top-p margin)."""
@@ -252,7 +277,7 @@ def filter_row(x, temperature=1.0, top_k=0, top_p=1.0):
     out = np.empty_like(x)
     sc = np.empty_like(x)
     m = np.zeros(1)
-    thr = lib.spec_oracle_filter_row(_ptr(x), x.size, float(temperature), int(top_k), float(top_p), _ptr(out),
+    thr = lib.spec_oracle_filter_row(_ptr(x), x.size, _t32(temperature), int(top_k), float(top_p), _ptr(out),
                                      _ptr(m), _ptr(sc))
     return out, thr, float(m[0])
 
@@ -274,7 +299,7 @@ def verify_filtered(target, draft, tokens, seeds, temperature=1.0, top_k=0, top_
                diag=np.zeros((B, K, 4)), accept_margin=np.zeros((B, K)), cdf_margin=np.zeros(B),
                thr=np.zeros(R), pmargin=np.zeros(R))
     rc = lib.spec_oracle_verify_filtered(dt, _ptr(target), _ptr(draft), _ptr(tokens), _ptr(seeds), B, K, V,
-                                         float(temperature), int(top_k), float(top_p), _ptr(out["accept_len"]),
+                                         _t32(temperature), int(top_k), float(top_p), _ptr(out["accept_len"]),
                                          _ptr(out["out_tokens"]), _ptr(out["diag"]), _ptr(out["accept_margin"]),
                                          _ptr(out["cdf_margin"]), _ptr(out["thr"]), _ptr(out["pmargin"]))
     if rc != 0:
@@ -299,7 +324,7 @@ def cactus(target, draft, tokens, seeds, delta, temperature=1.0, seq_index=None,
                diag=np.zeros((B, K, 4)), gamma_star=np.zeros((B, K)), accept_margin=np.zeros((B, K)),
                cdf_margin=np.zeros(B))
     rc = lib.spec_oracle_cactus_ex(dt, _ptr(target), _ptr(draft), _ptr(tokens), _ptr(seeds), _ptr(si), B, K, V,
-                                float(temperature), float(delta), 1 if exact else 0, _ptr(out["accept_len"]),
+                                _t32(temperature), _t32(delta), 1 if exact else 0, _ptr(out["accept_len"]),
                                 _ptr(out["out_tokens"]), _ptr(out["diag"]), _ptr(out["gamma_star"]),
                                 _ptr(out["accept_margin"]), _ptr(out["cdf_margin"]), nthreads)
     if rc != 0:
@@ -329,7 +354,7 @@ def counterfactual(target, drafters, temperature=1.0, selected=-1, tokens=None, 
         si = _seq_index(seq_index, B)
         out.update(accept_len=np.zeros(B, np.int32), out_tokens=np.zeros((B, K + 1), np.int32),
                    diag=np.zeros((B, K, 4)), accept_margin=np.zeros((B, K)), cdf_margin=np.zeros(B))
-    rc = lib.spec_oracle_counterfactual(dt, _ptr(target), _ptr(drafters), N, B, K, V, float(temperature),
+    rc = lib.spec_oracle_counterfactual(dt, _ptr(target), _ptr(drafters), N, B, K, V, _t32(temperature),
                                         _ptr(out["gamma"]), _ptr(out["tv"]), selected, _ptr(tok), _ptr(sd),
                                         _ptr(si), _ptr(out.get("accept_len")), _ptr(out.get("out_tokens")),
                                         _ptr(out.get("diag")), _ptr(out.get("accept_margin")),

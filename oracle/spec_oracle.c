@@ -542,6 +542,71 @@ int spec_oracle_normalhedge(double* R, const double* loss, double* p, int N)
     return 0;
 }
 
+/* NormalHedge under delayed, censored feedback ([Hedge] Key design 3). The notes say that the accepted tokens
+ * of a round are revealed as one block when the round ends, that the counterfactual feedback is censored
+ * unless the selected drafter fills the chunk, that the loss is either 1 - gamma (the acceptance
+ * probability) or the accept length still available up to K + 1, that the delay is at most 2K, and that in
+ * practice the learner keeps a queue of feedback and keeps applying the next available one (the stochastic-
+ * setting reduction of Joulani, Gyorgy, Szepesvari, "Online learning under delayed feedback", ICML 2013).
+ * They give no pseudo-code; the reading taken here, one learner per sequence:
+ *  - round t reports gamma_t [N, K] (all drafters, all levels) and the accepted length L_t of the selected
+ *    drafter. Levels j < min(L_t + 1, K) have a fully verified context and are revealed, in level order, as
+ *    the next feedback items of the sequence; the levels after them are censored and never used;
+ *  - objective 0 (acceptance probability): item n's loss is 1 - gamma of item n, available at once;
+ *  - objective 1 (accept length): item n's loss is K + 1 minus the accept-length estimate over the window of
+ *    items n .. n + K - 1 (spec_oracle_accept_length's reading), available once item n + K - 1 has arrived,
+ *    so an item waits for at most the K - 1 items after it and the pending items never exceed 2K - 1;
+ *  - after each round every newly available loss is applied, oldest item first, as one NormalHedge round
+ *    (spec_oracle_normalhedge). Items whose window never completes are never applied.
+ * gamma [T][N][B][K], accept_len [T][B] in [0, K]; outputs after each round: weights [T][B][N] (the
+ * distribution for the next round) and applied [T][B] (NormalHedge rounds so far). Returns 0, or -1 for bad
+ * sizes or an accepted length outside [0, K]. */
+int spec_oracle_hedge_feedback(const double* gamma, const int32_t* accept_len, int T, int N, int B, int K,
+                               int objective, double* weights, int32_t* applied)
+{
+    if (T < 0 || N < 1 || N > 64 || B < 0 || K < 1 || K > 64 || (objective != 0 && objective != 1)) return -1;
+    for (long long i = 0; i < (long long)T * B; i++)
+        if (accept_len[i] < 0 || accept_len[i] > K) return -1;
+    double* items = (double*)malloc(sizeof(double) * ((size_t)T * K + 1) * N);
+    if (!items) return -1;
+    for (int b = 0; b < B; b++) {
+        double R[64], p[64], loss[64];
+        for (int i = 0; i < N; i++) {
+            R[i] = 0.0;
+            p[i] = 1.0 / N;
+        }
+        long long n_items = 0, next = 0, done = 0;
+        for (int t = 0; t < T; t++) {
+            const int L = accept_len[(size_t)t * B + b];
+            const int valid = L + 1 < K ? L + 1 : K;
+            for (int j = 0; j < valid; j++, n_items++)
+                for (int i = 0; i < N; i++)
+                    items[n_items * N + i] = gamma[(((size_t)t * N + i) * B + b) * K + j];
+            while (objective == 0 ? next < n_items : next + K - 1 < n_items) {
+                for (int i = 0; i < N; i++) {
+                    if (objective == 0) {
+                        loss[i] = 1.0 - items[next * N + i];
+                    } else {
+                        double run = 1.0, total = 1.0;
+                        for (int k = 0; k < K; k++) {
+                            run *= items[(next + k) * N + i];
+                            total += run;
+                        }
+                        loss[i] = (double)(K + 1) - total;
+                    }
+                }
+                spec_oracle_normalhedge(R, loss, p, N);
+                next++;
+                done++;
+            }
+            for (int i = 0; i < N; i++) weights[((size_t)t * B + b) * N + i] = p[i];
+            applied[(size_t)t * B + b] = (int32_t)done;
+        }
+    }
+    free(items);
+    return 0;
+}
+
 /* Standardised sampling ([SpS] §8 Q4: temperature, top-k and top-p are folded into p and q before the
  * ratio, the same transforms for the target and the draft row). For one row of logits x at temperature T:
  * top-k (0 < k < V) keeps the logits at or above the k-th largest; then top-p (0 < top_p < 1) keeps, of what

@@ -564,7 +564,9 @@ def test_cactus_exact_root_law(delta):
     for b in range(B):
         for j in range(K):
             q = special.softmax(tgt[b, j].astype(np.float64))[tok[b, j]]
-            assert out["gamma_star"][b, j] == pytest.approx(oracle.cactus_gamma_kl(q, delta), abs=1e-12)
+            # the batched entry takes delta as the C ABI does, a 32-bit float
+            assert out["gamma_star"][b, j] == pytest.approx(oracle.cactus_gamma_kl(q, float(np.float32(delta))),
+                                                            abs=1e-12)
 
 
 # ----------------------------------------------------------------------------------------------
@@ -722,6 +724,108 @@ def test_normalhedge_regret_update_and_learning():
         assert np.allclose(Rs, Rn, atol=1e-9) and np.allclose(ps, pn, atol=1e-9)
         R, p = Rn, pn
     assert np.argmax(p) == 3 and p[3] > 0.5
+
+
+# ----------------------------------------------------------------------------------------------
+# NormalHedge under delayed, censored feedback ([Hedge] Key design 3; reading in spec_oracle_hedge_feedback)
+# ----------------------------------------------------------------------------------------------
+def _hf_rounds(rng, T, N, B, K, lo=0.05, hi=0.95):
+    gamma = rng.uniform(lo, hi, (T, N, B, K))
+    L = rng.integers(0, K + 1, (T, B)).astype(np.int32)
+    return gamma, L
+
+
+def _revealed(gamma, L, b):
+    """The feedback items of sequence b in order: levels j < min(L_t + 1, K) of each round."""
+    T, N, B, K = gamma.shape
+    items = []
+    for t in range(T):
+        for j in range(min(int(L[t, b]) + 1, K)):
+            items.append((t, gamma[t, :, b, j]))
+    return items
+
+
+def test_hedge_feedback_reduces_to_normalhedge():
+    """Objective 0 is plain NormalHedge over 1 - gamma of the revealed levels, in order; with every level
+    revealed (L = K) that is K NormalHedge rounds per round."""
+    rng = np.random.default_rng(120)
+    T, N, B, K = 12, 5, 3, 4
+    gamma, L = _hf_rounds(rng, T, N, B, K)
+    L[:, 0] = K                                            # sequence 0: nothing censored
+    w, applied = oracle.hedge_feedback(gamma, L, objective=0)
+    for b in range(B):
+        R, p = np.zeros(N), np.full(N, 1.0 / N)
+        items = _revealed(gamma, L, b)
+        n = 0
+        for t in range(T):
+            while n < len(items) and items[n][0] <= t:
+                R, p, _ = oracle.normalhedge(R, 1.0 - items[n][1], p)
+                n += 1
+            assert applied[t, b] == n
+            assert np.allclose(w[t, b], p, atol=1e-12)
+    assert np.array_equal(applied[:, 0], K * np.arange(1, T + 1))
+
+
+def test_hedge_feedback_censored_levels_never_count():
+    """Levels at or past min(L + 1, K) are censored: any value there leaves every weight unchanged."""
+    rng = np.random.default_rng(121)
+    T, N, B, K = 15, 6, 4, 5
+    gamma, L = _hf_rounds(rng, T, N, B, K)
+    for obj in (0, 1):
+        w, a = oracle.hedge_feedback(gamma, L, objective=obj)
+        g2 = gamma.copy()
+        for t in range(T):
+            for b in range(B):
+                g2[t, :, b, min(int(L[t, b]) + 1, K):] = rng.uniform(0, 1, (N, K - min(int(L[t, b]) + 1, K)))
+        w2, a2 = oracle.hedge_feedback(g2, L, objective=obj)
+        assert np.array_equal(a, a2) and np.array_equal(w, w2)
+
+
+def test_hedge_feedback_accept_length_window_and_delay():
+    """Objective 1: item n's loss is K + 1 minus the accept-length estimate over items n .. n + K - 1 (the
+    estimate pinned by enumeration and simulated chains above); it is applied in the push that delivers item
+    n + K - 1, so at most K - 1 items wait after a push and none waits for more than K - 1 later items."""
+    rng = np.random.default_rng(122)
+    T, N, B, K = 20, 4, 3, 4
+    gamma, L = _hf_rounds(rng, T, N, B, K)
+    w, applied = oracle.hedge_feedback(gamma, L, objective=1)
+    for b in range(B):
+        items = _revealed(gamma, L, b)
+        G = np.array([it[1] for it in items])               # [n_items, N]
+        R, p = np.zeros(N), np.full(N, 1.0 / N)
+        n = 0
+        for t in range(T):
+            arrived = sum(1 for it in items if it[0] <= t)
+            assert applied[t, b] == max(0, arrived - K + 1)
+            assert arrived - applied[t, b] <= K - 1
+            while n + K - 1 < arrived:
+                win = G[n:n + K].T[None]                      # [1, N, K]
+                est, loss = oracle.accept_length(win)
+                R, p, _ = oracle.normalhedge(R, loss[0], p)
+                n += 1
+            assert np.allclose(w[t, b], p, atol=1e-12)
+
+
+def test_hedge_feedback_learns_the_best_drafter():
+    """A drafter whose gamma is larger at every level ends with most of the weight, under both losses and
+    with heavy censoring."""
+    rng = np.random.default_rng(123)
+    T, N, B, K = 150, 6, 2, 5
+    gamma = rng.uniform(0.2, 0.8, (T, N, B, K))
+    gamma[:, 2] = np.minimum(gamma[:, 2] + 0.15, 1.0)
+    L = rng.integers(0, 3, (T, B)).astype(np.int32)
+    for obj in (0, 1):
+        w, _ = oracle.hedge_feedback(gamma, L, objective=obj)
+        assert np.all(np.argmax(w[-1], axis=1) == 2)
+        assert np.all(w[-1][:, 2] > 0.5)
+
+
+def test_hedge_feedback_rejects_bad_lengths():
+    g = np.full((2, 3, 1, 4), 0.5)
+    with pytest.raises(ValueError):
+        oracle.hedge_feedback(g, np.array([[0], [5]], np.int32))
+    with pytest.raises(ValueError):
+        oracle.hedge_feedback(g, np.array([[0], [-1]], np.int32))
 
 
 # ----------------------------------------------------------------------------------------------
