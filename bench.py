@@ -229,6 +229,167 @@ def run_reference(args, w):
 # ------------------------------------------------------------------------------------------------
 # GPU arm
 # ------------------------------------------------------------------------------------------------
+# The per-workload records of the line: every named workload at the Llama-3 / Qwen vocabularies, each timed
+# the same way as the headline (graph replay over a ring of distinct input batches larger than L2), plus the
+# standardised-sampling path (top-k / top-p) on the headline's shapes.
+RECORD_WORKLOADS = ("sps_llama3_b64_k5", "hedgespec_n7_b32_k5", "cactus_qwen_b128_m20", "hedgespec_n21_b256_k8")
+FILTER_TOP_K, FILTER_TOP_P = 64, 0.95
+
+
+class Runner:
+    """One workload on one device: its ring of input batches, output buffers and the call through the binding."""
+
+    def __init__(self, sv, torch, w, dev, rank, max_ring, kind=None, filtered=False):
+        self.sv, self.torch, self.w, self.dev = sv, torch, w, dev
+        self.kind = kind or kind_of(w)
+        self.filtered = filtered
+        self.batch_bytes = w.algorithmic_bytes()
+        ring = max(2, -(-4 * L2_BYTES // self.batch_bytes))        # >= 4x L2 in flight across the ring
+        self.ring = min(ring, max_ring)
+        self.batches = [workloads.make(w.scaled(gen_seed=w.gen_seed + 101 * i + 7919 * rank), device=dev)
+                        for i in range(self.ring)]
+        if filtered:
+            n = sv.load().spec_filter_workspace_size(w.B, w.K, w.V, 0 if w.dtype == "bf16" else 1)
+            self.ws = torch.zeros(n, dtype=torch.uint8, device=dev)
+        else:
+            self.ws = sv.new_workspace(w.B, w.K, w.V, w.N, dev)
+        self.acc = torch.empty(w.B, dtype=torch.int32, device=dev)
+        self.outt = torch.empty((w.B, w.K + 1), dtype=torch.int32, device=dev)
+        self.gam = torch.empty((w.N, w.B, w.K), dtype=torch.float32, device=dev) if self.kind == "counterfactual" \
+            else None
+        # kernels per call: the row pass (statistics or gamma kernel) and the chain-and-draw kernel; the
+        # filtered path adds its threshold and mask kernels
+        self.launches_per_call = 4 if filtered else 2
+
+    def entry_point(self):
+        w = self.w
+        if self.filtered:
+            return "spec_verify_filtered (top_k %d, top_p %g)" % (FILTER_TOP_K, FILTER_TOP_P)
+        return {"verify": "spec_verify", "cactus": "spec_cactus_verify (delta %g)" % max(w.deltas or (0.0,)),
+                "counterfactual": "spec_counterfactual_gamma (N %d, fused verify of drafter %d)" % (
+                    w.N, w.selected)}[self.kind]
+
+    def call(self, bt, s=None):
+        w, sv = self.w, self.sv
+        if self.filtered:
+            sv.verify_filtered(bt["target"], bt["draft"], bt["tokens"], bt["seeds"], w.temperature, FILTER_TOP_K,
+                               FILTER_TOP_P, accept_len=self.acc, out_tokens=self.outt, want_diag=False,
+                               workspace=self.ws, stream=s)
+        elif self.kind == "counterfactual":
+            sv.counterfactual_gamma(bt["target"], bt["drafters"], w.temperature, w.selected, bt["tokens"],
+                                    bt["seeds"], gamma=self.gam, want_loss=False, accept_len=self.acc,
+                                    out_tokens=self.outt, want_diag=False, workspace=self.ws, stream=s)
+        elif self.kind == "cactus":
+            sv.cactus_verify(bt["target"], bt["draft"], bt["tokens"], bt["seeds"], max(w.deltas), w.temperature,
+                             accept_len=self.acc, out_tokens=self.outt, want_diag=False, workspace=self.ws, stream=s)
+        else:
+            sv.verify(bt["target"], bt["draft"], bt["tokens"], bt["seeds"], w.temperature, accept_len=self.acc,
+                      out_tokens=self.outt, want_diag=False, workspace=self.ws, stream=s)
+
+    def step(self, i):
+        self.call(self.batches[i % self.ring])
+
+    def capture(self, first, steps):
+        """The calls of steps first .. first + steps - 1 captured once into a CUDA graph: host-side marshalling
+        (tens of microseconds of Python a call) would otherwise leave the GPU idle between calls."""
+        torch = self.torch
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(self.dev)
+        with torch.cuda.graph(graph, stream=cap):
+            for i in range(steps):
+                self.step(first + i)
+        graph.replay()
+        torch.cuda.synchronize(self.dev)
+        return graph
+
+    def free(self):
+        self.batches = None
+        self.ws = self.gam = None
+        self.torch.cuda.empty_cache()
+
+
+def timed_replays(torch, graph, replays, stream, dev, pg, local):
+    """Replays `graph` `replays` times between CUDA events on the launching stream, with the clock sampler
+    running; returns (elapsed ms, max over ranks; clock summary)."""
+    barrier(pg, torch)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    start.record(stream)
+    for _ in range(replays):
+        graph.replay()
+    stop.record(stream)
+    barrier(pg, torch)
+    clocks.stop()
+    return max_over_ranks(pg, torch, start.elapsed_time(stop), dev), clocks
+
+
+def sustained(torch, graph, steps, ms_per_step, stream, dev, pg, local, seconds):
+    """The same graph replayed back to back for about `seconds` right after the timed region, with the clock
+    sampler running: tens of clock samples under load, and the per-call time over a longer window."""
+    replays = max(1, int(seconds * 1e3 / max(ms_per_step * steps, 1e-3)))
+    ms, clocks = timed_replays(torch, graph, replays, stream, dev, pg, local)
+    return {"ms_per_step": ms / (replays * steps), "steps": replays * steps, "seconds": ms / 1e3}, clocks
+
+
+def merge_clocks(a, b):
+    """Clock record of the timed region and the sustained replay together."""
+    samples = a.samples + b.samples
+    out = {"sm_mhz": statistics.median(samples) if samples else None,
+           "sm_max_mhz": a.max_mhz or b.max_mhz, "reasons": sorted(a.reasons | b.reasons), "samples": len(samples),
+           "window": "the timed region and the sustained replay of the same graph that follows it"}
+    if a.nvml is None:
+        out["reasons"] = ["nvml unavailable"]
+    return out
+
+
+def cpu_baseline(w, host, seconds, max_seq):
+    n_seq = min(w.B, max_seq)
+    reps, total_dt, cores = 0, 0.0, os.cpu_count() or 1
+    while total_dt < seconds and reps < 1000:
+        _, dt, cores = time_oracle(w, host, n_seq)
+        reps += 1
+        total_dt += dt
+    return {"value": reps * n_seq * w.K / total_dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": "%d of %d sequences of one %s batch, repeated %d times (%.1f s)" % (
+                n_seq, w.B, w.name, reps, total_dt)}
+
+
+def record_for(args, torch, sv, w, dev, rank, stream, pg, local, filtered=False):
+    """Per-workload record: positions/s, the average call, achieved GB/s against the measured peak and the
+    recorded DRAM traffic, timed like the headline; plus a short oracle baseline on the host."""
+    r = Runner(sv, torch, w, dev, rank, args.max_ring, filtered=filtered)
+    for i in range(args.warmup):
+        r.step(i)
+    torch.cuda.synchronize(dev)
+    steps = args.steps
+    graph = r.capture(args.warmup, steps)
+    ms, c1 = timed_replays(torch, graph, 1, stream, dev, pg, local)
+    sus, c2 = sustained(torch, graph, steps, ms / steps, stream, dev, pg, local, args.sustain_seconds)
+    peak, peak_kind = peaks()
+    call_s = ms / steps / 1e3
+    achieved = r.batch_bytes / call_s / 1e9
+    name = w.name + ("+top_k%d_top_p%g" % (FILTER_TOP_K, FILTER_TOP_P) if filtered else "")
+    rec = {"workload": name, "entry_point": r.entry_point(), "B": w.B, "K": w.K, "V": w.V, "N": w.N,
+           "temperature": w.temperature, "positions_per_call": w.positions,
+           "value": w.positions / call_s, "unit": UNIT, "steps": steps, "avg_call_us": call_s * 1e6,
+           "bytes_per_call": r.batch_bytes, "achieved_gbs": achieved, "peak_gbs": peak, "peak_kind": peak_kind,
+           "frac": achieved / peak, "traffic": None if filtered else RECORDED_TRAFFIC.get(kernel_source_hash(), {}).get(w.name),
+           "sustained_call_us": sus["ms_per_step"] * 1e3, "sustained_calls": sus["steps"],
+           "clocks": merge_clocks(c1, c2),
+           "l2": "ring of %d distinct batches (%.0f MB) > 129 MB L2" % (r.ring, r.ring * r.batch_bytes / 1e6),
+           "device_status": sv.read_status(r.ws) if not filtered else None}
+    if filtered:
+        rec["note"] = ("bytes_per_call counts one read of every logit; the path reads the logits three times and "
+                       "writes a filtered copy once")
+    if not args.no_cpu_baseline and rank == 0 and not filtered:
+        host = {k: r.batches[0][k].to("cpu") for k in ("target", "drafters" if r.kind == "counterfactual"
+                                                          else "draft", "tokens", "seeds")}
+        rec["cpu_baseline"] = cpu_baseline(w, host, args.record_cpu_seconds, max(1, args.cpu_sequences // 8))
+    r.free()
+    return rec
+
+
 def run_ours(args, w):
     import torch
     import speculative_decoding_verification_target_gb300 as sv
@@ -237,88 +398,51 @@ def run_ours(args, w):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     sv.load()
-    batch_bytes = w.algorithmic_bytes()
-    ring = max(2, -(-4 * L2_BYTES // batch_bytes))        # >= 4x L2 in flight across the ring
-    ring = min(ring, args.max_ring)
-    batches = [workloads.make(w.scaled(gen_seed=w.gen_seed + 101 * i + 7919 * rank), device=dev)
-               for i in range(ring)]
-    kind = kind_of(w)
-    ws = sv.new_workspace(w.B, w.K, w.V, w.N, dev)
-    acc = torch.empty(w.B, dtype=torch.int32, device=dev)
-    outt = torch.empty((w.B, w.K + 1), dtype=torch.int32, device=dev)
-    gam = torch.empty((w.N, w.B, w.K), dtype=torch.float32, device=dev) if kind == "counterfactual" else None
     stream = torch.cuda.current_stream(dev)
-    # kernels per call: the statistics pass (gamma kernel for gamma calls) and the chain-and-draw kernel
-    launches_per_call = 2
-
-    def call(bt, s=None):
-        if kind == "counterfactual":
-            sv.counterfactual_gamma(bt["target"], bt["drafters"], w.temperature, w.selected, bt["tokens"],
-                                    bt["seeds"], gamma=gam, want_loss=False, accept_len=acc, out_tokens=outt,
-                                    want_diag=False, workspace=ws, stream=s)
-        elif kind == "cactus":
-            sv.cactus_verify(bt["target"], bt["draft"], bt["tokens"], bt["seeds"], max(w.deltas), w.temperature,
-                             accept_len=acc, out_tokens=outt, want_diag=False, workspace=ws, stream=s)
-        else:
-            sv.verify(bt["target"], bt["draft"], bt["tokens"], bt["seeds"], w.temperature, accept_len=acc,
-                      out_tokens=outt, want_diag=False, workspace=ws, stream=s)
-
-    def step(i):
-        call(batches[i % ring])
-
+    r = Runner(sv, torch, w, dev, rank, args.max_ring)
+    kind = r.kind
+    batch_bytes = r.batch_bytes
     for i in range(args.warmup):
-        step(i)
+        r.step(i)
     torch.cuda.synchronize(dev)
-    # Host-side marshalling per call (tens of microseconds of Python) would otherwise leave the GPU idle
-    # between ~30 us calls: the K timed steps are captured once into a CUDA graph and replayed.
-    graph = torch.cuda.CUDAGraph()
-    cap = torch.cuda.Stream(dev)
-    with torch.cuda.graph(graph, stream=cap):
-        for i in range(args.steps):
-            step(args.warmup + i)
-    graph.replay()
-    torch.cuda.synchronize(dev)
-    barrier(pg, torch)
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(local)
-    clocks.start()
-    start.record(stream)
-    graph.replay()
-    stop.record(stream)
-    barrier(pg, torch)
-    clocks.stop()
-    elapsed_ms = start.elapsed_time(stop)
-    elapsed_ms = max_over_ranks(pg, torch, elapsed_ms, dev)
+    graph = r.capture(args.warmup, args.steps)
+    # the timed region: exactly `steps` calls (one graph replay)
+    elapsed_ms, clocks_timed = timed_replays(torch, graph, 1, stream, dev, pg, local)
+    sus, clocks_sus = sustained(torch, graph, args.steps, elapsed_ms / args.steps, stream, dev, pg, local,
+                                args.sustain_seconds)
     # eager calls through the binding, for reference (includes host marshalling gaps)
     e_start, e_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e_start.record(stream)
     for i in range(args.steps):
-        step(i)
+        r.step(i)
     e_stop.record(stream)
     torch.cuda.synchronize(dev)
     eager_ms = e_start.elapsed_time(e_stop) / args.steps
-    status = sv.read_status(ws)
+    status = sv.read_status(r.ws)
 
     # end to end through the public call: pinned host inputs -> device, the call, results -> host
-    hb = batches[0]
+    hb = r.batches[0]
     in_keys = ("target", "drafters" if kind == "counterfactual" else "draft", "tokens", "seeds")
     host_in = {k: hb[k].to("cpu").pin_memory() for k in in_keys}
     dev_in = {k: torch.empty_like(hb[k]) for k in host_in}
     host_out = {"accept_len": torch.empty(w.B, dtype=torch.int32).pin_memory(),
                 "out_tokens": torch.empty((w.B, w.K + 1), dtype=torch.int32).pin_memory()}
-    if gam is not None:
-        host_out["gamma"] = torch.empty(tuple(gam.shape), dtype=torch.float32).pin_memory()
+    if r.gam is not None:
+        host_out["gamma"] = torch.empty(tuple(r.gam.shape), dtype=torch.float32).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
     d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+
+    def copy_out():
+        host_out["accept_len"].copy_(r.acc, non_blocking=True)
+        host_out["out_tokens"].copy_(r.outt, non_blocking=True)
+        if r.gam is not None:
+            host_out["gamma"].copy_(r.gam, non_blocking=True)
 
     def e2e_step():
         for k in host_in:
             dev_in[k].copy_(host_in[k], non_blocking=True)
-        call(dev_in, stream)
-        host_out["accept_len"].copy_(acc, non_blocking=True)
-        host_out["out_tokens"].copy_(outt, non_blocking=True)
-        if gam is not None:
-            host_out["gamma"].copy_(gam, non_blocking=True)
+        r.call(dev_in, stream)
+        copy_out()
 
     e2e_steps = max(3, min(args.steps, 20 if batch_bytes < (2 << 30) else 3))
     for _ in range(2):
@@ -354,12 +478,9 @@ def run_ours(args, w):
             if i + 1 < n:
                 copy_in(i + 1)
             stream.wait_event(copied[i % 2])
-            call(dev_in2[i % 2], stream)
+            r.call(dev_in2[i % 2], stream)
             consumed[i % 2].record(stream)
-            host_out["accept_len"].copy_(acc, non_blocking=True)
-            host_out["out_tokens"].copy_(outt, non_blocking=True)
-            if gam is not None:
-                host_out["gamma"].copy_(gam, non_blocking=True)
+            copy_out()
 
     e2e_pipelined(2)
     torch.cuda.synchronize(dev)
@@ -369,6 +490,18 @@ def run_ours(args, w):
     e1.record(stream)
     barrier(pg, torch)
     e2e_ms = max_over_ranks(pg, torch, e0.elapsed_time(e1), dev)
+    host_first = {k: r.batches[0][k].to("cpu") for k in in_keys} if not args.no_cpu_baseline else None
+    r.free()
+    del dev_in, dev_in2, host_in
+
+    # every named workload at the large vocabularies, and the filtered path, timed the same way
+    records = []
+    if not args.no_records:
+        for name in RECORD_WORKLOADS:
+            if name == w.name:
+                continue
+            records.append(record_for(args, torch, sv, workloads.WORKLOADS[name], dev, rank, stream, pg, local))
+        records.append(record_for(args, torch, sv, w, dev, rank, stream, pg, local, filtered=True))
 
     if rank != 0:
         return 0
@@ -382,17 +515,16 @@ def run_ours(args, w):
     peak, peak_kind = peaks()
     avg_call_s = elapsed_ms / args.steps / 1e3
     achieved = batch_bytes / avg_call_s / 1e9
+    clocks = merge_clocks(clocks_timed, clocks_sus)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "fp32", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "K": w.K, "V": w.V, "N": w.N, "temperature": w.temperature,
                    "positions_per_step_per_gpu": w.positions, "bytes_per_step_per_gpu": batch_bytes,
-                   "entry_point": {"verify": "spec_verify", "cactus": "spec_cactus_verify (delta %g)" % max(
-                       w.deltas or (0.0,)), "counterfactual": "spec_counterfactual_gamma (N %d, fused verify "
-                       "of drafter %d)" % (w.N, w.selected)}[kind],
+                   "entry_point": r.entry_point(),
                    "l2": "inputs larger than L2: ring of %d distinct batches (%.0f MB) > 129 MB L2" % (
-                       ring, ring * batch_bytes / 1e6),
+                       r.ring, r.ring * batch_bytes / 1e6),
                    "parallelism": "replicas over sequences" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": RECORDED_TRAFFIC.get(kernel_source_hash(), {}).get(w.name), "peak_kind": peak_kind,
@@ -401,29 +533,22 @@ def run_ours(args, w):
                                    "gamma_kernel" if kind == "counterfactual" else "stats_kernel", kind),
                      "avg_call_us": avg_call_s * 1e6, "eager_call_us": eager_ms * 1e3,
                      "frac_of_8tbs_nominal": achieved / 8000.0},
+        "sustained": {"ms_per_step": sus["ms_per_step"], "steps": sus["steps"], "seconds": sus["seconds"],
+                      "frac": batch_bytes / (sus["ms_per_step"] / 1e3) / 1e9 / peak},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_best_ms / e2e_steps,
                 "mode": "pipelined: step i + 1's host-to-device copy overlaps step i's call (two device buffers)"
                         if pipelined else "serial: copy in, call, copy out, one step after another",
                 "pipelined_value": positions * e2e_steps / (e2e_ms / 1e3),
                 "serial_value": positions * e2e_steps / (e2e_serial_ms / 1e3)},
-        "gpu_launches": launches_per_call * args.steps,
-        "clocks": clocks.summary(),
+        "gpu_launches": r.launches_per_call * args.steps,
+        "clocks": clocks,
         "device_status": status,
     }
-    if not args.no_cpu_baseline:
-        host = {k: batches[0][k].to("cpu") for k in ("target", "drafters" if kind == "counterfactual" else "draft",
-                                                       "tokens", "seeds")}
-        n_seq = min(w.B, args.cpu_sequences)
-        reps, total_dt = 0, 0.0
-        while total_dt < args.cpu_seconds and reps < 1000:
-            _, dt, cores = time_oracle(w, host, n_seq)
-            reps += 1
-            total_dt += dt
-        line["cpu_baseline"] = {"value": reps * n_seq * w.K / total_dt, "unit": UNIT, "cores": cores,
-                                "kind": "oracle",
-                                "sample": "%d of %d sequences of one %s batch, repeated %d times (%.1f s)" % (
-                                    n_seq, w.B, w.name, reps, total_dt)}
+    if host_first is not None:
+        line["cpu_baseline"] = cpu_baseline(w, host_first, args.cpu_seconds, args.cpu_sequences)
+    if records:
+        line["records"] = records
     print(json.dumps(line), flush=True)
     return 0
 
@@ -440,6 +565,9 @@ def main():
     ap.add_argument("--ref-sequences", type=int, default=16)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-records", action="store_true", help="headline workload only")
+    ap.add_argument("--sustain-seconds", type=float, default=0.5)
+    ap.add_argument("--record-cpu-seconds", type=float, default=4.0)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w = workloads.WORKLOADS[args.workload]
