@@ -159,9 +159,36 @@ spec_status spec_accept_length_estimate(const float* gamma, int N, int B, int K,
  * or the accept-length loss); regret: device float [N], the cumulative regret, updated in place by
  * (weights . loss) - loss. Next weights: p_i proportional to ([R_i]+ / c) exp([R_i]+^2 / (2 c)) with c solving
  * (1/N) sum_i exp([R_i]+^2 / (2 c)) = e; uniform when no regret is positive. Start from regret 0 and uniform
- * weights. Delayed feedback (the notes' queue of Joulani et al. 2013) is the caller's: apply rounds in the
- * order their feedback arrives. 1 <= N <= 64. One warp; asynchronous on `stream`; allocates nothing. */
+ * weights. For the notes' delayed, censored feedback, spec_hedge_feedback_push keeps the queue and applies
+ * this rule to each loss as it becomes available. 1 <= N <= 64. One warp; asynchronous on `stream`; allocates nothing. */
 spec_status spec_normalhedge_update(float* regret, const float* loss, float* weights, int N, void* stream);
+
+/* NormalHedge under delayed, censored feedback, one learner per sequence ("Not-a-Bandit ...", Key design 3:
+ * the accepted tokens of a round are revealed as one block when the round ends; the counterfactual feedback
+ * is censored unless the selected drafter fills the chunk; the loss is 1 - gamma or the accept length still
+ * available up to K + 1; the delay is at most 2K; in practice the learner keeps a queue of feedback and keeps
+ * applying the next available one, the stochastic-setting reduction of Joulani, Gyorgy, Szepesvari, "Online
+ * learning under delayed feedback", ICML 2013). The notes give no pseudo-code; the reading taken:
+ *  - each round, spec_hedge_feedback_push receives the round's counterfactual gamma [N, B, K] (as written by
+ *    spec_counterfactual_gamma) and the accepted length accept_len [B] of the selected drafter. For sequence
+ *    b, levels j < min(accept_len[b] + 1, K) have a fully verified context and are appended, in level order,
+ *    to the sequence's queue of feedback items; the levels after them are censored and never used;
+ *  - objective 0 (acceptance probability): an item's loss is 1 - gamma, available at once;
+ *    objective 1 (accept length): item n's loss is K + 1 minus the accept-length estimate of
+ *    spec_accept_length_estimate over the window of items n .. n + K - 1, available once item n + K - 1 has
+ *    arrived (so at most 2K - 1 items are ever pending);
+ *  - every newly available loss is applied, oldest item first, as one NormalHedge round
+ *    (spec_normalhedge_update's rule); items whose window never completes are never applied.
+ * State: caller-owned device memory of spec_hedge_feedback_state_size(N, B, K) bytes, 16-byte aligned, set up
+ * by spec_hedge_feedback_init (regrets 0, uniform weights, empty queues, the objective). Outputs of a push
+ * (device, nullable): weights [B, N], the distribution for the next round; applied [B], the NormalHedge rounds
+ * applied so far. An accepted length outside [0, K] skips that sequence's round and sets bit 1 of the status
+ * word at byte 16 of the sequence's state. 1 <= N <= 64, 1 <= K <= 64; one warp per sequence; asynchronous on
+ * `stream`; pushes on one state must not overlap on the GPU. Allocates nothing. */
+size_t spec_hedge_feedback_state_size(int N, int B, int K);
+spec_status spec_hedge_feedback_init(void* state, int N, int B, int K, int objective, void* stream);
+spec_status spec_hedge_feedback_push(void* state, const float* gamma, const int32_t* accept_len, int N, int B, int K,
+                                     float* weights, int32_t* applied, void* stream);
 
 /* Bytes of workspace spec_verify_filtered needs: the spec_verify workspace, one float per row and a filtered
  * copy of every target and draft row (the same size as the logits). 0 for invalid sizes or dtype. */
@@ -213,18 +240,6 @@ spec_status spec_clear_status(void* workspace, void* stream);
 
 /* Thread-local message describing the last non-OK status returned on this thread. */
 const char* spec_last_error(void);
-
-/* Tuning and test hook: forces the number of CTAs of the statistics pass of spec_verify, spec_cactus_verify,
- * spec_cactus_kl_verify and spec_verify_static (1 to 1024; 0 restores the automatic choice, every SM once). The grid fixes how
- * the rows are cut into per-warp segments, so results depend on it only through floating-point summation
- * order. Process-wide, not thread-safe. Returns 0, or -1 for an unsupported value. */
-int spec_debug_set_stats_grid(int ctas);
-
-/* Tuning and test hook: the launch plan of the last call made on this thread, as five ints: 0, ring slots
- * per warp, CTAs launched, kernel (0: the statistics pass of spec_verify / spec_cactus_verify /
- * spec_verify_static; 2: the gamma kernel of spec_counterfactual_gamma, which parks rows in tensor
- * memory; 3: the argmax pass of spec_greedy_verify), pieces per row. out5 is host memory. Returns 0, or -1 for a NULL pointer. */
-int spec_debug_last_plan(int* out5);
 
 #ifdef __cplusplus
 }

@@ -22,8 +22,10 @@ STATUS_BAD_TOKEN, STATUS_TIMEOUT = 1, 2
 EXPORTS = ("spec_workspace_size", "spec_verify", "spec_counterfactual_gamma", "spec_cactus_verify", "spec_cactus_kl_verify",
            "spec_greedy_verify", "spec_accept_length_estimate",
            "spec_normalhedge_update", "spec_filter_workspace_size", "spec_verify_filtered",
-           "spec_read_status", "spec_clear_status", "spec_last_error",
-           "spec_debug_last_plan", "spec_verify_static", "spec_debug_set_stats_grid")
+           "spec_read_status", "spec_clear_status", "spec_last_error", "spec_verify_static",
+           "spec_hedge_feedback_state_size", "spec_hedge_feedback_init", "spec_hedge_feedback_push")
+# tuning and test hooks (csrc/specverify_internal.h): exported by the library, not part of the C ABI
+TEST_HOOKS = ("spec_debug_set_stats_grid", "spec_debug_last_plan", "spec_debug_exp2ff", "spec_debug_set_draw_tau")
 
 _lib = None
 
@@ -70,6 +72,12 @@ def load(build_if_missing: bool = False):
     lib.spec_filter_workspace_size.restype = Z
     lib.spec_verify_filtered.argtypes = [P, P, I, P, P, I, I, I, F, I, F, P, P, P, P, Z, P]
     lib.spec_verify_filtered.restype = I
+    lib.spec_hedge_feedback_state_size.argtypes = [I, I, I]
+    lib.spec_hedge_feedback_state_size.restype = Z
+    lib.spec_hedge_feedback_init.argtypes = [P, I, I, I, I, P]
+    lib.spec_hedge_feedback_init.restype = I
+    lib.spec_hedge_feedback_push.argtypes = [P, P, P, I, I, I, P, P, P]
+    lib.spec_hedge_feedback_push.restype = I
     lib.spec_read_status.argtypes = [P, P, P]
     lib.spec_read_status.restype = I
     lib.spec_clear_status.argtypes = [P, P]
@@ -80,6 +88,10 @@ def load(build_if_missing: bool = False):
     lib.spec_debug_set_stats_grid.restype = I
     lib.spec_debug_last_plan.argtypes = [ctypes.POINTER(ctypes.c_int)]
     lib.spec_debug_last_plan.restype = I
+    lib.spec_debug_set_draw_tau.argtypes = [F]
+    lib.spec_debug_set_draw_tau.restype = I
+    lib.spec_debug_exp2ff.argtypes = [P, P, P, P, I, F, P]
+    lib.spec_debug_exp2ff.restype = I
     lib.spec_verify_static.argtypes = [P, P, I, P, P, I, I, I, F, P, P, P, ctypes.POINTER(ctypes.c_uint32), P]
     lib.spec_verify_static.restype = I
     _lib = lib
@@ -233,6 +245,37 @@ def normalhedge_update(regret, loss, weights, stream=None):
     for t, nm in ((regret, "regret"), (loss, "loss"), (weights, "weights")):
         _need(t, nm, torch.float32, (N,))
     _check(load().spec_normalhedge_update(_p(regret), _p(loss), _p(weights), N, _stream(stream)))
+
+
+class HedgeFeedback:
+    """NormalHedge learners (one per sequence) under delayed, censored feedback: each round, push the round's
+    counterfactual gamma [N, B, K] and the selected drafter's accepted lengths [B]; the revealed levels are
+    queued and every available loss is applied (objective 0: 1 - gamma per level; 1: the accept-length loss
+    over a window of K levels). `weights` [B, N] is the distribution for the next round."""
+
+    def __init__(self, N, B, K, objective=0, device=None, stream=None):
+        self.N, self.B, self.K = N, B, K
+        lib = load()
+        n = int(lib.spec_hedge_feedback_state_size(N, B, K))
+        if n == 0 and B > 0:
+            raise ValueError("unsupported sizes N=%d B=%d K=%d" % (N, B, K))
+        dev = device or "cuda"
+        self.state = torch.zeros(max(n, 16), dtype=torch.uint8, device=dev)
+        self.weights = torch.full((B, N), 1.0 / N, dtype=torch.float32, device=dev)
+        self.applied = torch.zeros(B, dtype=torch.int32, device=dev)
+        _check(lib.spec_hedge_feedback_init(_p(self.state), N, B, K, int(objective), _stream(stream)))
+
+    def push(self, gamma, accept_len, stream=None):
+        _need(gamma, "gamma", torch.float32, (self.N, self.B, self.K))
+        _need(accept_len, "accept_len", torch.int32, (self.B,))
+        _check(load().spec_hedge_feedback_push(_p(self.state), _p(gamma), _p(accept_len), self.N, self.B, self.K,
+                                               _p(self.weights), _p(self.applied), _stream(stream)))
+        return self.weights
+
+    def status(self):
+        """Per-sequence status words (bit 1: a round with an accepted length outside [0, K] was skipped)."""
+        n = self.state.numel() // max(self.B, 1)
+        return self.state.view(self.B, n)[:, 16:20].contiguous().view(torch.int32).view(-1).cpu()
 
 
 def verify_filtered(target, draft, tokens, seeds, temperature=1.0, top_k=0, top_p=1.0, *, accept_len=None,

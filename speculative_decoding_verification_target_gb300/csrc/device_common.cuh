@@ -234,6 +234,31 @@ __device__ __forceinline__ FF warp_incl_scan_ff(FF v, int lane) {
     }
     return v;
 }
+// a * b for floats a, b as a float-float (the product's rounding error recovered with one fused multiply-add)
+__device__ __forceinline__ FF ff_two_prod(float a, float b) {
+    const float p = __fmul_rn(a, b);
+    return {p, __fmaf_rn(a, b, -p)};
+}
+// a * b for float-floats (the lo * lo term, below the result's precision, is dropped)
+__device__ __forceinline__ FF ff_mul(FF a, FF b) {
+    const FF p = ff_two_prod(a.hi, b.hi);
+    return ff_fast_two_sum(p.hi, __fadd_rn(p.lo, __fmaf_rn(a.hi, b.lo, __fmul_rn(a.lo, b.hi))));
+}
+// Square root of a float-float x >= 0: the float root y0 and one Newton step on the exact residual
+// x - y0^2, y = y0 + (x - y0^2) / (2 y0).
+__device__ __forceinline__ FF ff_sqrt(FF x) {
+    if (!(x.hi > 0.f)) return {0.f, 0.f};
+    const float y0 = __fsqrt_rn(x.hi);
+    const FF sq = ff_two_prod(y0, y0);
+    const float r = __fadd_rn(__fadd_rn(__fsub_rn(x.hi, sq.hi), -sq.lo), x.lo);   // x - y0^2 (x.hi - sq.hi exact)
+    return ff_fast_two_sum(y0, __fdiv_rn(r, __fmul_rn(2.f, y0)));
+}
+// a / b for float-floats, b > 0: the float quotient and one correction with the exact residual.
+__device__ __forceinline__ FF ff_div(FF a, FF b) {
+    const float q0 = __fdiv_rn(a.hi, b.hi);
+    const FF r = ff_sub(a, ff_mul(b, FF{q0, 0.f}));
+    return ff_fast_two_sum(q0, __fdiv_rn(__fadd_rn(r.hi, r.lo), b.hi));
+}
 __device__ __forceinline__ void st_cluster_f32x2(uint32_t addr, float a, float b) {
     asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
 }

@@ -8,6 +8,7 @@
 #include <mutex>
 
 #include "specverify.h"
+#include "specverify_internal.h"
 #include "specverify_filter.cuh"
 #include "specverify_gamma.cuh"
 
@@ -29,8 +30,12 @@ constexpr int MAX_V = 262144;
 constexpr int MAX_N = 64;
 constexpr size_t WS_HEADER = 256;          // status word + padding
 constexpr int SMEM_MAX_PER_CTA = 232448;   // opt-in maximum per CTA
+constexpr int DYN_SMEM_CEIL = SMEM_MAX_PER_CTA - 24576;   // dynamic ceiling of the gamma kernel (its static
+                                                          // shared memory stays below 24 KB)
+constexpr int DRAW_SMEM_CEIL = SMEM_MAX_PER_CTA - 65536;  // and of the draw kernel (static below 64 KB)
 
 int g_stats_grid_override = 0;   // CTAs of the statistics kernel (0 = automatic)
+float g_draw_tau = 0.f;          // chunk mass above which the draw takes its float-float path (0 = default)
 thread_local int g_last_plan[5] = {0, 0, 0, 0, 0};   // see spec_debug_last_plan
 
 // Workspace layout: [status header][row partials]. The row partials are the statistics pass's segment
@@ -125,8 +130,8 @@ cudaError_t stats_ctas(StatsFn fn, size_t smem, int& out) {
     return cudaSuccess;
 }
 
-// Raises the dynamic shared-memory ceiling of a draw kernel once per device (its chunk masses need up to
-// 128 KB).
+// Raises the dynamic shared-memory ceiling of a draw or gamma kernel once per device (the draw's bulk-copy
+// slots take 128 KB for bf16 rows, the gamma kernel's ring 197 KB).
 std::mutex g_dsm_mu;
 struct DsmEntry {
     const void* fn;
@@ -136,13 +141,34 @@ DsmEntry g_dsm[32];
 int g_dsm_n = 0;
 
 template <class Fn>
-cudaError_t draw_smem_ceiling(Fn fn, int dev) {
+cudaError_t draw_smem_ceiling(Fn fn, int dev, int ceiling) {
     std::lock_guard<std::mutex> lk(g_dsm_mu);
     for (int i = 0; i < g_dsm_n; ++i)
         if (g_dsm[i].fn == reinterpret_cast<const void*>(fn) && g_dsm[i].device == dev) return cudaSuccess;
-    const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX_PER_CTA - 8192);
+    const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, ceiling);
     if (e == cudaSuccess && g_dsm_n < 32) g_dsm[g_dsm_n++] = {reinterpret_cast<const void*>(fn), dev};
     return e;
+}
+
+// Constants of the draw's float-float arithmetic, from double precision: 2^(k/32) for k = -16..16, ln 2 and
+// c = log2(e) / T, each split into a float pair; and the chunk mass above which a chunk takes the exact path.
+FFc ff_constants(float temperature) {
+    FFc k = {};
+    auto split = [](double v) { const float h = static_cast<float>(v); return make_float2(h, static_cast<float>(v - h)); };
+    for (int j = -16; j <= 16; ++j) k.tab[j + 16] = split(std::exp2(j / 32.0));
+    const double ln2 = std::log(2.0);
+    const float2 l = split(ln2);
+    k.ln2_hi = l.x;
+    k.ln2_lo = l.y;
+    // c_hi rounded towards zero, so that c_lo > 0: a -inf logit then gives -inf * c_lo + l = -inf and an
+    // exponent of -inf (a negative c_lo would make it -inf + inf = NaN)
+    const double cd = 1.0 / (ln2 * static_cast<double>(temperature));
+    float ch = static_cast<float>(cd);
+    if (static_cast<double>(ch) >= cd) ch = std::nextafter(ch, 0.f);
+    k.c_hi = ch;
+    k.c_lo = static_cast<float>(cd - static_cast<double>(ch));
+    k.tau = g_draw_tau > 0.f ? g_draw_tau : D_TAU;
+    return k;
 }
 
 // The chain and its draw for one drafter (one cluster per sequence), launched with programmatic stream
@@ -167,7 +193,9 @@ spec_status launch_draw(const Call& a, bool aligned, const unsigned char* draft,
     d.V = a.V;
     d.c = static_cast<float>(1.4426950408889634 / static_cast<double>(a.temperature));
     d.delta = a.delta;
-    d.cactus = a.cactus;
+    // delta = 0 makes gamma* = p_target(n) and the scale 1 exactly: the standard draw
+    d.cactus = a.delta > 0.f ? a.cactus : 0;
+    d.k = ff_constants(a.temperature);
     d.accept_len = a.accept_len;
     d.out_tokens = a.out_tokens;
     d.diag = a.diag;
@@ -181,16 +209,15 @@ spec_status launch_draw(const Call& a, bool aligned, const unsigned char* draft,
     int cps = 1;
     while (cps < D_MAX_CPS && static_cast<long long>(a.B) * cps * 2 <= sms) cps *= 2;
     d.cps = cps;
-    // chunk masses, plus (bulk-copy mode) a two-piece slot and an mbarrier per warp when they fit
-    const size_t cm_bytes = static_cast<size_t>((d.np + cps - 1) / cps) * D_CPP * sizeof(float);
+    // (bulk-copy mode) a two-piece slot and an mbarrier per warp, when they fit
     const size_t ring_bytes = static_cast<size_t>(DW) * (2 * static_cast<size_t>(PE) * eb + sizeof(uint64_t));
-    const size_t dsmem_cap = SMEM_MAX_PER_CTA - 8192;   // the ceiling draw_smem_ceiling sets
-    d.tma = aligned && cm_bytes + ring_bytes <= dsmem_cap ? 1 : 0;
-    const size_t dsmem = cm_bytes + (d.tma ? ring_bytes : 0);
+    const size_t dsmem_cap = DRAW_SMEM_CEIL;   // the ceiling draw_smem_ceiling sets for it
+    d.tma = aligned && ring_bytes <= dsmem_cap ? 1 : 0;
+    const size_t dsmem = d.tma ? ring_bytes : 0;
     using DrawFn = void (*)(const DParams);
     DrawFn dfn = a.dtype == SPEC_BF16 ? (aligned ? draw_kernel<Bf16, true> : draw_kernel<Bf16, false>)
                                       : (aligned ? draw_kernel<F32, true> : draw_kernel<F32, false>);
-    e = draw_smem_ceiling(dfn, dev);
+    e = draw_smem_ceiling(dfn, dev, DRAW_SMEM_CEIL);
     if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "draw kernel attribute failed: %s", cudaGetErrorString(e));
     // its CTAs start as the grid before it frees SMs and wait for it (griddepcontrol.wait) after reading
     // their inputs
@@ -383,7 +410,7 @@ spec_status run_gamma(const Call& a, bool aligned) {
     g.status = reinterpret_cast<unsigned*>(ws);
     using GammaFn = void (*)(const CgParams);
     GammaFn gfn = a.dtype == SPEC_BF16 ? gamma_kernel<Bf16> : gamma_kernel<F32>;
-    e = draw_smem_ceiling(gfn, dev);   // G_SMEM is below that ceiling
+    e = draw_smem_ceiling(gfn, dev, DYN_SMEM_CEIL);   // G_SMEM is below that ceiling
     if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "gamma kernel attribute failed: %s", cudaGetErrorString(e));
     g_last_plan[0] = 0;
     g_last_plan[1] = G_R;
@@ -671,6 +698,54 @@ spec_status spec_normalhedge_update(float* regret, const float* loss, float* wei
     return SPEC_OK;
 }
 
+size_t spec_hedge_feedback_state_size(int N, int B, int K) {
+    if (N < 1 || N > MAX_N || B < 0 || K < 1 || K > MAX_K) return 0;
+    return hf_seq_bytes(N, K) * static_cast<size_t>(B);
+}
+
+spec_status spec_hedge_feedback_init(void* state, int N, int B, int K, int objective, void* stream) {
+    if (N < 1 || N > MAX_N) return fail(SPEC_ERR_INVALID, "N must be in [1, %d] (got %d)", MAX_N, N);
+    if (B < 0) return fail(SPEC_ERR_INVALID, "B must be >= 0 (got %d)", B);
+    if (K < 1 || K > MAX_K) return fail(SPEC_ERR_INVALID, "K must be in [1, %d] (got %d)", MAX_K, K);
+    if (objective != 0 && objective != 1) return fail(SPEC_ERR_INVALID, "objective must be 0 or 1 (got %d)", objective);
+    if (B == 0) return SPEC_OK;
+    if (!state) return fail(SPEC_ERR_INVALID, "state must not be NULL");
+    if (reinterpret_cast<uintptr_t>(state) % 16) return fail(SPEC_ERR_INVALID, "state must be 16-byte aligned");
+    HfParams h = {};
+    h.state = static_cast<unsigned char*>(state);
+    h.N = N;
+    h.B = B;
+    h.K = K;
+    h.objective = objective;
+    hedge_feedback_init_kernel<<<static_cast<unsigned>((B + 7) / 8), 256, 0, static_cast<cudaStream_t>(stream)>>>(h);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "hedge feedback init launch failed: %s", cudaGetErrorString(e));
+    return SPEC_OK;
+}
+
+spec_status spec_hedge_feedback_push(void* state, const float* gamma, const int32_t* accept_len, int N, int B, int K,
+                                     float* weights, int32_t* applied, void* stream) {
+    if (N < 1 || N > MAX_N) return fail(SPEC_ERR_INVALID, "N must be in [1, %d] (got %d)", MAX_N, N);
+    if (B < 0) return fail(SPEC_ERR_INVALID, "B must be >= 0 (got %d)", B);
+    if (K < 1 || K > MAX_K) return fail(SPEC_ERR_INVALID, "K must be in [1, %d] (got %d)", MAX_K, K);
+    if (B == 0) return SPEC_OK;
+    if (!state || !gamma || !accept_len) return fail(SPEC_ERR_INVALID, "state, gamma and accept_len must not be NULL");
+    if (reinterpret_cast<uintptr_t>(state) % 16) return fail(SPEC_ERR_INVALID, "state must be 16-byte aligned");
+    HfParams h = {};
+    h.state = static_cast<unsigned char*>(state);
+    h.gamma = gamma;
+    h.accept_len = accept_len;
+    h.N = N;
+    h.B = B;
+    h.K = K;
+    h.weights = weights;
+    h.applied = applied;
+    hedge_feedback_push_kernel<<<static_cast<unsigned>((B + 7) / 8), 256, 0, static_cast<cudaStream_t>(stream)>>>(h);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "hedge feedback push launch failed: %s", cudaGetErrorString(e));
+    return SPEC_OK;
+}
+
 size_t spec_filter_workspace_size(int B, int K, int V, spec_dtype dtype) {
     if (B < 0 || K < 0 || V < 1 || (dtype != SPEC_BF16 && dtype != SPEC_FP32)) return 0;
     return filter_layout(B, K, V, dtype == SPEC_BF16 ? 2 : 4).total;
@@ -789,6 +864,21 @@ const char* spec_last_error(void) { return g_err; }
 int spec_debug_last_plan(int* out5) {
     if (!out5) return -1;
     for (int i = 0; i < 5; ++i) out5[i] = g_last_plan[i];
+    return 0;
+}
+
+int spec_debug_exp2ff(const float* d, const float* l_hi, const float* l_lo, float* out, int n, float temperature,
+                      void* stream) {
+    if (n < 0 || !(temperature > 0.f) || (n > 0 && (!d || !l_hi || !l_lo || !out))) return -1;
+    if (n == 0) return 0;
+    ff_exp2_probe_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        d, l_hi, l_lo, out, n, ff_constants(temperature));
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+int spec_debug_set_draw_tau(float tau) {
+    if (!(tau >= 0.f)) return -1;
+    g_draw_tau = tau;
     return 0;
 }
 

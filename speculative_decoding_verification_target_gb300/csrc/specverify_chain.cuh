@@ -251,6 +251,9 @@ __global__ void __launch_bounds__(SNT, 1) stats_kernel(const __grid_constant__ S
 // draw kernel
 // ------------------------------------------------------------------------------------------------
 constexpr int D_MAX_CPS = 8;            // CTAs per sequence (one cluster)
+constexpr float D_TAU = 1.f / 1024.f;   // fast chunk mass (residual plus overlap) above which a chunk is recomputed
+                                        // at float-float precision
+constexpr int D_QCH = 32;               // chunks of a warp's queue of such chunks
 constexpr int D_CPP = PE / CHUNK;       // chunks per piece
 
 struct DParams {
@@ -269,6 +272,7 @@ struct DParams {
     int tma;                       // 1: pieces come through a per-warp shared-memory slot by bulk copies
     float c, delta;
     int cactus;                    // 0: standard, 1: Cactus (Taylor gamma*), 2: Cactus (root of the KL constraint)
+    FFc k;                         // constants of the float-float arithmetic of the draw
     int32_t* accept_len;           // [B]
     int32_t* out_tokens;           // [B, K+1]
     float* diag;                   // [B, K, 4] or null
@@ -292,118 +296,98 @@ __device__ __forceinline__ MaxSum d_row_stats(const DParams& p, const Split& sp,
     return warp_ms(a, c);
 }
 
-// Masses of the chunks lane l holds of a piece (chunks l + 32 q): mode 1 the residual (h - q)+, mode 2 h
-// itself, element `et` of the piece (if >= 0) being h = hpatch. Element for element the values of
-// chunk_mass and chunk_values.
+// A float pair stored into the shared memory of CTA 0 of this cluster from CTA `self`.
+__device__ __forceinline__ void st_cta0_f32x2(float2* local, uint32_t self, float a, float b) {
+    if (self == 0) *local = make_float2(a, b);
+    else st_cluster_f32x2(map_to_rank(smem_addr(local), 0), a, b);
+}
+
+// What warp 0 of CTA 0 hands to the CTA for the pick inside the chosen piece.
+struct PickPlan {
+    int ft;          // chosen piece (-1: none, -2: already drawn)
+    FF before, tp;   // mass before the piece; the target u * Z
+};
+
+// The fast mass of one chunk (element et, if >= 0, is the Cactus token with h = hpatch) and its overlap.
 template <class E>
-__device__ __forceinline__ void piece_chunk_masses(int mode, const typename E::Raw (&rt)[PCH],
-                                                   const typename E::Raw (&ro)[PCH], int lane, float c, PairOff o,
-                                                   int et, float hpatch, float (&cm)[PCH]) {
-    const int etc = et >= 0 ? et / CHUNK : -1;
-    float2 unused = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int q = 0; q < PCH; ++q) {
-        if (lane + 32 * q != etc) {
-            cm[q] = chunk_mass<E>(mode, rt[q], ro[q], c, o, unused);
-        } else {
-            float ovl = 0.f;
-            cm[q] = chunk_mass_patch_only<E>(mode, rt[q], ro[q], c, o, et % CHUNK, hpatch, ovl);
-        }
+__device__ __forceinline__ float fast_chunk(int mode, const typename E::Raw& rt, const typename E::Raw& ro, float c,
+                                            PairOff o, int et, float hpatch, float& ovl) {
+    float2 o2 = make_float2(0.f, 0.f);
+    if (et < 0) {
+        const float m = chunk_mass<E>(mode, rt, ro, c, o, o2);
+        ovl = o2.x + o2.y;
+        return m;
     }
+    ovl = 0.f;
+    return chunk_mass_patch_only<E>(mode, rt, ro, c, o, et, hpatch, ovl);
 }
 
-// A float (float-float) of the shared memory of CTA `owner` of this cluster (this CTA's own when owner == self).
-__device__ __forceinline__ float cluster_f32(const float* local, uint32_t owner, uint32_t self) {
-    return owner == self ? *local : ld_cluster_f32(map_to_rank(smem_addr(local), owner));
-}
-__device__ __forceinline__ FF cluster_ff(const float2* local, uint32_t owner, uint32_t self) {
-    const float2 v = owner == self ? *local : ld_cluster_f32x2(map_to_rank(smem_addr(local), owner));
-    return {v.x, v.y};
-}
-
-// Inverse CDF inside piece ft of the row (warp-collective): the chunk whose running mass (from `before`,
-// accumulated in float-float like every sum above the chunk) first exceeds tp, from the chunk masses its CTA kept (chunks 8 l .. 8 l + 7 to lane l), then the element
-// inside that chunk from its recomputed values. When rounding leaves no chunk above tp, the last chunk with
-// positive mass; inside the chunk, the last positive element likewise. -1 if the piece has no mass.
-template <class E, bool AL>
-__device__ int pick_in_piece(const float* cm_slot, uint32_t owner, uint32_t self, const unsigned char* trow,
-                             const unsigned char* orow, int mode, int e_begin, int V, float c, PairOff o,
-                             int tok, float ht, FF tp, FF before, int lane) {
-    const int nch = (min(PE, V - e_begin) + CHUNK - 1) / CHUNK;
-    float cv[8];
-    FF loc = {0.f, 0.f};
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        const int k = 8 * lane + q;
-        cv[q] = k < nch ? cluster_f32(cm_slot + k, owner, self) : 0.f;
-        loc = ff_addf(loc, cv[q]);
-    }
-    const FF incl = warp_incl_scan_ff(loc, lane);
-    const FF end = ff_add(before, incl);
-    const unsigned over = __ballot_sync(0xffffffffu, loc.hi > 0.f && ff_gt(end, tp));
-    const unsigned posm = __ballot_sync(0xffffffffu, loc.hi > 0.f);
-    if (!posm) return -1;
-    const int ln = over ? __ffs(over) - 1 : 31 - __clz(posm);
-    int chunk = -1;
-    FF bchunk = {0.f, 0.f};
-    if (lane == ln) {
-        FF a = ff_sub(end, loc);
-        int pk = -1, lp = -1;
-        FF bpk = {0.f, 0.f}, blp = {0.f, 0.f};
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const FF a2 = ff_addf(a, cv[q]);
-            if (cv[q] > 0.f) {
-                lp = q;
-                blp = a;
-                if (pk < 0 && ff_gt(a2, tp)) {
-                    pk = q;
-                    bpk = a;
-                }
-            }
-            a = a2;
-        }
-        chunk = 8 * ln + (pk >= 0 ? pk : lp);
-        bchunk = pk >= 0 ? bpk : blp;
-    }
-    chunk = __shfl_sync(0xffffffffu, chunk, ln);
-    bchunk = ff_shfl(bchunk, ln);
-    const int e0 = e_begin + chunk * CHUNK;
-    const typename E::Raw rt = E::template gload<AL>(trow, e0, V);
-    const typename E::Raw ro = mode == 1 ? E::template gload<AL>(orow, e0, V) : rt;
-    const int et = (tok >= e0 && tok < e0 + CHUNK) ? tok - e0 : -1;
-    float v[8], ovl = 0.f;
-    chunk_values<E>(mode, rt, ro, c, o, et, ht, v, ovl);
-    FF a = bchunk;
-    int pick = -1, lp = -1;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        a = ff_addf(a, v[q]);
-        if (v[q] > 0.f) {
-            lp = q;
-            if (pick < 0 && ff_gt(a, tp)) pick = q;
-        }
-    }
-    return pick >= 0 ? e0 + pick : (lp >= 0 ? e0 + lp : -1);
+// Cactus at one position, from the token's logit x and its row's offsets: the float-float p_T(n), gamma* and
+// the scale s = (1 - gamma*) / (1 - p_T(n)) of the other tokens (out of line: once per position).
+__device__ __noinline__ void cactus_precise(float x, float nm, float l, float l_lo, float delta, bool kl, const FFc& k,
+                                            const float2* tab, FF& g, FF& sc) {
+    const FF dt = ff_two_sum(x, nm);
+    const FF q1 = ff_exp2(ff_exponent(dt.hi, k, l, l_lo, dt.lo), k, tab);
+    g = cactus_gamma_ff(q1, delta, kl, k);
+    const FF one = {1.f, 0.f};
+    sc = q1.hi < 1.f ? ff_div(ff_sub(one, g), ff_sub(one, q1)) : FF{0.f, 0.f};
 }
 
-// One cluster of cps CTAs per sequence b (CTA rank = blockIdx.x % cps). Every CTA derives the row scalars
+// A warp's queue of large chunks (n of them, n <= D_QCH: raw logits of both rows, the fast mass, the Cactus
+// token's index in the chunk or -1) evaluated at float-float precision, eight lanes to a chunk and four chunks
+// at a time (warp-collective). Returns this lane's share of the corrections (float-float mass minus fast mass).
+template <class E>
+__device__ __noinline__ FF flush_chunks(int mode, const typename E::Raw* qrt, const typename E::Raw* qro, const float* qcm,
+                                        const int* qet, int n, const PairOffX po, const FFc& k, const float2* tab, FF g,
+                                        int lane) {
+    __syncwarp();
+    FF acc = {0.f, 0.f};
+    const int e = lane & 7;
+    for (int base = 0; base < n; base += 4) {
+        const int i = base + (lane >> 3);
+        FF r = {0.f, 0.f};
+        if (i < n) {
+            const float2 xt2 = E::pair(qrt[i], e >> 1), xd2 = E::pair(qro[i], e >> 1);
+            r = elem_exact(mode, (e & 1) ? xt2.y : xt2.x, (e & 1) ? xd2.y : xd2.x, po, k, tab, e == qet[i], g);
+        }
+        const FF sum = group8_sum(r);
+        if (i < n && e == 0) acc = ff_add(acc, ff_addf(sum, -qcm[i]));
+    }
+    __syncwarp();
+    return acc;
+}
+
+// One cluster of cps CTAs per sequence (CTA rank = blockIdx.x % cps). Every CTA derives the row scalars
 // and the chain itself (the same arithmetic on the same data, so the same L); the pieces of the drawn row
-// are dealt to the CTAs round robin, and CTA 0 makes the draw from the masses the CTAs keep in shared
-// memory, read across the cluster.
+// are dealt to the CTAs round robin, each piece's residual mass (its large chunks recomputed at float-float
+// precision) goes to CTA 0, and CTA 0 finds the piece holding u * Z and re-reads that one piece to find the
+// token (fast_chunk, chunk_values and elem_exact give the same values in both places).
 template <class E, bool AL>
 __global__ void __launch_bounds__(DNT, 1) draw_kernel(const __grid_constant__ DParams p) {
     using Raw = typename E::Raw;
-    // dynamic shared memory: [ceil(np / cps)][D_CPP] chunk masses of this CTA's pieces, then (bulk-copy
-    // mode) one slot per warp holding a target piece and a draft piece, then one mbarrier per warp
-    extern __shared__ __align__(128) float d_cm[];
+    // dynamic shared memory (bulk-copy mode): one slot per warp holding a target piece and a draft piece,
+    // then one mbarrier per warp
+    extern __shared__ __align__(128) unsigned char d_smem[];
     __shared__ float s_ht[D_MAX_K + 1], s_pd[D_MAX_K];
-    // row offsets: target rows (nm, plain l), the h rows of the chain (l with the Cactus scale), draft rows
-    __shared__ float s_nmt[D_MAX_K + 1], s_ltp[D_MAX_K + 1], s_lt[D_MAX_K], s_nmo[D_MAX_K], s_lo[D_MAX_K];
+    // row offsets: target rows (nm, l as a float pair), the fast h rows of the chain (l with the Cactus
+    // scale), draft rows
+    __shared__ float s_nmt[D_MAX_K + 1], s_ltp[D_MAX_K + 1], s_ltp_lo[D_MAX_K + 1], s_lt[D_MAX_K];
+    __shared__ float s_nmo[D_MAX_K], s_lo[D_MAX_K], s_lo_lo[D_MAX_K];
     __shared__ float s_xt[D_MAX_K], s_xd[D_MAX_K];
     __shared__ int s_tok[D_MAX_K];
-    __shared__ float2 s_tiles[D_MAX_PIECES];  // piece masses (float-float sums of chunk masses), gathered in CTA 0
-    __shared__ int s_L;
+    __shared__ float2 s_sc[D_MAX_K], s_g[D_MAX_K];   // Cactus, per position: precise scale s and gamma*
+    __shared__ float2 s_tiles[D_MAX_PIECES];          // per piece: residual mass (float-float), gathered in CTA 0
+    __shared__ float2 s_tab[33];                      // the float-float exp2 table
+    __shared__ Raw s_qrt[DW][D_QCH], s_qro[DW][D_QCH];   // per warp: queue of large chunks (logits of both rows,
+    __shared__ float s_qcm[DW][D_QCH];                   // fast mass, Cactus token index)
+    __shared__ int s_qet[DW][D_QCH];
+    __shared__ int s_pl[D_CPP], s_pn;                 // the pick: large chunks of the chosen piece,
+    __shared__ float2 s_pm[D_CPP];                    // their float-float masses (by chunk)
+    __shared__ float2 s_pr[D_CPP][8];                 // and element residuals (by list position)
+    __shared__ float2 s_wscan[DW];                    // the pick's per-warp chunk totals
+    __shared__ int s_wfirst[DW], s_wlast[DW];
+    __shared__ PickPlan s_plan;
+    __shared__ int s_L, s_emit;
     const float NINF = __uint_as_float(0xFF800000u);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int cps = p.cps;
@@ -415,14 +399,13 @@ __global__ void __launch_bounds__(DNT, 1) draw_kernel(const __grid_constant__ DP
     const Split sp(p.P, p.G);
     const bool use_tma = AL && p.tma;
     constexpr int PIECE_BYTES = PE * E::BYTES;
-    unsigned char* const ring = reinterpret_cast<unsigned char*>(d_cm) +
-                                static_cast<size_t>((np + cps - 1) / cps) * D_CPP * sizeof(float);
-    unsigned char* const slot = ring + static_cast<size_t>(warp) * 2 * PIECE_BYTES;
-    uint64_t* const fullb = reinterpret_cast<uint64_t*>(ring + static_cast<size_t>(DW) * 2 * PIECE_BYTES) + warp;
+    unsigned char* const slot = d_smem + static_cast<size_t>(warp) * 2 * PIECE_BYTES;
+    uint64_t* const fullb = reinterpret_cast<uint64_t*>(d_smem + static_cast<size_t>(DW) * 2 * PIECE_BYTES) + warp;
     if (use_tma && lane == 0) {
         mbar_init(fullb, 1);
         fence_mbarrier_init_cluster();
     }
+    for (int i = threadIdx.x; i < 33; i += DNT) s_tab[i] = p.k.tab[i];
     __syncwarp();
     uint32_t uses = 0;       // completed phases of this warp's mbarrier
     int n_issued = 0;        // lane 0: bulk-copy groups started
@@ -458,13 +441,21 @@ __global__ void __launch_bounds__(DNT, 1) draw_kernel(const __grid_constant__ DP
         if (lane == 0) {
             const RowOff o = row_off(ms);
             const float pt = prob_at(x, o, c);   // 0 without a (valid) token
+            // the row offset -log2 S also as a float pair, for the exact recomputations
+            float ll = 0.f;
+            if (ms.s > 0.f) {
+                const FF l2 = ff_log2(FF{ms.s, 0.f}, p.k);
+                ll = __fsub_rn(__fsub_rn(-l2.hi, o.l), l2.lo);
+            }
             if (tgt) {
                 s_nmt[j] = o.nm;
                 s_ltp[j] = o.l;
+                s_ltp_lo[j] = ll;
                 s_ht[j] = pt;
             } else {
                 s_nmo[j] = o.nm;
                 s_lo[j] = o.l;
+                s_lo_lo[j] = ll;
                 s_pd[j] = pt;
             }
         }
@@ -480,9 +471,9 @@ __global__ void __launch_bounds__(DNT, 1) draw_kernel(const __grid_constant__ DP
             if (j < K) {
                 float ht = s_ht[j], lt = s_ltp[j];
                 if (p.cactus) {
-                    float log2s;
-                    if (p.cactus == 2) cactus_scalars_kl(s_ht[j], p.delta, ht, log2s);
-                    else cactus_scalars(s_ht[j], p.delta, ht, log2s);
+                    float log2s, sf;
+                    if (p.cactus == 2) cactus_scalars_kl(s_ht[j], p.delta, ht, log2s, sf);
+                    else cactus_scalars(s_ht[j], p.delta, ht, log2s, sf);
                     lt = s_ltp[j] + log2s;
                 }
                 s_ht[j] = ht;
@@ -506,8 +497,21 @@ __global__ void __launch_bounds__(DNT, 1) draw_kernel(const __grid_constant__ DP
     }
     __syncthreads();
     const int L = s_L;
+    // Cactus, at the positions whose residual is drawn (or reported): gamma* and the scale s of the other
+    // tokens from the float-float p_T(n). The fast masses use them too (h(n) = gamma*, log2 s in the offset).
+    if (p.cactus && warp == 0) {
+        for (int j = lane; j < K; j += 32) {
+            if (s_tok[j] < 0 || !(p.diag || j == L)) continue;
+            FF g1, sc;
+            cactus_precise(s_xt[j], s_nmt[j], s_ltp[j], s_ltp_lo[j], p.delta, p.cactus == 2, p.k, s_tab, g1, sc);
+            s_sc[j] = make_float2(sc.hi, sc.lo);
+            s_g[j] = make_float2(g1.hi, g1.lo);
+            s_lt[j] = s_ltp[j] + log2f(sc.hi);
+        }
+    }
+    __syncthreads();
 
-    // ---- chunk and piece masses of row L (of every position's row pair, too, when diag asks for Z) ----
+    // ---- masses of row L (of every position's row pair, too, when diag asks for Z) ----
     // The number of passes, and so of cluster barriers, depends on the call alone, never on L: with diag,
     // pass K (the bonus row) runs empty unless L = K.
     const int n_pass = p.diag ? K + 1 : 1;
@@ -516,11 +520,16 @@ __global__ void __launch_bounds__(DNT, 1) draw_kernel(const __grid_constant__ DP
         const int j = p.diag ? it : L;
         const bool idle = j == K && L != K;
         const int mode = j < K ? 1 : 2;   // 1: residual (h - q)+ against the draft row, 2: the bonus p_target
+        const bool cact = mode == 1 && p.cactus && s_tok[j] >= 0;
         const unsigned char* trow = p.target + (static_cast<size_t>(b) * (K + 1) + j) * row_bytes;
         const unsigned char* orow = mode == 1 ? p.draft + (static_cast<size_t>(b) * K + j) * row_bytes : trow;
+        // fast offsets (h row with the Cactus scale folded in) and the exact ones
         const PairOff po = mode == 1 ? PairOff{s_nmt[j], s_lt[j], s_nmo[j], s_lo[j]} : PairOff{s_nmt[K], s_ltp[K], 0.f, 0.f};
-        const float ht = mode == 1 ? s_ht[j] : 0.f;
-        const int tok = mode == 1 ? s_tok[j] : -1;
+        const PairOffX px = mode == 1 ? PairOffX{s_nmt[j], s_ltp[j], s_ltp_lo[j], cact ? s_sc[j].x : 1.f, s_nmo[j], s_lo[j], s_lo_lo[j]}
+                                      : PairOffX{s_nmt[K], s_ltp[K], s_ltp_lo[K], 1.f, 0.f, 0.f, 0.f};
+        const int tok = cact ? s_tok[j] : -1;
+        const FF gx = cact ? FF{s_g[j].x, s_g[j].y} : FF{0.f, 0.f};
+        const float hpatch = gx.hi;
         // bulk copy of piece pc of both rows (the target alone for a bonus row) into this warp's slot
         auto issue = [&](int pc) {
             if (lane == 0 && ok_all) {
@@ -561,95 +570,214 @@ __global__ void __launch_bounds__(DNT, 1) draw_kernel(const __grid_constant__ DP
                     ro[q] = mode == 1 ? E::template gload<AL>(orow, e0, V) : rt[q];
                 }
             }
-            const int et = (tok >= pc * PE && tok < pc * PE + PE) ? tok - pc * PE : -1;
-            float cm[PCH];
-            piece_chunk_masses<E>(mode, rt, ro, lane, c, po, et, ht, cm);
             FF loc = {0.f, 0.f};
+            int nq = 0;   // large chunks waiting in this warp's queue
 #pragma unroll
             for (int q = 0; q < PCH; ++q) {
-                d_cm[i * D_CPP + lane + 32 * q] = cm[q];
-                loc = ff_addf(loc, cm[q]);
-            }
-            const FF m = warp_sum(loc);
-            // the piece mass goes straight to CTA 0, which makes the draw
-            if (lane == 0) {
-                if (rank == 0) s_tiles[pc] = make_float2(m.hi, m.lo);
-                else st_cluster_f32x2(map_to_rank(smem_addr(&s_tiles[pc]), 0), m.hi, m.lo);
-            }
-        }
-        cluster_sync_all();   // every CTA's masses are in place and visible to the cluster
-        if (rank == 0 && warp == 0 && !idle) {
-            // piece masses in vocabulary order (np <= 4 * 32: lane l owns pieces seg l .. seg l + seg - 1)
-            const int seg = (np + 31) / 32;
-            const int lo = min(np, lane * seg), hi = min(np, lo + seg);
-            FF tv[4];
-            FF local = {0.f, 0.f};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int t = lo + k;
-                tv[k] = t < hi ? FF{s_tiles[t].x, s_tiles[t].y} : FF{0.f, 0.f};
-                local = ff_add(local, tv[k]);
-            }
-            const FF incl = warp_incl_scan_ff(local, lane);
-            FF excl = ff_shfl_up(incl, 1);
-            if (lane == 0) excl = FF{0.f, 0.f};
-            const FF Z = ff_shfl(incl, 31);
-            if (p.diag && j < K && lane == 0) p.diag[(static_cast<size_t>(b) * K + j) * 4 + 2] = Z.hi + Z.lo;
-            if (j == L) {
-                const float u = philox_uniform(seed, static_cast<uint32_t>(b), static_cast<uint32_t>(L), 1u);
-                if (mode == 1 && !(Z.hi > 0.f)) {
-                    // the residual rounded to zero mass: draw from h over the whole row instead
-                    double all = 0.0;
-                    for (int e0 = lane * CHUNK; e0 < V; e0 += 32 * CHUNK) {
-                        const Raw rt = E::template gload<AL>(trow, e0, V);
-                        float2 unused = make_float2(0.f, 0.f);
-                        const int et = (tok >= e0 && tok < e0 + CHUNK) ? tok - e0 : -1;
-                        all += static_cast<double>(chunk_mass_patched<E>(2, rt, rt, c, po, et, ht, unused));
+                const int e0 = pc * PE + (lane + 32 * q) * CHUNK;
+                const int et = (tok >= e0 && tok < e0 + CHUNK) ? tok - e0 : -1;
+                float ovl;
+                const float cm = fast_chunk<E>(mode, rt[q], ro[q], c, po, et, hpatch, ovl);
+                loc = ff_addf(loc, cm);
+                // a large chunk (or the Cactus token's) joins the queue: its float-float mass will replace cm
+                const bool big = cm + ovl > p.k.tau || et >= 0;
+                const unsigned bm = __ballot_sync(0xffffffffu, big);
+                if (bm) {
+                    const int cnt = __popc(bm);
+                    if (nq + cnt > D_QCH) {
+                        loc = ff_add(loc, flush_chunks<E>(mode, s_qrt[warp], s_qro[warp], s_qcm[warp], s_qet[warp], nq, px,
+                                                          p.k, s_tab, gx, lane));
+                        nq = 0;
                     }
-                    const double tp = static_cast<double>(u) * warp_sum(all);
-                    emitted = scan_pick<E, AL>(c, trow, trow, 2, 0, V, po, tok, ht, tp, 0.0, lane);
-                } else {
-                    const FF tp = ff_mulf(Z, u);
-                    // first piece whose prefix exceeds tp (else the last piece with mass)
-                    int found = -1, lastp = -1;
-                    FF before_found = {0.f, 0.f}, before_last = {0.f, 0.f};
-                    FF run = excl;
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int t = lo + k;
-                        if (t < hi) {
-                            const FF m = tv[k];
-                            const FF pre = ff_add(run, m);
-                            if (m.hi > 0.f) {
-                                lastp = t;
-                                before_last = run;
-                                if (found < 0 && ff_gt(pre, tp)) {
-                                    found = t;
-                                    before_found = run;
-                                }
-                            }
-                            run = pre;
-                        }
+                    if (big) {
+                        const int at = nq + __popc(bm & ((1u << lane) - 1u));
+                        s_qrt[warp][at] = rt[q];
+                        s_qro[warp][at] = ro[q];
+                        s_qcm[warp][at] = cm;
+                        s_qet[warp][at] = et;
                     }
-                    const unsigned hit = __ballot_sync(0xffffffffu, found >= 0);
-                    int ft;
-                    FF before_piece;
-                    if (hit) {
-                        const int ln = __ffs(hit) - 1;
-                        ft = __shfl_sync(0xffffffffu, found, ln);
-                        before_piece = ff_shfl(before_found, ln);
-                    } else {
-                        const unsigned any = __ballot_sync(0xffffffffu, lastp >= 0);
-                        const int ln = any ? 31 - __clz(any) : 0;
-                        ft = __shfl_sync(0xffffffffu, lastp, ln);
-                        before_piece = ff_shfl(before_last, ln);
-                    }
-                    if (ft >= 0)
-                        emitted = pick_in_piece<E, AL>(d_cm + (ft / cps) * D_CPP, static_cast<uint32_t>(ft % cps), rank,
-                                                       trow, orow, mode, ft * PE, V, c, po, tok, ht, tp,
-                                                       before_piece, lane);
+                    nq += cnt;
                 }
             }
+            if (nq)
+                loc = ff_add(loc, flush_chunks<E>(mode, s_qrt[warp], s_qro[warp], s_qcm[warp], s_qet[warp], nq, px, p.k,
+                                                  s_tab, gx, lane));
+            const FF m = warp_sum(loc);
+            // the piece mass goes straight to CTA 0, which makes the draw
+            if (lane == 0) st_cta0_f32x2(&s_tiles[pc], rank, m.hi, m.lo);
+        }
+        cluster_sync_all();   // every CTA's masses are in place and visible to the cluster
+        if (rank == 0) {
+            if (warp == 0 && !idle) {
+                // piece masses in vocabulary order (np <= 4 * 32: lane l owns pieces seg l .. seg l + seg - 1)
+                const int seg = (np + 31) / 32;
+                const int lo = min(np, lane * seg), hi = min(np, lo + seg);
+                FF tv[4];
+                FF local = {0.f, 0.f};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int t = lo + k;
+                    tv[k] = t < hi ? FF{s_tiles[t].x, s_tiles[t].y} : FF{0.f, 0.f};
+                    local = ff_add(local, tv[k]);
+                }
+                const FF incl = warp_incl_scan_ff(local, lane);
+                FF excl = ff_shfl_up(incl, 1);
+                if (lane == 0) excl = FF{0.f, 0.f};
+                const FF Z = ff_shfl(incl, 31);
+                if (p.diag && j < K && lane == 0) p.diag[(static_cast<size_t>(b) * K + j) * 4 + 2] = Z.hi + Z.lo;
+                if (j == L) {
+                    const float u = philox_uniform(seed, static_cast<uint32_t>(b), static_cast<uint32_t>(L), 1u);
+                    PickPlan plan = {};
+                    plan.ft = -1;
+                    if (mode == 1 && !(Z.hi > 0.f)) {
+                        // the residual rounded to zero mass: draw from h over the whole row instead
+                        const float ht = s_ht[j];
+                        const int tk = s_tok[j];
+                        double all = 0.0;
+                        for (int e0 = lane * CHUNK; e0 < V; e0 += 32 * CHUNK) {
+                            const Raw rt = E::template gload<AL>(trow, e0, V);
+                            float2 unused = make_float2(0.f, 0.f);
+                            const int et = (tk >= e0 && tk < e0 + CHUNK) ? tk - e0 : -1;
+                            all += static_cast<double>(chunk_mass_patched<E>(2, rt, rt, c, po, et, ht, unused));
+                        }
+                        const double tpd = static_cast<double>(u) * warp_sum(all);
+                        emitted = scan_pick<E, AL>(c, trow, trow, 2, 0, V, po, tk, ht, tpd, 0.0, lane);
+                        plan.ft = -2;
+                    } else {
+                        const FF tp = ff_mulf(Z, u);
+                        // first piece whose prefix exceeds tp (else the last piece with mass)
+                        int found = -1, lastp = -1;
+                        FF before_found = {0.f, 0.f}, before_last = {0.f, 0.f};
+                        FF run = excl;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int t = lo + k;
+                            if (t < hi) {
+                                const FF mm = tv[k];
+                                const FF pre = ff_add(run, mm);
+                                if (mm.hi > 0.f) {
+                                    lastp = t;
+                                    before_last = run;
+                                    if (found < 0 && ff_gt(pre, tp)) {
+                                        found = t;
+                                        before_found = run;
+                                    }
+                                }
+                                run = pre;
+                            }
+                        }
+                        const unsigned hit = __ballot_sync(0xffffffffu, found >= 0);
+                        if (hit) {
+                            const int ln = __ffs(hit) - 1;
+                            plan.ft = __shfl_sync(0xffffffffu, found, ln);
+                            plan.before = ff_shfl(before_found, ln);
+                        } else {
+                            const unsigned any = __ballot_sync(0xffffffffu, lastp >= 0);
+                            const int ln = any ? 31 - __clz(any) : 0;
+                            plan.ft = __shfl_sync(0xffffffffu, lastp, ln);
+                            plan.before = ff_shfl(before_last, ln);
+                        }
+                        plan.tp = tp;
+                    }
+                    if (lane == 0) {
+                        s_plan = plan;
+                        s_emit = emitted;
+                    }
+                }
+            }
+            __syncthreads();   // CTA 0: the plan is in place
+            if (j == L && !idle && s_plan.ft >= 0) {
+                // ---- the pick inside piece ft: one thread a chunk, the chunks' masses scanned across the CTA in
+                // vocabulary order, then the elements of the chunk holding u * Z ----
+                const PickPlan plan = s_plan;
+                const int ft = plan.ft;
+                const int nch = (min(PE, V - ft * PE) + CHUNK - 1) / CHUNK;
+                const int ch = threadIdx.x;   // chunk of the piece (D_CPP = 256 <= DNT)
+                const int e0 = ft * PE + ch * CHUNK;
+                const int et = (tok >= e0 && tok < e0 + CHUNK) ? tok - e0 : -1;
+                float v[8];   // the chunk's fast residual per element
+                FF m = {0.f, 0.f};
+                bool big = false;
+                Raw rt = E::ninf(), ro = E::ninf();
+                if (threadIdx.x == 0) s_pn = 0;
+                __syncthreads();
+                if (ch < nch) {
+                    rt = E::template gload<AL>(trow, e0, V);
+                    ro = mode == 1 ? E::template gload<AL>(orow, e0, V) : rt;
+                    float ovl, unused = 0.f;
+                    const float cm = fast_chunk<E>(mode, rt, ro, c, po, et, hpatch, ovl);
+                    chunk_values<E>(mode, rt, ro, c, po, et, hpatch, v, unused);
+                    m = FF{cm, 0.f};
+                    big = cm + ovl > p.k.tau || et >= 0;
+                    if (big) s_pl[atomicAdd(&s_pn, 1)] = ch;
+                }
+                __syncthreads();
+                // the piece's large chunks at float-float precision, eight threads to a chunk
+                {
+                    const int npl = s_pn;
+                    for (int base = 0; base < npl; base += DNT / 8) {
+                        const int li = base + threadIdx.x / 8, e = threadIdx.x & 7;
+                        FF r = {0.f, 0.f};
+                        if (li < npl) {
+                            const int cj = s_pl[li];
+                            const int c0 = ft * PE + cj * CHUNK;
+                            const Raw xt = E::template gload<AL>(trow, c0, V);
+                            const Raw xd = mode == 1 ? E::template gload<AL>(orow, c0, V) : xt;
+                            const float2 xt2 = E::pair(xt, e >> 1), xd2 = E::pair(xd, e >> 1);
+                            const int cet = (tok >= c0 && tok < c0 + CHUNK) ? tok - c0 : -1;
+                            r = elem_exact(mode, (e & 1) ? xt2.y : xt2.x, (e & 1) ? xd2.y : xd2.x, px, p.k, s_tab, e == cet, gx);
+                            s_pr[li][e] = make_float2(r.hi, r.lo);
+                        }
+                        const FF sum = group8_sum(r);
+                        if (li < npl && e == 0) s_pm[s_pl[li]] = make_float2(sum.hi, sum.lo);
+                    }
+                }
+                __syncthreads();
+                if (big) m = FF{s_pm[ch].x, s_pm[ch].y};
+                // CTA-wide scan of the chunk masses (warps in order)
+                const FF incl = warp_incl_scan_ff(m, lane);
+                if (lane == 31) s_wscan[warp] = make_float2(incl.hi, incl.lo);
+                __syncthreads();
+                FF start = plan.before;
+                for (int w = 0; w < warp; ++w) start = ff_add(start, FF{s_wscan[w].x, s_wscan[w].y});
+                FF excl = ff_shfl_up(incl, 1);
+                if (lane == 0) excl = FF{0.f, 0.f};
+                start = ff_add(start, excl);
+                const FF end = ff_add(start, m);
+                const bool pos = ch < nch && m.hi > 0.f;
+                const unsigned over = __ballot_sync(0xffffffffu, pos && ff_gt(end, plan.tp));
+                const unsigned posm = __ballot_sync(0xffffffffu, pos);
+                if (lane == 0) {
+                    s_wfirst[warp] = over ? warp * 32 + __ffs(over) - 1 : 0x7fffffff;
+                    s_wlast[warp] = posm ? warp * 32 + 31 - __clz(posm) : -1;
+                }
+                __syncthreads();
+                int first = 0x7fffffff, last = -1;
+                for (int w = 0; w < DW; ++w) {
+                    first = min(first, s_wfirst[w]);
+                    last = max(last, s_wlast[w]);
+                }
+                const int chosen = first != 0x7fffffff ? first : last;
+                if (ch == chosen) {
+                    int li = -1;   // the chunk's place in the list of large chunks
+                    if (big)
+                        for (int t = 0; t < s_pn; ++t)
+                            if (s_pl[t] == ch) li = t;
+                    FF a = start;
+                    int pick = -1, lp = -1;
+                    for (int e = 0; e < 8; ++e) {
+                        const FF r = li >= 0 ? FF{s_pr[li][e].x, s_pr[li][e].y} : FF{v[e], 0.f};
+                        a = ff_add(a, r);
+                        if (r.hi > 0.f) {
+                            lp = e;
+                            if (pick < 0 && ff_gt(a, plan.tp)) pick = e;
+                        }
+                    }
+                    s_emit = pick >= 0 ? e0 + pick : (lp >= 0 ? e0 + lp : -1);
+                }
+                __syncthreads();
+            }
+            if (j == L && !idle) emitted = s_emit;
         }
         cluster_sync_all();   // CTA 0 has read the other CTAs' masses; the buffers may be rewritten or released
     }

@@ -597,23 +597,19 @@ __device__ __forceinline__ float nh_log_mean(float a0, float a1, bool v0, bool v
     return mx + logf(s / static_cast<float>(N));
 }
 
-__global__ void __launch_bounds__(32) normalhedge_kernel(float* __restrict__ regret, const float* __restrict__ loss,
-                                                         float* __restrict__ weights, int N) {
-    const int lane = threadIdx.x;
-    const bool v0 = lane < N, v1 = lane + 32 < N;
-    const float p0 = v0 ? weights[lane] : 0.f, p1 = v1 ? weights[lane + 32] : 0.f;
-    const float l0 = v0 ? loss[lane] : 0.f, l1 = v1 ? loss[lane + 32] : 0.f;
-    const float lp = warp_sum(p0 * l0 + p1 * l1);
-    const float r0 = v0 ? regret[lane] + (lp - l0) : 0.f;
-    const float r1 = v1 ? regret[lane + 32] + (lp - l1) : 0.f;
-    if (v0) regret[lane] = r0;
-    if (v1) regret[lane + 32] = r1;
+// One NormalHedge round on the registers of one warp: lane l holds experts l (valid v0) and l + 32 (v1), their
+// regrets r0, r1 and weights p0, p1; l0, l1 are this round's losses. Every lane ends with the new state.
+__device__ __forceinline__ void nh_round(int N, bool v0, bool v1, float l0, float l1, float& r0, float& r1,
+                                         float& p0, float& p1) {
+    const float lp = warp_sum((v0 ? p0 * l0 : 0.f) + (v1 ? p1 * l1 : 0.f));
+    r0 = v0 ? r0 + (lp - l0) : 0.f;
+    r1 = v1 ? r1 + (lp - l1) : 0.f;
     const float q0 = fmaxf(r0, 0.f), q1 = fmaxf(r1, 0.f);
     const float m = warp_max(fmaxf(q0, q1));
     if (!(m > 0.f)) {
         const float u = 1.f / static_cast<float>(N);
-        if (v0) weights[lane] = u;
-        if (v1) weights[lane + 32] = u;
+        p0 = v0 ? u : 0.f;
+        p1 = v1 ? u : 0.f;
         return;
     }
     const float lm2 = 2.f * logf(m);
@@ -630,9 +626,171 @@ __global__ void __launch_bounds__(32) normalhedge_kernel(float* __restrict__ reg
     const float w1 = (v1 && q1 > 0.f) ? logf(q1 / c) + q1 * q1 / (2.f * c) : NINF;
     const float mx = warp_max(fmaxf(w0, w1));
     const float e0 = w0 > NINF ? expf(w0 - mx) : 0.f, e1 = w1 > NINF ? expf(w1 - mx) : 0.f;
-    const float s = warp_sum(e0 + e1);
-    if (v0) weights[lane] = e0 / s;
-    if (v1) weights[lane + 32] = e1 / s;
+    const float sum = warp_sum(e0 + e1);
+    p0 = e0 / sum;
+    p1 = e1 / sum;
+}
+
+__global__ void __launch_bounds__(32) normalhedge_kernel(float* __restrict__ regret, const float* __restrict__ loss,
+                                                         float* __restrict__ weights, int N) {
+    const int lane = threadIdx.x;
+    const bool v0 = lane < N, v1 = lane + 32 < N;
+    float p0 = v0 ? weights[lane] : 0.f, p1 = v1 ? weights[lane + 32] : 0.f;
+    const float l0 = v0 ? loss[lane] : 0.f, l1 = v1 ? loss[lane + 32] : 0.f;
+    float r0 = v0 ? regret[lane] : 0.f, r1 = v1 ? regret[lane + 32] : 0.f;
+    nh_round(N, v0, v1, l0, l1, r0, r1, p0, p1);
+    if (v0) {
+        regret[lane] = r0;
+        weights[lane] = p0;
+    }
+    if (v1) {
+        regret[lane + 32] = r1;
+        weights[lane + 32] = p1;
+    }
+}
+
+// ------------------------------------------------------------------------------------------------
+// NormalHedge under delayed, censored feedback
+// ------------------------------------------------------------------------------------------------
+// "Not-a-Bandit ...", Key design 3: the accepted tokens of a round are revealed as one block when it ends,
+// the counterfactual feedback is censored unless the selected drafter fills the chunk, the loss is 1 - gamma or
+// the accept length still available up to K + 1, the delay is at most 2K, and the learner keeps a queue of
+// feedback and keeps applying the next available one (the stochastic-setting reduction of Joulani, Gyorgy,
+// Szepesvari, ICML 2013). Reading (one learner per sequence): round t reveals levels j < min(L_t + 1, K) of its
+// gamma [N, K], in level order, as the sequence's next feedback items; the later levels are censored and
+// skipped. Objective 0: item n's loss 1 - gamma is available at once. Objective 1: item n's loss is K + 1 minus
+// the accept-length estimate over items n .. n + K - 1, available once item n + K - 1 has arrived. Each push
+// applies every newly available loss, oldest first, as one NormalHedge round.
+//
+// State of one sequence (HF_HEAD bytes of header, then regrets and weights of up to 64 drafters, then a ring of
+// 2K items of N floats): at most 2K - 1 items wait at once (K - 1 left after a push, K new ones).
+constexpr int HF_HEAD = 32;
+constexpr unsigned HF_STATUS_BAD_LEN = 1u;   // an accepted length outside [0, K]: that round was skipped
+struct HfHead {
+    int count, head, applied, objective;
+    unsigned status;
+    int pad[3];
+};
+__host__ __device__ constexpr size_t hf_seq_bytes(int N, int K) {
+    return (static_cast<size_t>(HF_HEAD) + 2 * 64 * sizeof(float) + static_cast<size_t>(2 * K) * N * sizeof(float) + 15) /
+           16 * 16;
+}
+
+struct HfParams {
+    unsigned char* state;          // B sequences of hf_seq_bytes(N, K)
+    const float* gamma;            // [N, B, K] (push)
+    const int32_t* accept_len;     // [B] (push)
+    int N, B, K, objective;        // objective: init only
+    float* weights;                // [B, N] or null: the distribution for the next round
+    int32_t* applied;              // [B] or null: NormalHedge rounds applied so far
+};
+
+// One warp per sequence: regrets 0, uniform weights, empty queue.
+__global__ void __launch_bounds__(256) hedge_feedback_init_kernel(const HfParams p) {
+    const int lane = threadIdx.x & 31;
+    const int b = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (b >= p.B) return;
+    unsigned char* st = p.state + static_cast<size_t>(b) * hf_seq_bytes(p.N, p.K);
+    HfHead* h = reinterpret_cast<HfHead*>(st);
+    float* R = reinterpret_cast<float*>(st + HF_HEAD);
+    float* W = R + 64;
+    R[lane] = 0.f;
+    R[lane + 32] = 0.f;
+    W[lane] = lane < p.N ? 1.f / static_cast<float>(p.N) : 0.f;
+    W[lane + 32] = lane + 32 < p.N ? 1.f / static_cast<float>(p.N) : 0.f;
+    if (lane == 0) {
+        h->count = 0;
+        h->head = 0;
+        h->applied = 0;
+        h->objective = p.objective;
+        h->status = 0u;
+    }
+}
+
+// One warp per sequence: append the revealed levels of this round's gamma, then apply every available loss.
+__global__ void __launch_bounds__(256) hedge_feedback_push_kernel(const HfParams p) {
+    const int lane = threadIdx.x & 31;
+    const int b = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (b >= p.B) return;
+    const int N = p.N, K = p.K, cap = 2 * K;
+    unsigned char* st = p.state + static_cast<size_t>(b) * hf_seq_bytes(N, K);
+    HfHead* h = reinterpret_cast<HfHead*>(st);
+    float* R = reinterpret_cast<float*>(st + HF_HEAD);
+    float* W = R + 64;
+    float* ring = W + 64;
+    const bool v0 = lane < N, v1 = lane + 32 < N;
+    int count = h->count, head = h->head, applied = h->applied;
+    const int objective = h->objective;
+    const int L = __ldg(p.accept_len + b);
+    if (L < 0 || L > K) {
+        if (lane == 0) h->status |= HF_STATUS_BAD_LEN;
+    } else {
+        const int valid = min(L + 1, K);
+        for (int j = 0; j < valid; ++j) {
+            float* item = ring + static_cast<size_t>((head + count) % cap) * N;
+            if (v0) item[lane] = __ldg(p.gamma + (static_cast<size_t>(lane) * p.B + b) * K + j);
+            if (v1) item[lane + 32] = __ldg(p.gamma + (static_cast<size_t>(lane + 32) * p.B + b) * K + j);
+            ++count;
+        }
+        __syncwarp();
+    }
+    float r0 = v0 ? R[lane] : 0.f, r1 = v1 ? R[lane + 32] : 0.f;
+    float p0 = v0 ? W[lane] : 0.f, p1 = v1 ? W[lane + 32] : 0.f;
+    while (objective == 0 ? count >= 1 : count >= K) {
+        float l0, l1;
+        if (objective == 0) {
+            const float* item = ring + static_cast<size_t>(head) * N;
+            l0 = v0 ? 1.f - item[lane] : 0.f;
+            l1 = v1 ? 1.f - item[lane + 32] : 0.f;
+        } else {   // K + 1 minus the accept-length estimate 1 + sum_k prod_{j<=k} gamma_j over the window
+            float run0 = 1.f, tot0 = 1.f, run1 = 1.f, tot1 = 1.f;
+            for (int k = 0; k < K; ++k) {
+                const float* item = ring + static_cast<size_t>((head + k) % cap) * N;
+                if (v0) {
+                    run0 *= item[lane];
+                    tot0 += run0;
+                }
+                if (v1) {
+                    run1 *= item[lane + 32];
+                    tot1 += run1;
+                }
+            }
+            l0 = v0 ? static_cast<float>(K + 1) - tot0 : 0.f;
+            l1 = v1 ? static_cast<float>(K + 1) - tot1 : 0.f;
+        }
+        nh_round(N, v0, v1, l0, l1, r0, r1, p0, p1);
+        head = (head + 1) % cap;
+        --count;
+        ++applied;
+    }
+    if (v0) {
+        R[lane] = r0;
+        W[lane] = p0;
+        if (p.weights) p.weights[static_cast<size_t>(b) * N + lane] = p0;
+    }
+    if (v1) {
+        R[lane + 32] = r1;
+        W[lane + 32] = p1;
+        if (p.weights) p.weights[static_cast<size_t>(b) * N + lane + 32] = p1;
+    }
+    if (lane == 0) {
+        h->count = count;
+        h->head = head;
+        h->applied = applied;
+        if (p.applied) p.applied[b] = applied;
+    }
+}
+
+// Test hook: the draw's float-float exponent and exp2 on n inputs (d = x - M, row offset l as a pair).
+__global__ void __launch_bounds__(256) ff_exp2_probe_kernel(const float* __restrict__ d, const float* __restrict__ l_hi,
+                                                            const float* __restrict__ l_lo, float* __restrict__ out,
+                                                            int n, const FFc k) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const FF e = ff_exponent(d[i], k, l_hi[i], l_lo[i]);
+    const FF y = ff_exp2(e, k, k.tab);
+    out[2 * i] = y.hi;
+    out[2 * i + 1] = y.lo;
 }
 
 }  // namespace specv

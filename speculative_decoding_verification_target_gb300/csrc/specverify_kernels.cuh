@@ -191,12 +191,13 @@ __device__ __forceinline__ float beta_of(MaxSum g, float c) { return -fmaf(g.m, 
 
 // Cactus closed form on q = p_target(t): gamma* = min(q + sqrt(2 delta q (1 - q)), 1) and the log2 of the
 // scale (1 - gamma*) / (1 - q) applied to every other token (-inf when q = 1).
-__device__ __forceinline__ void cactus_scalars(float q, float delta, float& gstar, float& log2s) {
+__device__ __forceinline__ void cactus_scalars(float q, float delta, float& gstar, float& log2s, float& scale) {
     float gs = q + sqrtf(2.f * delta * q * (1.f - q));
     gs = fminf(gs, 1.f);
     const float s = q < 1.f ? __fdiv_rn(1.f - gs, 1.f - q) : 0.f;
     gstar = gs;
     log2s = log2f(s);
+    scale = s;
 }
 
 // The same scalars with gamma* the root of the divergence constraint instead of its Taylor closed form
@@ -210,7 +211,7 @@ __device__ __forceinline__ float cactus_kl_f(float q, float g) {
     const float b = g < 1.f ? (1.f - g) * logf((1.f - g) / (1.f - q)) : 0.f;
     return a + b;
 }
-__device__ __forceinline__ void cactus_scalars_kl(float q, float delta, float& gstar, float& log2s) {
+__device__ __forceinline__ float cactus_root_kl(float q, float delta) {
     float gs;
     if (!(delta > 0.f) || !(q > 0.f)) {
         gs = q;
@@ -234,9 +235,14 @@ __device__ __forceinline__ void cactus_scalars_kl(float q, float delta, float& g
         }
         gs = g;
     }
+    return gs;
+}
+__device__ __noinline__ void cactus_scalars_kl(float q, float delta, float& gstar, float& log2s, float& scale) {
+    const float gs = cactus_root_kl(q, delta);
     const float s = q < 1.f ? __fdiv_rn(1.f - gs, 1.f - q) : 0.f;
     gstar = gs;
     log2s = log2f(s);
+    scale = s;
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -333,6 +339,150 @@ __device__ __forceinline__ float chunk_mass_patched(int mode, const typename E::
     return m;
 }
 
+// ------------------------------------------------------------------------------------------------
+// the residual draw at float-float precision
+// ------------------------------------------------------------------------------------------------
+// The draw compares a running sum of residual masses with u * Z, so every error it makes moves a CDF
+// boundary. The fast per-element arithmetic above rounds the exponent (x - M) c + L (a few 1e-7 of the element
+// for exponents of 8 to 32) and its SFU exp2 adds about 1e-7. Summed over a row these errors are a few 1e-9
+// of mass, and most of it comes from the few largest elements (an emulation of that arithmetic on rows of the
+// Llama-3 workload: a median error of 3.9e-9 at the drawn boundary, 1.6e-9 once the elements above 1e-2 are
+// exact). So the draw recomputes, at float-float precision (about 44 bits: the exponent as a float-float
+// with c = log2(e) / T and L as float pairs, and a float-float exp2), every chunk whose fast mass (residual
+// plus overlap) exceeds a threshold, and corrects its piece's mass by the difference. The large chunks of a
+// warp wait in a queue and are evaluated eight lanes to a chunk (one lane alone would run each element's long
+// chain of dependent float-float steps one after another). Cactus: gamma* and the scale s of the other tokens
+// come from the float-float p_T(n) (the Taylor form in float-float, the divergence root refined by one
+// float-float Newton step); the token's chunk always takes the exact path.
+// Host-computed constants of the float-float arithmetic (double precision, split into float pairs).
+struct FFc {
+    float2 tab[33];          // 2^(k / 32), k = -16 .. 16
+    float ln2_hi, ln2_lo;    // ln 2
+    float c_hi, c_lo;        // log2(e) / T, c_hi rounded towards zero (c_lo > 0)
+    float tau;               // a chunk whose fast mass (residual plus overlap) exceeds this is recomputed exactly
+};
+
+// (x - M) c + L as a float-float, with d = x - M given as the float-float d_hi + d_lo (d_lo = 0 for bf16 logits,
+// whose difference is exact in float): the product's rounding error by a fused multiply-add, the sum's by
+// TwoSum.
+__device__ __forceinline__ FF ff_exponent(float d, const FFc& k, float l_hi, float l_lo, float d_lo = 0.f) {
+    const float p1 = __fmul_rn(d, k.c_hi);
+    const float e1 = __fmaf_rn(d, k.c_hi, -p1);
+    const FF s = ff_two_sum(p1, l_hi);
+    const float small = __fmaf_rn(d_lo, k.c_hi, __fmaf_rn(d, k.c_lo, l_lo));
+    return ff_fast_two_sum(s.hi, __fadd_rn(s.lo, __fadd_rn(e1, small)));
+}
+
+// 2^e for a float-float e (0 below 2^-125; tab = k.tab, or a copy of it in shared memory, where lanes that look
+// up different entries do not serialise): e.hi = n + j/32 + g with n and j integers and
+// |g| <= 1/64 (all exact in float), 2^(j/32) from the table, 2^(g + e.lo) = exp(q) with q = (g + e.lo) ln 2
+// as a float-float and the Taylor series of exp to q^5 / 5! (|q| < 0.011: the next term is below 3e-15).
+__device__ __forceinline__ FF ff_exp2(FF e, const FFc& k, const float2* tab) {
+    if (!(e.hi > -125.f)) return {0.f, 0.f};
+    const float n = rintf(e.hi);
+    const float f = __fsub_rn(e.hi, n);
+    const float jf = rintf(__fmul_rn(f, 32.f));
+    const float g = __fmaf_rn(jf, -0.03125f, f);
+    const float qh = __fmul_rn(g, k.ln2_hi);
+    const float ql = __fadd_rn(__fmaf_rn(g, k.ln2_hi, -qh), __fmaf_rn(g, k.ln2_lo, __fmul_rn(e.lo, k.ln2_hi)));
+    // exp(qh) = 1 + qh + qh^2 / 2 + qh^2 t with t = qh / 6 + qh^2 / 24 + qh^3 / 120; qh^2 exactly as a pair
+    float t = __fmaf_rn(qh, 1.f / 120.f, 1.f / 24.f);
+    t = __fmul_rn(qh, __fmaf_rn(qh, t, 1.f / 6.f));
+    const FF q2 = ff_two_prod(qh, qh);
+    const float tail_r = __fmaf_rn(q2.hi, t, __fmul_rn(0.5f, q2.lo));
+    FF one_q = ff_fast_two_sum(1.f, qh);
+    const FF with_sq = ff_fast_two_sum(one_q.hi, __fmul_rn(0.5f, q2.hi));
+    // exp(qh + ql) = exp(qh) (1 + ql), to first order in ql
+    const float lo = __fadd_rn(__fadd_rn(one_q.lo, with_sq.lo), __fmaf_rn(ql, with_sq.hi, tail_r));
+    one_q.hi = with_sq.hi;
+    const float2 T = tab[static_cast<int>(jf) + 16];
+    const float ph = __fmul_rn(one_q.hi, T.x);
+    const float pl = __fadd_rn(__fmaf_rn(one_q.hi, T.x, -ph), __fmaf_rn(one_q.hi, T.y, __fmaf_rn(lo, T.x, __fmul_rn(lo, T.y))));
+    const FF r = ff_fast_two_sum(ph, pl);
+    const float sc = __int_as_float((static_cast<int>(n) + 127) << 23);   // 2^n, exact for n >= -125
+    return {__fmul_rn(r.hi, sc), __fmul_rn(r.lo, sc)};
+}
+
+// log2 of a float-float x > 0: the float log2 and one Newton step on 2^y = x, y = y0 + (x 2^-y0 - 1) / ln 2
+// (the residual x 2^-y0 - 1 is about 1e-7, so the step leaves an error of order 1e-14).
+__device__ __noinline__ FF ff_log2(FF x, const FFc& k) {
+    const float y0 = log2f(x.hi);
+    const FF r = ff_sub(ff_mul(x, ff_exp2(FF{-y0, 0.f}, k, k.tab)), FF{1.f, 0.f});
+    // (r.hi + r.lo) / ln 2 with 1 / ln 2 = log2(e) = c_hi * T for T = 1 is not available here: divide by ln 2
+    const float inv_ln2 = __fdiv_rn(1.f, k.ln2_hi);
+    return ff_fast_two_sum(y0, __fmul_rn(__fadd_rn(r.hi, r.lo), inv_ln2));
+}
+// natural log of a float-float x > 0 (log2 x times ln 2)
+__device__ __forceinline__ FF ff_log(FF x, const FFc& k) { return ff_mul(ff_log2(x, k), FF{k.ln2_hi, k.ln2_lo}); }
+
+// gamma* at float-float precision from a float-float q = p_target(n): the Taylor closed form min(q +
+// sqrt(2 delta q (1 - q)), 1) in float-float, or (kl) the float root of the divergence constraint refined by
+// one Newton step in float-float (the float root is within about 1e-7 of the root, so one step leaves an error
+// of order 1e-14).
+__device__ __noinline__ FF cactus_gamma_ff(FF q, float delta, bool kl, const FFc& k) {
+    if (!(delta > 0.f) || !(q.hi > 0.f)) return q;
+    const FF one = {1.f, 0.f};
+    if (!kl) {
+        const FF root = ff_sqrt(ff_mulf(ff_mul(q, ff_sub(one, q)), 2.f * delta));
+        const FF g = ff_add(q, root);
+        return ff_gt(g, one) ? one : g;
+    }
+    if (!(q.hi < 1.f)) return one;
+    const float g0 = cactus_root_kl(q.hi, delta);
+    if (!(g0 < 1.f) || !(g0 > q.hi)) return FF{g0, 0.f};
+    const FF g = {g0, 0.f};
+    const FF a = ff_log(ff_div(g, q), k);                          // ln(g / q)
+    const FF b = ff_log(ff_div(ff_sub(one, g), ff_sub(one, q)), k);  // ln((1 - g) / (1 - q))
+    const FF f = ff_sub(ff_add(ff_mul(g, a), ff_mul(ff_sub(one, g), b)), FF{delta, 0.f});
+    const FF d = ff_sub(a, b);
+    if (!(d.hi > 0.f)) return g;
+    const FF gn = ff_sub(g, ff_div(f, d));
+    return (gn.hi > q.hi && gn.hi < 1.f) ? gn : g;
+}
+
+// Offsets of the row pair a draw is exactly recomputed from: target row (nmt = -M_T, L_T = -log2 S_T as
+// lt + lt_lo, and the Cactus scale s of h = s p^_T; 1 otherwise), draft row (nmo = -M_D, lo + lo_lo).
+struct PairOffX {
+    float nmt, lt, lt_lo, s, nmo, lo, lo_lo;
+};
+
+// One element of a row pair at float-float precision. mode 1: the residual r = (h - p_D)+ with h = s p^_T, or
+// h = g for the Cactus token (tok); mode 2: the bonus row, r = p^_T. xt, xd: the element's logits. The exponent
+// (x - M) c + L is a float-float (c = c_hi + c_lo, L = lt + lt_lo; x - M as a float-float, exact for bf16
+// logits) and so is its exp2. The draw evaluates this for every element of its few large chunks, eight lanes
+// to a chunk, and replaces the chunk's fast mass by their sum.
+__device__ __noinline__ FF elem_exact(int mode, float xt, float xd, const PairOffX& po, const FFc& k,
+                                         const float2* tab, bool tok, FF g) {
+    const float NINF = __uint_as_float(0xFF800000u);
+    FF h;
+    if (tok) {
+        h = g;
+    } else {
+        FF pt = {0.f, 0.f};
+        if (xt > NINF) {
+            const FF dt = ff_two_sum(xt, po.nmt);
+            pt = ff_exp2(ff_exponent(dt.hi, k, po.lt, po.lt_lo, dt.lo), k, tab);
+        }
+        h = ff_mulf(pt, po.s);
+    }
+    if (mode != 1) return h;
+    FF q = {0.f, 0.f};
+    if (xd > NINF) {
+        const FF dd = ff_two_sum(xd, po.nmo);
+        q = ff_exp2(ff_exponent(dd.hi, k, po.lo, po.lo_lo, dd.lo), k, tab);
+    }
+    return ff_gt(h, q) ? ff_sub(h, q) : FF{0.f, 0.f};
+}
+
+// Sum of a float-float over aligned groups of 8 lanes (fixed association: every lane of a group gets the
+// same value).
+__device__ __forceinline__ FF group8_sum(FF v) {
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1)
+        v = ff_add(v, FF{__shfl_xor_sync(0xffffffffu, v.hi, o), __shfl_xor_sync(0xffffffffu, v.lo, o)});
+    return v;
+}
+
 // Inclusive scan across the warp (Hillis-Steele, fixed association order).
 template <class T>
 __device__ __forceinline__ T warp_incl_scan(T v, int lane) {
@@ -397,7 +547,7 @@ __device__ __forceinline__ void piece_stats(const typename E::Raw (&r)[PCH], flo
 // inverse CDF
 // ------------------------------------------------------------------------------------------------
 template <class E, bool AL>
-__device__ int scan_pick(float c, const unsigned char* trow, const unsigned char* orow, int mode, int e_begin,
+__device__ __noinline__ int scan_pick(float c, const unsigned char* trow, const unsigned char* orow, int mode, int e_begin,
                          int e_end, PairOff o, int tok, float ht, double tp, double before, int lane) {
     using Raw = typename E::Raw;
     int last_pos = -1;

@@ -8,6 +8,7 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "specverify.h")
+INTERNAL = os.path.join(ROOT, "speculative_decoding_verification_target_gb300", "csrc", "specverify_internal.h")
 
 
 @pytest.fixture(scope="module")
@@ -18,10 +19,10 @@ def lib():
     return sv.load()
 
 
-def declared_functions():
-    text = open(HEADER).read()
+def declared_functions(path=HEADER):
+    text = open(path).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(spec_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(spec_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_three_calls():
@@ -37,6 +38,16 @@ def test_every_declared_symbol_is_exported(lib):
     for n in names:
         assert hasattr(lib, n), n
     assert set(sv.EXPORTS) == set(names)
+
+
+def test_test_hooks_are_outside_the_abi(lib):
+    """The tuning hooks live in an internal header: exported, but not declared by the C ABI header."""
+    import speculative_decoding_verification_target_gb300 as sv
+    hooks = declared_functions(INTERNAL)
+    assert set(hooks) == set(sv.TEST_HOOKS)
+    assert not set(hooks) & set(declared_functions())
+    for n in hooks:
+        assert hasattr(lib, n), n
 
 
 def test_workspace_size(lib):

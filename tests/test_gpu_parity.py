@@ -487,15 +487,14 @@ def test_counterfactual_without_diag_matches():
 # ------------------------------------------------------------------------------------------------
 @pytest.mark.parametrize("name,delta", [
     ("sps_llama3_b64_k5", None), ("hedgespec_n7_b32_k5", None), ("hedgespec_n21_b256_k8", None),
-    ("cactus_qwen_b128_m20", 0.0), ("cactus_qwen_b128_m20", 1.0),
-    pytest.param("cactus_qwen_b128_m20", 0.75, marks=pytest.mark.xfail(
-        strict=False, reason="one draw in 2560 positions (0.04%) lands 5.8e-9 of mass from a CDF boundary, "
-                             "below what fp32 element masses resolve")),
+    ("cactus_qwen_b128_m20", 0.0), ("cactus_qwen_b128_m20", 0.75), ("cactus_qwen_b128_m20", 1.0),
 ])
 def test_full_batch_near_ties(name, delta):
-    """Every sequence of the workload against the oracle: tokens and accept lengths bit-exact except at
-    near ties, which must stay under 0.01% of positions. The counterfactual workloads check both the plain
-    verify of the selected drafter and the chain fused into the gamma call."""
+    """Every sequence of the workload's base batch against the oracle, with and without diag: tokens and
+    accept lengths bit-exact except at near ties, which are counted here; their rate (under 0.01% of
+    positions) is asserted over many batches in test_gpu_near_ties.py, since one batch of 2560 positions
+    cannot resolve it. The counterfactual workloads check both the plain verify of the selected drafter and
+    the chain fused into the gamma call."""
     w = workloads.WORKLOADS[name]
     inp = workloads.make(w, device="cuda")
     draft = inp["drafters"][w.selected].contiguous() if w.N > 1 else inp["draft"]
@@ -511,14 +510,15 @@ def test_full_batch_near_ties(name, delta):
         lean = sv.cactus_verify(inp["target"], draft, inp["tokens"], inp["seeds"], delta, w.temperature,
                                 want_diag=False)
     torch.cuda.synchronize()
-    assert_chain(out, ref, w.K)
+    assert_diag(out, ref)
+    assert_chain(out, ref, w.K, rate=False)
     # the launch the benchmark times (no diag: one draw pass over the row pair of each sequence's draw)
-    assert_chain(lean, ref, w.K)
+    assert_chain(lean, ref, w.K, rate=False)
     if w.N > 1:
         fused = sv.counterfactual_gamma(inp["target"], inp["drafters"], w.temperature, w.selected, inp["tokens"],
                                         inp["seeds"], want_diag=False)
         torch.cuda.synchronize()
-        assert_chain(fused, ref, w.K)
+        assert_chain(fused, ref, w.K, rate=False)
 
 
 # ------------------------------------------------------------------------------------------------
@@ -675,3 +675,82 @@ def test_verify_filtered_without_filters_is_verify():
     torch.cuda.synchronize()
     for k in ("accept_len", "out_tokens", "diag"):
         assert torch.equal(a[k], f[k])
+
+
+# ------------------------------------------------------------------------------------------------
+# the residual draw's float-float exp2 (its large elements), against fp64
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("T", [1.0, 0.7, 2.3])
+def test_ff_exp2_building_block(T):
+    import ctypes
+    rng = np.random.default_rng(7)
+    n = 1 << 16
+    # d = x - M of bf16 logits (exact in float), row offsets l = -log2 S as a float pair
+    x = torch.tensor(rng.normal(0, 4, n), dtype=torch.float32).to(torch.bfloat16).float()
+    M = torch.tensor(rng.normal(8, 2, n), dtype=torch.float32).to(torch.bfloat16).float()
+    d = torch.minimum(x - M, torch.zeros(n))
+    l64 = -np.log2(rng.uniform(1.0, 50.0, n))
+    l_hi = torch.tensor(l64, dtype=torch.float32)
+    l_lo = torch.tensor(l64 - l_hi.double().numpy(), dtype=torch.float32)
+    dd, lh, ll = d.cuda(), l_hi.cuda(), l_lo.cuda()
+    out = torch.empty(2 * n, dtype=torch.float32, device="cuda")
+    lib = sv.load()
+    P = ctypes.c_void_p
+    rc = lib.spec_debug_exp2ff(P(dd.data_ptr()), P(lh.data_ptr()), P(ll.data_ptr()), P(out.data_ptr()), n,
+                               ctypes.c_float(T), P(torch.cuda.current_stream().cuda_stream))
+    assert rc == 0
+    torch.cuda.synchronize()
+    o = out.cpu().double().numpy().reshape(n, 2)
+    got = o[:, 0] + o[:, 1]
+    c = 1.0 / (np.log(2.0) * float(np.float32(T)))   # the temperature as the C ABI receives it
+    exact = np.exp2(d.double().numpy() * c + l_hi.double().numpy() + l_lo.double().numpy())
+    keep = exact > 1e-30
+    rel = np.abs(got[keep] - exact[keep]) / exact[keep]
+    assert rel.max() < 1e-10, rel.max()
+
+
+# ------------------------------------------------------------------------------------------------
+# NormalHedge under delayed, censored feedback (one learner per sequence), against the oracle
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("N,B,K,objective", [(3, 5, 5, 0), (21, 8, 8, 0), (7, 4, 5, 1), (64, 3, 8, 1), (2, 6, 1, 1)])
+def test_hedge_feedback_queue(N, B, K, objective):
+    rng = np.random.default_rng(300 + N + K)
+    T = 80
+    gamma = rng.uniform(0.05, 0.95, (T, N, B, K))
+    gamma[:, N // 2] = np.minimum(gamma[:, N // 2] + 0.1, 1.0)   # one drafter better on average
+    L = rng.integers(0, K + 1, (T, B)).astype(np.int32)
+    w_ref, a_ref = oracle.hedge_feedback(gamma, L, objective)
+    hf = sv.HedgeFeedback(N, B, K, objective)
+    worst = 0.0
+    for t in range(T):
+        g = torch.tensor(gamma[t], dtype=torch.float32, device="cuda")
+        w = hf.push(g, torch.tensor(L[t], device="cuda"))
+        torch.cuda.synchronize()
+        assert np.array_equal(hf.applied.cpu().numpy(), a_ref[t])
+        worst = max(worst, float(np.abs(w.cpu().numpy() - w_ref[t]).max()))
+    assert worst <= 2e-3, worst
+    assert np.all(hf.status().numpy() == 0)
+
+
+def test_hedge_feedback_bad_length_skips_the_round():
+    """An accepted length outside [0, K] skips that sequence's round and sets its status bit; the other
+    sequences are unaffected."""
+    N, B, K, T = 4, 3, 4, 12
+    rng = np.random.default_rng(310)
+    gamma = rng.uniform(0.1, 0.9, (T, N, B, K))
+    L = rng.integers(0, K + 1, (T, B)).astype(np.int32)
+    hf = sv.HedgeFeedback(N, B, K, 0)
+    for t in range(T):
+        Lt = L[t].copy()
+        if t == 5:
+            Lt[1] = K + 3
+        hf.push(torch.tensor(gamma[t], dtype=torch.float32, device="cuda"), torch.tensor(Lt, device="cuda"))
+    torch.cuda.synchronize()
+    keep = [t for t in range(T) if t != 5]
+    w_ref, a_ref = oracle.hedge_feedback(gamma, L, 0)
+    w_skip, a_skip = oracle.hedge_feedback(gamma[keep][:, :, 1:2], L[keep][:, 1:2], 0)
+    st = hf.status().numpy()
+    assert st[1] == 1 and st[0] == 0 and st[2] == 0
+    assert hf.applied.cpu().numpy()[1] == a_skip[-1, 0]
+    assert np.abs(hf.weights.cpu().numpy()[1] - w_skip[-1, 0]).max() <= 2e-3
+    assert np.abs(hf.weights.cpu().numpy()[[0, 2]] - w_ref[-1, [0, 2]]).max() <= 2e-3

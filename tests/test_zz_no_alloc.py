@@ -7,8 +7,10 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import speculative_decoding_verification_target_gb300 as sv
 import workloads
+from parity_util import assert_chain, assert_diag, host
 
 pytestmark = pytest.mark.gpu
 
@@ -62,3 +64,21 @@ def test_static_scratch_reports_bad_tokens_per_call():
     assert status == 1   # SPEC_STATUS_BAD_TOKEN for this call
     _, _, _, status = _static_call(lib, inp, w, stream)
     assert status == 0   # cleared by the next call
+
+
+def test_static_scratch_against_the_oracle():
+    """The static-scratch call checked directly against the fp64 oracle: an fp32 workload whose V is not a
+    multiple of 8 (rows not 16-byte aligned: element-wise loads), then a bf16 one, back to back."""
+    lib = sv.load()
+    stream = torch.cuda.current_stream()
+    for w in (workloads.WORKLOADS["tiny_sps_v1000"].scaled(B=6, V=1001),
+              workloads.WORKLOADS["sps_llama3_b64_k5"].scaled(B=8, gen_seed=77)):
+        inp = workloads.make(w, device="cuda")
+        ref = oracle.verify(host(inp["target"]), host(inp["draft"]), inp["tokens"].cpu().numpy(),
+                            inp["seeds"].cpu().numpy().astype(np.uint64), w.temperature)
+        acc, out, diag, status = _static_call(lib, inp, w, stream)
+        torch.cuda.synchronize()
+        assert status == 0
+        got = {"accept_len": acc, "out_tokens": out, "diag": diag}
+        assert_diag(got, ref)
+        assert_chain(got, ref, w.K)
