@@ -30,9 +30,6 @@ constexpr int MAX_V = 262144;
 constexpr int MAX_N = 64;
 constexpr size_t WS_HEADER = 256;          // status word + padding
 constexpr int SMEM_MAX_PER_CTA = 232448;   // opt-in maximum per CTA
-constexpr int DYN_SMEM_CEIL = SMEM_MAX_PER_CTA - 24576;   // dynamic ceiling of the gamma kernel (its static
-                                                          // shared memory stays below 24 KB)
-constexpr int DRAW_SMEM_CEIL = SMEM_MAX_PER_CTA - 65536;  // and of the draw kernel (static below 64 KB)
 
 int g_stats_grid_override = 0;   // CTAs of the statistics kernel (0 = automatic)
 float g_draw_tau = 0.f;          // chunk mass above which the draw takes its float-float path (0 = default)
@@ -136,18 +133,31 @@ std::mutex g_dsm_mu;
 struct DsmEntry {
     const void* fn;
     int device;
+    int cap;
 };
 DsmEntry g_dsm[32];
 int g_dsm_n = 0;
 
+// Raises a kernel's dynamic shared-memory limit to all that its static shared memory leaves of the per-CTA
+// maximum (once per kernel and device) and returns that limit in *cap.
 template <class Fn>
-cudaError_t draw_smem_ceiling(Fn fn, int dev, int ceiling) {
+cudaError_t dyn_smem_ceiling(Fn fn, int dev, int* cap) {
     std::lock_guard<std::mutex> lk(g_dsm_mu);
     for (int i = 0; i < g_dsm_n; ++i)
-        if (g_dsm[i].fn == reinterpret_cast<const void*>(fn) && g_dsm[i].device == dev) return cudaSuccess;
-    const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, ceiling);
-    if (e == cudaSuccess && g_dsm_n < 32) g_dsm[g_dsm_n++] = {reinterpret_cast<const void*>(fn), dev};
-    return e;
+        if (g_dsm[i].fn == reinterpret_cast<const void*>(fn) && g_dsm[i].device == dev) {
+            *cap = g_dsm[i].cap;
+            return cudaSuccess;
+        }
+    cudaFuncAttributes at = {};
+    cudaError_t e = cudaFuncGetAttributes(&at, fn);
+    if (e != cudaSuccess) return e;
+    const int c = SMEM_MAX_PER_CTA - static_cast<int>(at.sharedSizeBytes);
+    if (c <= 0) return cudaErrorInvalidValue;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, c);
+    if (e != cudaSuccess) return e;
+    if (g_dsm_n < 32) g_dsm[g_dsm_n++] = {reinterpret_cast<const void*>(fn), dev, c};
+    *cap = c;
+    return cudaSuccess;
 }
 
 // Constants of the draw's float-float arithmetic, from double precision: 2^(k/32) for k = -16..16, ln 2 and
@@ -211,14 +221,14 @@ spec_status launch_draw(const Call& a, bool aligned, const unsigned char* draft,
     d.cps = cps;
     // (bulk-copy mode) a two-piece slot and an mbarrier per warp, when they fit
     const size_t ring_bytes = static_cast<size_t>(DW) * (2 * static_cast<size_t>(PE) * eb + sizeof(uint64_t));
-    const size_t dsmem_cap = DRAW_SMEM_CEIL;   // the ceiling draw_smem_ceiling sets for it
-    d.tma = aligned && ring_bytes <= dsmem_cap ? 1 : 0;
-    const size_t dsmem = d.tma ? ring_bytes : 0;
     using DrawFn = void (*)(const DParams);
     DrawFn dfn = a.dtype == SPEC_BF16 ? (aligned ? draw_kernel<Bf16, true> : draw_kernel<Bf16, false>)
                                       : (aligned ? draw_kernel<F32, true> : draw_kernel<F32, false>);
-    e = draw_smem_ceiling(dfn, dev, DRAW_SMEM_CEIL);
+    int dsmem_cap = 0;
+    e = dyn_smem_ceiling(dfn, dev, &dsmem_cap);
     if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "draw kernel attribute failed: %s", cudaGetErrorString(e));
+    d.tma = aligned && ring_bytes <= static_cast<size_t>(dsmem_cap) ? 1 : 0;
+    const size_t dsmem = d.tma ? ring_bytes : 0;
     // its CTAs start as the grid before it frees SMs and wait for it (griddepcontrol.wait) after reading
     // their inputs
     cudaLaunchAttribute da[2];
@@ -410,7 +420,9 @@ spec_status run_gamma(const Call& a, bool aligned) {
     g.status = reinterpret_cast<unsigned*>(ws);
     using GammaFn = void (*)(const CgParams);
     GammaFn gfn = a.dtype == SPEC_BF16 ? gamma_kernel<Bf16> : gamma_kernel<F32>;
-    e = draw_smem_ceiling(gfn, dev, DYN_SMEM_CEIL);   // G_SMEM is below that ceiling
+    int gcap = 0;
+    e = dyn_smem_ceiling(gfn, dev, &gcap);
+    if (e == cudaSuccess && G_SMEM > static_cast<size_t>(gcap)) e = cudaErrorInvalidValue;
     if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "gamma kernel attribute failed: %s", cudaGetErrorString(e));
     g_last_plan[0] = 0;
     g_last_plan[1] = G_R;
@@ -446,19 +458,22 @@ spec_status run_filtered(const Call& a, int top_k, float top_p) {
     f.thr = reinterpret_cast<float*>(ws + fl.thr_off);
     f.out_a = ws + fl.ta_off;
     f.out_b = ws + fl.tb_off;
-    if (a.dtype == SPEC_BF16) threshold_kernel<Bf16><<<static_cast<unsigned>(f.rows_n), FT_NT, 0, a.stream>>>(f);
-    else threshold_kernel<F32><<<static_cast<unsigned>(f.rows_n), FT_NT, 0, a.stream>>>(f);
-    cudaError_t e = cudaGetLastError();
+    f.vec = (static_cast<size_t>(a.V) * eb) % 16 == 0 && reinterpret_cast<uintptr_t>(a.target) % 16 == 0 &&
+            reinterpret_cast<uintptr_t>(a.others) % 16 == 0 && reinterpret_cast<uintptr_t>(f.out_a) % 16 == 0 &&
+            reinterpret_cast<uintptr_t>(f.out_b) % 16 == 0;
+    using ThrFn = void (*)(const FParams);
+    ThrFn tfn = a.dtype == SPEC_BF16 ? threshold_kernel<Bf16> : threshold_kernel<F32>;
+    int dev = 0, tcap = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = dyn_smem_ceiling(tfn, dev, &tcap);
+    if (e == cudaSuccess && F_SMEM > static_cast<size_t>(tcap)) e = cudaErrorInvalidValue;
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "threshold kernel attribute failed: %s", cudaGetErrorString(e));
+    tfn<<<static_cast<unsigned>(f.rows_n), FT_NT, F_SMEM, a.stream>>>(f);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "threshold kernel launch failed: %s", cudaGetErrorString(e));
-    // grid-stride copy: up to 64 CTAs of 256 threads per SM
-    int dev = 0, sms = 0;
-    e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "device query failed: %s", cudaGetErrorString(e));
-    const long long elems = f.rows_n * static_cast<long long>(a.V);
-    const unsigned mblocks = static_cast<unsigned>(std::min<long long>((elems + 255) / 256, 64LL * sms));
-    if (a.dtype == SPEC_BF16) mask_kernel<Bf16><<<mblocks, 256, 0, a.stream>>>(f);
-    else mask_kernel<F32><<<mblocks, 256, 0, a.stream>>>(f);
+    // the filtered copies: one CTA per row
+    if (a.dtype == SPEC_BF16) mask_kernel<Bf16><<<static_cast<unsigned>(f.rows_n), 256, 0, a.stream>>>(f);
+    else mask_kernel<F32><<<static_cast<unsigned>(f.rows_n), 256, 0, a.stream>>>(f);
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "mask kernel launch failed: %s", cudaGetErrorString(e));
     Call c = a;

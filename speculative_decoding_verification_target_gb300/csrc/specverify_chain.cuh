@@ -357,6 +357,37 @@ __device__ __noinline__ FF flush_chunks(int mode, const typename E::Raw* qrt, co
     return acc;
 }
 
+// Every large chunk of piece pc (more than a queue holds), read again from memory: its float-float mass minus
+// the fast one, eight lanes to a chunk (warp-collective; returns this lane's share).
+template <class E, bool AL>
+__device__ __noinline__ FF piece_exact(int mode, const unsigned char* trow, const unsigned char* orow, int pc, int V,
+                                       float c, const PairOff po, const PairOffX px, const FFc& k, const float2* tab,
+                                       int tok, float hpatch, FF g, int lane) {
+    FF acc = {0.f, 0.f};
+    const int e = lane & 7;
+    for (int base = 0; base < PE / CHUNK; base += 4) {
+        const int e0 = pc * PE + (base + (lane >> 3)) * CHUNK;
+        FF r = {0.f, 0.f};
+        float cm = 0.f;
+        bool big = false;
+        if (e0 < V) {
+            const typename E::Raw rt = E::template gload<AL>(trow, e0, V);
+            const typename E::Raw ro = mode == 1 ? E::template gload<AL>(orow, e0, V) : rt;
+            const int et = (tok >= e0 && tok < e0 + CHUNK) ? tok - e0 : -1;
+            float ovl;
+            cm = fast_chunk<E>(mode, rt, ro, c, po, et, hpatch, ovl);
+            big = cm + ovl > k.tau || et >= 0;
+            if (big) {
+                const float2 xt2 = E::pair(rt, e >> 1), xd2 = E::pair(ro, e >> 1);
+                r = elem_exact(mode, (e & 1) ? xt2.y : xt2.x, (e & 1) ? xd2.y : xd2.x, px, k, tab, e == et, g);
+            }
+        }
+        const FF sum = group8_sum(r);
+        if (big && e == 0) acc = ff_add(acc, ff_addf(sum, -cm));
+    }
+    return acc;
+}
+
 // One cluster of cps CTAs per sequence (CTA rank = blockIdx.x % cps). Every CTA derives the row scalars
 // and the chain itself (the same arithmetic on the same data, so the same L); the pieces of the drawn row
 // are dealt to the CTAs round robin, each piece's residual mass (its large chunks recomputed at float-float
@@ -571,7 +602,7 @@ __global__ void __launch_bounds__(DNT, 1) draw_kernel(const __grid_constant__ DP
                 }
             }
             FF loc = {0.f, 0.f};
-            int nq = 0;   // large chunks waiting in this warp's queue
+            int nq = 0;   // large chunks of this piece in the warp's queue (more than D_QCH: all redone below)
 #pragma unroll
             for (int q = 0; q < PCH; ++q) {
                 const int e0 = pc * PE + (lane + 32 * q) * CHUNK;
@@ -583,23 +614,19 @@ __global__ void __launch_bounds__(DNT, 1) draw_kernel(const __grid_constant__ DP
                 const bool big = cm + ovl > p.k.tau || et >= 0;
                 const unsigned bm = __ballot_sync(0xffffffffu, big);
                 if (bm) {
-                    const int cnt = __popc(bm);
-                    if (nq + cnt > D_QCH) {
-                        loc = ff_add(loc, flush_chunks<E>(mode, s_qrt[warp], s_qro[warp], s_qcm[warp], s_qet[warp], nq, px,
-                                                          p.k, s_tab, gx, lane));
-                        nq = 0;
-                    }
-                    if (big) {
-                        const int at = nq + __popc(bm & ((1u << lane) - 1u));
+                    const int at = nq + __popc(bm & ((1u << lane) - 1u));
+                    if (big && at < D_QCH) {
                         s_qrt[warp][at] = rt[q];
                         s_qro[warp][at] = ro[q];
                         s_qcm[warp][at] = cm;
                         s_qet[warp][at] = et;
                     }
-                    nq += cnt;
+                    nq += __popc(bm);
                 }
             }
-            if (nq)
+            if (nq > D_QCH)   // a flat row: every large chunk of the piece again, from memory
+                loc = ff_add(loc, piece_exact<E, AL>(mode, trow, orow, pc, V, c, po, px, p.k, s_tab, tok, hpatch, gx, lane));
+            else if (nq)
                 loc = ff_add(loc, flush_chunks<E>(mode, s_qrt[warp], s_qro[warp], s_qcm[warp], s_qet[warp], nq, px, p.k,
                                                   s_tab, gx, lane));
             const FF m = warp_sum(loc);

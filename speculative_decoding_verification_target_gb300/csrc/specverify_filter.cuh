@@ -3,21 +3,30 @@
 // ratio is taken). Every such filter keeps the logits at or above a per-row threshold, so the filtered
 // verification is the ordinary one on rows whose other logits are -inf:
 //   - threshold_kernel: one CTA per row finds the threshold by radix selection on order-preserving integer
-//     keys of the logits, 8 bits a pass from the top (2 passes for bf16, 4 for fp32). Top-k (0 < k < V)
+//     keys of the logits, 4 bits a pass from the top (4 passes for bf16, 8 for fp32). Top-k (0 < k < V)
 //     descends by counts to the k-th largest value; top-p (0 < top_p < 1), on what top-k kept, descends by
 //     the mass sum_x 2^((x - M) c) to the value at which the mass from the largest logit down first reaches
-//     top_p of the kept total. Ties at a threshold are all kept (the kept set depends on values only);
+//     top_p of the kept total. Ties at a threshold are all kept (the kept set depends on values only). Once
+//     the elements still in play fit in shared memory (at most F_CAP keys), one more pass over the row copies
+//     them there and the remaining passes read only them;
 //   - mask_kernel: writes the filtered rows (kept logits unchanged, the others -inf) into the caller's
 //     workspace, and the chain kernels run on them.
-// The masses of a pass are summed in a fixed order (one lane per warp adds its warp's values in lane order;
-// warps are merged in warp order), so the threshold does not depend on timing.
+// The histograms of a pass are integer sums, so they do not depend on the order of the additions: counts, and
+// masses in 64-bit fixed point (2^-44 units; a mass 2^((x - M) c) is at most 1 and a row holds at most 2^18
+// logits, so a bin cannot overflow). Each thread adds into its own column of the shared-memory histograms (no
+// atomics, no contention however the keys cluster) and the columns are summed after the pass.
 #pragma once
 #include "specverify_kernels.cuh"
 
 namespace specv {
 
-constexpr int FT_W = 16;                // warps per CTA of the threshold kernel
-constexpr int FT_NT = FT_W * 32;
+constexpr int FT_NT = 256;               // threads of a threshold CTA
+constexpr int FT_W = FT_NT / 32;
+constexpr int F_DIGIT = 4;               // bits of a radix digit
+constexpr int F_BINS = 1 << F_DIGIT;
+constexpr int F_CAP = 4096;              // keys a CTA's candidate list holds
+constexpr size_t F_SMEM = static_cast<size_t>(F_BINS) * FT_NT * (sizeof(unsigned long long) + sizeof(unsigned)) +
+                          static_cast<size_t>(F_CAP) * sizeof(uint32_t);
 
 // order-preserving keys: a larger logit has a larger unsigned key (negative values reversed)
 template <class E>
@@ -26,9 +35,9 @@ template <>
 struct FKey<Bf16> {
     using K = uint32_t;
     static constexpr int BITS = 16;
+    __device__ static K of_bits(uint32_t b) { return (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u); }
     __device__ static K key(const unsigned char* row, int e) {
-        const uint32_t b = reinterpret_cast<const uint16_t*>(row)[e];
-        return (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u);
+        return of_bits(reinterpret_cast<const uint16_t*>(row)[e]);
     }
     __device__ static float value_of(K k) {
         const uint32_t b = (k & 0x8000u) ? (k & 0x7FFFu) : (~k & 0xFFFFu);
@@ -39,9 +48,9 @@ template <>
 struct FKey<F32> {
     using K = uint32_t;
     static constexpr int BITS = 32;
+    __device__ static K of_bits(uint32_t b) { return (b & 0x80000000u) ? ~b : (b | 0x80000000u); }
     __device__ static K key(const unsigned char* row, int e) {
-        const uint32_t b = reinterpret_cast<const uint32_t*>(row)[e];
-        return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+        return of_bits(reinterpret_cast<const uint32_t*>(row)[e]);
     }
     __device__ static float value_of(K k) {
         const uint32_t b = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
@@ -60,6 +69,7 @@ struct FParams {
     float* thr;                    // [rows_n] threshold value (-inf: nothing filtered)
     unsigned char* out_a;          // filtered copies, same layout as rows_a / rows_b
     unsigned char* out_b;
+    int vec;                       // every row starts on 16 bytes and holds whole 16-byte words
 };
 
 __device__ __forceinline__ const unsigned char* f_row(const FParams& p, long long r, size_t row_bytes) {
@@ -67,140 +77,260 @@ __device__ __forceinline__ const unsigned char* f_row(const FParams& p, long lon
                           : p.rows_b + static_cast<size_t>(r - p.rows_a_n) * row_bytes;
 }
 
+constexpr float F_FIX = 17592186044416.f;    // 2^44: the fixed-point unit of the mass histograms
+
+// Calls f(key, valid) for every logit of a row, a CTA's threads striding over it: 16-byte words when the row
+// allows them (vec), else single elements. Every thread of a warp makes the same number of calls (valid is
+// false past the end), so f may use warp votes.
+template <class E, class F>
+__device__ __forceinline__ void for_row_keys(const unsigned char* row, int V, bool vec, F&& f) {
+    using KT = typename FKey<E>::K;
+    if (vec) {
+        const uint4* w4 = reinterpret_cast<const uint4*>(row);
+        const int n4 = static_cast<int>(static_cast<size_t>(V) * E::BYTES / 16);
+#pragma unroll 2
+        for (int i0 = 0; i0 < n4; i0 += FT_NT) {
+            const int i = i0 + static_cast<int>(threadIdx.x);
+            const bool ok = i < n4;
+            const uint4 w = ok ? __ldg(w4 + i) : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if constexpr (E::BYTES == 2) {
+                    f(static_cast<KT>(FKey<E>::of_bits(u[j] & 0xFFFFu)), ok);
+                    f(static_cast<KT>(FKey<E>::of_bits(u[j] >> 16)), ok);
+                } else {
+                    f(static_cast<KT>(FKey<E>::of_bits(u[j])), ok);
+                }
+            }
+        }
+    } else {
+        for (int e0 = 0; e0 < V; e0 += FT_NT) {
+            const int e = e0 + static_cast<int>(threadIdx.x);
+            const bool ok = e < V;
+            f(ok ? FKey<E>::key(row, e) : KT(0), ok);
+        }
+    }
+}
+
 template <class E>
 __global__ void __launch_bounds__(FT_NT) threshold_kernel(const __grid_constant__ FParams p) {
     using KT = typename FKey<E>::K;
     constexpr int BITS = FKey<E>::BITS;
-    __shared__ float s_hist[FT_W][256];   // per-warp histogram of this pass (counts or masses)
-    __shared__ float s_tot[256];
-    __shared__ unsigned s_sel[2];          // chosen bin, and the bins above it (as float bits: mass)
-    __shared__ float s_red[FT_W];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    extern __shared__ __align__(16) unsigned char f_smem[];
+    unsigned long long* hm = reinterpret_cast<unsigned long long*>(f_smem);   // masses [F_BINS][FT_NT]
+    unsigned* hc = reinterpret_cast<unsigned*>(hm + F_BINS * FT_NT);          // counts [F_BINS][FT_NT]
+    KT* cand = reinterpret_cast<KT*>(hc + F_BINS * FT_NT);                     // candidate keys [F_CAP]
+    __shared__ unsigned s_cnt[F_BINS];
+    __shared__ unsigned long long s_mass[F_BINS];
+    __shared__ unsigned s_sel, s_n;
+    __shared__ unsigned long long s_above;
+    __shared__ KT s_kmax[FT_W];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const long long r = blockIdx.x;
     const int V = p.V;
+    const bool vec = p.vec != 0;
     const size_t row_bytes = static_cast<size_t>(V) * E::BYTES;
     const unsigned char* row = f_row(p, r, row_bytes);
     const float NINF = __uint_as_float(0xFF800000u);
+    for (int b = 0; b < F_BINS; ++b) {
+        hc[b * FT_NT + tid] = 0u;
+        hm[b * FT_NT + tid] = 0ull;
+    }
 
-    // one radix pass: histogram (by 8-bit digit at `shift`) of the elements whose key is >= lo and whose
-    // higher digits equal `prefix`; weight 1 (counts) or the element's mass 2^((x - M) c)
-    auto pass = [&](KT prefix, int shift, KT lo, bool mass, float M) {
-        for (int q = threadIdx.x; q < FT_W * 256; q += FT_NT) (&s_hist[0][0])[q] = 0.f;
+    // is key k in the set: k >= lo and its digits from bit `from` up equal `prefix` (from >= BITS: any digits)
+    auto in_set = [&](KT k, KT prefix, int from, KT lo) {
+        return k >= lo && (from >= BITS || (k >> from) == prefix);
+    };
+    // the largest key of the row (all threads get it); kmax holds this thread's share
+    auto cta_kmax = [&](KT kmax) -> KT {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) kmax = max(kmax, static_cast<KT>(__shfl_xor_sync(0xffffffffu, kmax, o)));
+        if (lane == 0) s_kmax[warp] = kmax;
         __syncthreads();
-        const int nsteps = (V + FT_NT - 1) / FT_NT;
-        for (int it = 0; it < nsteps; ++it) {
-            const int e = it * FT_NT + threadIdx.x;
-            int bin = -1;
-            float w = 0.f;
-            if (e < V) {
-                const KT k = FKey<E>::key(row, e);
-                const bool in = k >= lo && (shift + 8 >= BITS || (k >> (shift + 8)) == prefix);
-                if (in) {
-                    bin = static_cast<int>((k >> shift) & 0xFFu);
-                    w = mass ? ex2((FKey<E>::value_of(k) - M) * p.c) : 1.f;
-                }
+        KT m = 0;
+        for (int w2 = 0; w2 < FT_W; ++w2) m = max(m, s_kmax[w2]);
+        return m;
+    };
+    // one radix pass over the set (the row, or the n_c candidates when n_c >= 0): its histogram by the digit
+    // at `shift`, counts and (mass) masses 2^((x - M) c) in fixed point; leaves the bins in s_cnt / s_mass.
+    // *kmax (when given) receives the largest key the pass read.
+    auto pass = [&](int n_c, KT prefix, int shift, KT lo, bool mass, float M, KT* kmax) {
+        KT km = 0;
+        auto add = [&](KT k, bool ok) {
+            km = max(km, ok ? k : KT(0));
+            if (ok && in_set(k, prefix, shift + F_DIGIT, lo)) {
+                const int bin = static_cast<int>((k >> shift) & (F_BINS - 1));
+                hc[bin * FT_NT + tid] += 1u;
+                // the mass times 2^44, truncated (exact above 2^-21; the truncation is below one unit)
+                if (mass) hm[bin * FT_NT + tid] += __float2ull_rz(ex2((FKey<E>::value_of(k) - M) * p.c) * F_FIX);
             }
-            // lane 0 adds the warp's 32 contributions in lane order (a fixed summation order)
-            for (int src = 0; src < 32; ++src) {
-                const int b = __shfl_sync(0xffffffffu, bin, src);
-                const float v = __shfl_sync(0xffffffffu, w, src);
-                if (lane == 0 && b >= 0) s_hist[warp][b] += v;
+        };
+        if (n_c < 0) for_row_keys<E>(row, V, vec, add);
+        else
+            for (int i = tid; i < n_c; i += FT_NT) add(cand[i], true);
+        __syncthreads();
+        {   // FT_NT / F_BINS threads (contiguous lanes) sum the columns of one bin
+            constexpr int PER = FT_NT / F_BINS;
+            const int b = tid / PER, part = tid % PER;
+            unsigned cs = 0u;
+            unsigned long long ms = 0ull;
+            for (int j = part; j < FT_NT; j += PER) {
+                cs += hc[b * FT_NT + j];
+                ms += hm[b * FT_NT + j];
+            }
+#pragma unroll
+            for (int o = PER / 2; o > 0; o >>= 1) {
+                cs += __shfl_xor_sync(0xffffffffu, cs, o);
+                ms += __shfl_xor_sync(0xffffffffu, ms, o);
+            }
+            if (part == 0) {
+                s_cnt[b] = cs;
+                s_mass[b] = ms;
             }
         }
         __syncthreads();
-        if (threadIdx.x < 256) {
-            float t = 0.f;
-            for (int w2 = 0; w2 < FT_W; ++w2) t += s_hist[w2][threadIdx.x];
-            s_tot[threadIdx.x] = t;
+        for (int b = 0; b < F_BINS; ++b) {   // this thread's columns, cleared for the next pass
+            hc[b * FT_NT + tid] = 0u;
+            hm[b * FT_NT + tid] = 0ull;
         }
-        __syncthreads();
+        if (kmax) *kmax = cta_kmax(km);
     };
     // the bin, from the top, where the running total first reaches `need`; returns the total above it
-    auto choose = [&](float need) -> float {
-        if (threadIdx.x == 0) {
-            float above = 0.f;
+    auto choose = [&](unsigned long long need, bool mass) -> unsigned long long {
+        if (tid == 0) {
+            unsigned long long above = 0ull;
             int b = 0;
-            for (b = 255; b > 0; --b) {
-                if (above + s_tot[b] >= need) break;
-                above += s_tot[b];
+            for (b = F_BINS - 1; b > 0; --b) {
+                const unsigned long long h = mass ? s_mass[b] : static_cast<unsigned long long>(s_cnt[b]);
+                if (above + h >= need) break;
+                above += h;
             }
-            s_sel[0] = static_cast<unsigned>(b);
-            s_sel[1] = __float_as_uint(above);
+            s_sel = static_cast<unsigned>(b);
+            s_above = above;
         }
         __syncthreads();
-        const float above = __uint_as_float(s_sel[1]);
-        return above;
+        return s_above;
+    };
+    // copies into the candidate list (any order: what follows only sums integers) the keys >= lo whose digits
+    // from bit `from` up equal prefix, or (ge) are at least prefix
+    auto compact = [&](KT prefix, int from, KT lo, bool ge) -> int {
+        if (tid == 0) s_n = 0u;
+        __syncthreads();
+        for_row_keys<E>(row, V, vec, [&](KT k, bool ok) {
+            const bool in = ok && k >= lo && (from >= BITS || (ge ? (k >> from) >= prefix : (k >> from) == prefix));
+            const unsigned bal = __ballot_sync(0xffffffffu, in);
+            if (bal) {
+                unsigned base = 0u;
+                if (lane == 0) base = atomicAdd(&s_n, static_cast<unsigned>(__popc(bal)));
+                base = __shfl_sync(0xffffffffu, base, 0);
+                if (in) {
+                    const unsigned at = base + static_cast<unsigned>(__popc(bal & ((1u << lane) - 1u)));
+                    if (at < static_cast<unsigned>(F_CAP)) cand[at] = k;
+                }
+            }
+        });
+        __syncthreads();
+        const int n = static_cast<int>(min(s_n, static_cast<unsigned>(F_CAP)));
+        __syncthreads();
+        return n;
     };
 
     KT lo = 0;                             // keep keys >= lo
-    bool filtered = false;
+    KT kmax = 0;                           // the row's largest key (once a pass has read the row)
+    bool have_max = false, filtered = false;
+    int n_c = -1;                          // keys in the candidate list (-1: passes read the row)
     if (p.top_k > 0 && p.top_k < V) {
         KT prefix = 0;
-        float need = static_cast<float>(p.top_k);
-        for (int shift = BITS - 8; shift >= 0; shift -= 8) {
-            pass(prefix, shift, 0, false, 0.f);
-            need -= choose(need);
-            prefix = (prefix << 8) | static_cast<KT>(s_sel[0]);
+        unsigned long long need = static_cast<unsigned long long>(p.top_k);
+        for (int shift = BITS - F_DIGIT; shift >= 0; shift -= F_DIGIT) {
+            pass(n_c, prefix, shift, 0, false, 0.f, have_max ? nullptr : &kmax);
+            have_max = true;
+            const unsigned long long above = choose(need, false);
+            const unsigned sel = s_sel, cnt = s_cnt[sel];
+            need -= above;
+            prefix = (prefix << F_DIGIT) | static_cast<KT>(sel);
             __syncthreads();
+            // every key from this prefix up: what top-k still sorts and everything it keeps
+            const unsigned long long n_ge = static_cast<unsigned long long>(p.top_k) - need + cnt;
+            if (n_c < 0 && shift > 0 && n_ge <= static_cast<unsigned long long>(F_CAP)) n_c = compact(prefix, shift, 0, true);
         }
         lo = prefix;
         filtered = true;
     }
     if (p.top_p > 0.f && p.top_p < 1.f) {
-        // the row's largest logit, then the kept total
-        float m = NINF;
-        for (int e = threadIdx.x; e < V; e += FT_NT) m = fmaxf(m, FKey<E>::value_of(FKey<E>::key(row, e)));
-        m = warp_max(m);
-        if (lane == 0) s_red[warp] = m;
-        __syncthreads();
-        float M = NINF;
-        for (int w2 = 0; w2 < FT_W; ++w2) M = fmaxf(M, s_red[w2]);
-        __syncthreads();
+        if (!have_max) {
+            KT km = 0;
+            for_row_keys<E>(row, V, vec, [&](KT k, bool ok) { km = max(km, ok ? k : KT(0)); });
+            kmax = cta_kmax(km);
+        }
+        const float M = FKey<E>::value_of(kmax);
         KT prefix = 0;
-        float need = 0.f;
-        for (int shift = BITS - 8; shift >= 0; shift -= 8) {
-            pass(prefix, shift, lo, true, M);
-            if (shift == BITS - 8) {   // the first pass sees every kept element: its bins sum to the total
-                if (threadIdx.x == 0) {
-                    float t = 0.f;
-                    for (int b = 255; b >= 0; --b) t += s_tot[b];
-                    s_red[0] = t;
-                }
-                __syncthreads();
-                need = p.top_p * s_red[0];
-                __syncthreads();
+        unsigned long long need = 0ull;
+        for (int shift = BITS - F_DIGIT; shift >= 0; shift -= F_DIGIT) {
+            pass(n_c, prefix, shift, lo, true, M, nullptr);
+            if (shift == BITS - F_DIGIT) {   // the first pass sees every kept element: its bins sum to the total
+                unsigned long long t = 0ull;
+                for (int b = 0; b < F_BINS; ++b) t += s_mass[b];
+                // top_p of the total, rounded up: the smallest fixed-point mass that reaches it
+                need = static_cast<unsigned long long>(ceil(static_cast<double>(p.top_p) * static_cast<double>(t)));
             }
-            need -= choose(need);
-            prefix = (prefix << 8) | static_cast<KT>(s_sel[0]);
+            const unsigned long long above = choose(need, true);
+            const unsigned sel = s_sel, cnt = s_cnt[sel];
+            need -= above;
+            prefix = (prefix << F_DIGIT) | static_cast<KT>(sel);
             __syncthreads();
+            if (n_c < 0 && shift > 0 && cnt <= static_cast<unsigned>(F_CAP)) n_c = compact(prefix, shift, lo, false);
         }
         if (!filtered || prefix > lo) lo = prefix;
         filtered = true;
     }
-    if (threadIdx.x == 0) p.thr[r] = filtered ? FKey<E>::value_of(lo) : NINF;
+    if (tid == 0) p.thr[r] = filtered ? FKey<E>::value_of(lo) : NINF;
 }
 
-// the filtered copies: logits at or above the row's threshold, -inf elsewhere
+// The filtered copies, one CTA per row: logits at or above the row's threshold, -inf elsewhere (16-byte words
+// when every row allows them).
 template <class E>
 __global__ void __launch_bounds__(256) mask_kernel(const __grid_constant__ FParams p) {
+    const long long r = blockIdx.x;
     const size_t V = static_cast<size_t>(p.V);
-    const size_t total = static_cast<size_t>(p.rows_n) * V;
-    for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-        const long long r = static_cast<long long>(i / V);
-        const size_t e = i - static_cast<size_t>(r) * V;
-        const float t = p.thr[r];
-        const unsigned char* src = r < p.rows_a_n ? p.rows_a + (static_cast<size_t>(r) * V + e) * E::BYTES
-                                                  : p.rows_b + (static_cast<size_t>(r - p.rows_a_n) * V + e) * E::BYTES;
-        unsigned char* dst = r < p.rows_a_n ? p.out_a + (static_cast<size_t>(r) * V + e) * E::BYTES
-                                            : p.out_b + (static_cast<size_t>(r - p.rows_a_n) * V + e) * E::BYTES;
+    const size_t row_bytes = V * E::BYTES;
+    const float t = p.thr[r];
+    const unsigned char* src = f_row(p, r, row_bytes);
+    unsigned char* dst = r < p.rows_a_n ? p.out_a + static_cast<size_t>(r) * row_bytes
+                                        : p.out_b + static_cast<size_t>(r - p.rows_a_n) * row_bytes;
+    auto keep16 = [&](uint32_t b) -> uint32_t {   // a bf16 in the low half of b
+        return __uint_as_float(b << 16) >= t ? b : 0xFF80u;
+    };
+    auto keep32 = [&](uint32_t b) -> uint32_t { return __uint_as_float(b) >= t ? b : 0xFF800000u; };
+    if (p.vec) {
+        const uint4* s4 = reinterpret_cast<const uint4*>(src);
+        uint4* d4 = reinterpret_cast<uint4*>(dst);
+        const size_t n4 = row_bytes / 16;
+#pragma unroll 4
+        for (size_t i = threadIdx.x; i < n4; i += blockDim.x) {
+            uint4 w = __ldg(s4 + i);
+            if constexpr (E::BYTES == 2) {
+                w.x = keep16(w.x & 0xFFFFu) | (keep16(w.x >> 16) << 16);
+                w.y = keep16(w.y & 0xFFFFu) | (keep16(w.y >> 16) << 16);
+                w.z = keep16(w.z & 0xFFFFu) | (keep16(w.z >> 16) << 16);
+                w.w = keep16(w.w & 0xFFFFu) | (keep16(w.w >> 16) << 16);
+            } else {
+                w.x = keep32(w.x);
+                w.y = keep32(w.y);
+                w.z = keep32(w.z);
+                w.w = keep32(w.w);
+            }
+            d4[i] = w;
+        }
+        return;
+    }
+    for (size_t e = threadIdx.x; e < V; e += blockDim.x) {
         if constexpr (E::BYTES == 2) {
-            const uint16_t b = *reinterpret_cast<const uint16_t*>(src);
-            const float x = __uint_as_float(static_cast<uint32_t>(b) << 16);
-            *reinterpret_cast<uint16_t*>(dst) = x >= t ? b : static_cast<uint16_t>(0xFF80u);
+            const uint16_t b = reinterpret_cast<const uint16_t*>(src)[e];
+            reinterpret_cast<uint16_t*>(dst)[e] = static_cast<uint16_t>(keep16(b));
         } else {
-            const float x = *reinterpret_cast<const float*>(src);
-            *reinterpret_cast<float*>(dst) = x >= t ? x : __uint_as_float(0xFF800000u);
+            reinterpret_cast<uint32_t*>(dst)[e] = keep32(reinterpret_cast<const uint32_t*>(src)[e]);
         }
     }
 }
