@@ -806,7 +806,9 @@ __global__ void __launch_bounds__(DNT, 1) draw_kernel(const __grid_constant__ DP
             }
             if (j == L && !idle) emitted = s_emit;
         }
-        cluster_sync_all();   // CTA 0 has read the other CTAs' masses; the buffers may be rewritten or released
+        // CTA 0 has read the other CTAs' masses before a next pass rewrites them; after the last pass no CTA
+        // touches another's shared memory, so each may finish on its own
+        if (it + 1 < n_pass) cluster_sync_all();
     }
 
     // after a failed wait a copy may still be in flight: it must land before the CTA may exit
