@@ -239,10 +239,11 @@ FILTER_TOP_K, FILTER_TOP_P = 64, 0.95
 class Runner:
     """One workload on one device: its ring of input batches, output buffers and the call through the binding."""
 
-    def __init__(self, sv, torch, w, dev, rank, max_ring, kind=None, filtered=False):
+    def __init__(self, sv, torch, w, dev, rank, max_ring, kind=None, filtered=False, one_launch=False):
         self.sv, self.torch, self.w, self.dev = sv, torch, w, dev
         self.kind = kind or kind_of(w)
         self.filtered = filtered
+        self.one_launch = one_launch
         self.batch_bytes = w.algorithmic_bytes()
         ring = max(2, -(-4 * L2_BYTES // self.batch_bytes))        # >= 4x L2 in flight across the ring
         self.ring = min(ring, max_ring)
@@ -259,15 +260,15 @@ class Runner:
             else None
         # kernels per call: the row pass (statistics or gamma kernel) and the chain-and-draw kernel; the
         # filtered path adds its threshold and mask kernels
-        self.launches_per_call = 4 if filtered else 2
+        self.launches_per_call = 4 if filtered else (1 if one_launch else 2)
 
     def entry_point(self):
         w = self.w
         if self.filtered:
             return "spec_verify_filtered (top_k %d, top_p %g)" % (FILTER_TOP_K, FILTER_TOP_P)
         return {"verify": "spec_verify", "cactus": "spec_cactus_verify (delta %g)" % max(w.deltas or (0.0,)),
-                "counterfactual": "spec_counterfactual_gamma (N %d, fused verify of drafter %d)" % (
-                    w.N, w.selected)}[self.kind]
+                "counterfactual": "spec_counterfactual_gamma (N %d, fused verify of drafter %d%s)" % (
+                    w.N, w.selected, "; gamma and chain in one cooperative launch" if self.one_launch else "")}[self.kind]
 
     def call(self, bt, s=None):
         w, sv = self.w, self.sv
@@ -355,26 +356,33 @@ def cpu_baseline(w, host, seconds, max_seq):
                 n_seq, w.B, w.name, reps, total_dt)}
 
 
-def record_for(args, torch, sv, w, dev, rank, stream, pg, local, filtered=False):
+def record_for(args, torch, sv, w, dev, rank, stream, pg, local, filtered=False, one_launch=False):
     """Per-workload record: positions/s, the average call, achieved GB/s against the measured peak and the
-    recorded DRAM traffic, timed like the headline; plus a short oracle baseline on the host."""
-    r = Runner(sv, torch, w, dev, rank, args.max_ring, filtered=filtered)
-    for i in range(args.warmup):
-        r.step(i)
-    torch.cuda.synchronize(dev)
-    steps = args.steps
-    graph = r.capture(args.warmup, steps)
+    recorded DRAM traffic, timed like the headline; plus a short oracle baseline on the host. one_launch: a
+    counterfactual call's gamma and chain as one cooperative launch (its graph is captured with that setting)."""
+    r = Runner(sv, torch, w, dev, rank, args.max_ring, filtered=filtered, one_launch=one_launch)
+    sv.set_gamma_one_launch(one_launch)
+    try:
+        for i in range(args.warmup):
+            r.step(i)
+        torch.cuda.synchronize(dev)
+        steps = args.steps
+        graph = r.capture(args.warmup, steps)
+    finally:
+        sv.set_gamma_one_launch(False)
     ms, c1 = timed_replays(torch, graph, 1, stream, dev, pg, local)
     sus, c2 = sustained(torch, graph, steps, ms / steps, stream, dev, pg, local, args.sustain_seconds)
     peak, peak_kind = peaks()
     call_s = ms / steps / 1e3
     achieved = r.batch_bytes / call_s / 1e9
-    name = w.name + ("+top_k%d_top_p%g" % (FILTER_TOP_K, FILTER_TOP_P) if filtered else "")
+    name = w.name + ("+top_k%d_top_p%g" % (FILTER_TOP_K, FILTER_TOP_P) if filtered else "") + \
+        (" (one launch)" if one_launch else "")
     rec = {"workload": name, "entry_point": r.entry_point(), "B": w.B, "K": w.K, "V": w.V, "N": w.N,
            "temperature": w.temperature, "positions_per_call": w.positions,
            "value": w.positions / call_s, "unit": UNIT, "steps": steps, "avg_call_us": call_s * 1e6,
            "bytes_per_call": r.batch_bytes, "achieved_gbs": achieved, "peak_gbs": peak, "peak_kind": peak_kind,
-           "frac": achieved / peak, "traffic": None if filtered else RECORDED_TRAFFIC.get(kernel_source_hash(), {}).get(w.name),
+           "frac": achieved / peak,
+           "traffic": None if (filtered or one_launch) else RECORDED_TRAFFIC.get(kernel_source_hash(), {}).get(w.name),
            "sustained_call_us": sus["ms_per_step"] * 1e3, "sustained_calls": sus["steps"],
            "clocks": merge_clocks(c1, c2),
            "l2": "ring of %d distinct batches (%.0f MB) > 129 MB L2" % (r.ring, r.ring * r.batch_bytes / 1e6),
@@ -382,7 +390,7 @@ def record_for(args, torch, sv, w, dev, rank, stream, pg, local, filtered=False)
     if filtered:
         rec["note"] = ("bytes_per_call counts one read of every logit; the path reads the logits three times and "
                        "writes a filtered copy once")
-    if not args.no_cpu_baseline and rank == 0 and not filtered:
+    if not args.no_cpu_baseline and rank == 0 and not filtered and not one_launch:
         host = {k: r.batches[0][k].to("cpu") for k in ("target", "drafters" if r.kind == "counterfactual"
                                                           else "draft", "tokens", "seeds")}
         rec["cpu_baseline"] = cpu_baseline(w, host, args.record_cpu_seconds, max(1, args.cpu_sequences // 8))
@@ -502,6 +510,11 @@ def run_ours(args, w):
                 continue
             records.append(record_for(args, torch, sv, workloads.WORKLOADS[name], dev, rank, stream, pg, local))
         records.append(record_for(args, torch, sv, w, dev, rank, stream, pg, local, filtered=True))
+        # the counterfactual workloads again with gamma and chain in one cooperative launch
+        for name in RECORD_WORKLOADS:
+            if kind_of(workloads.WORKLOADS[name]) == "counterfactual":
+                records.append(record_for(args, torch, sv, workloads.WORKLOADS[name], dev, rank, stream, pg, local,
+                                          one_launch=True))
 
     if rank != 0:
         return 0

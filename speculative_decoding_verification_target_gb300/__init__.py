@@ -25,7 +25,8 @@ EXPORTS = ("spec_workspace_size", "spec_verify", "spec_counterfactual_gamma", "s
            "spec_read_status", "spec_clear_status", "spec_last_error", "spec_verify_static",
            "spec_hedge_feedback_state_size", "spec_hedge_feedback_init", "spec_hedge_feedback_push")
 # tuning and test hooks (csrc/specverify_internal.h): exported by the library, not part of the C ABI
-TEST_HOOKS = ("spec_debug_set_stats_grid", "spec_debug_last_plan", "spec_debug_exp2ff", "spec_debug_set_draw_tau")
+TEST_HOOKS = ("spec_debug_set_stats_grid", "spec_debug_last_plan", "spec_debug_exp2ff", "spec_debug_set_draw_tau",
+              "spec_debug_set_gamma_one_launch")
 
 _lib = None
 
@@ -90,6 +91,8 @@ def load(build_if_missing: bool = False):
     lib.spec_debug_last_plan.restype = I
     lib.spec_debug_set_draw_tau.argtypes = [F]
     lib.spec_debug_set_draw_tau.restype = I
+    lib.spec_debug_set_gamma_one_launch.argtypes = [I]
+    lib.spec_debug_set_gamma_one_launch.restype = I
     lib.spec_debug_exp2ff.argtypes = [P, P, P, P, I, F, P]
     lib.spec_debug_exp2ff.restype = I
     lib.spec_verify_static.argtypes = [P, P, I, P, P, I, I, I, F, P, P, P, ctypes.POINTER(ctypes.c_uint32), P]
@@ -155,6 +158,13 @@ def set_stats_grid(ctas: int):
     """Tuning / test hook: CTAs of the statistics pass of verify / cactus_verify (0 = automatic)."""
     if load().spec_debug_set_stats_grid(int(ctas)) != 0:
         raise ValueError("unsupported statistics grid %r" % ctas)
+
+
+def set_gamma_one_launch(on: bool):
+    """Tuning / test hook: run counterfactual_gamma with a selected drafter as one cooperative launch (gamma,
+    a grid barrier, then the chain) instead of the gamma kernel followed by the draw kernel."""
+    if load().spec_debug_set_gamma_one_launch(1 if on else 0) != 0:
+        raise ValueError("unsupported value %r" % on)
 
 
 def last_plan() -> dict:

@@ -32,6 +32,7 @@ constexpr size_t WS_HEADER = 256;          // status word + padding
 constexpr int SMEM_MAX_PER_CTA = 232448;   // opt-in maximum per CTA
 
 int g_stats_grid_override = 0;   // CTAs of the statistics kernel (0 = automatic)
+int g_gamma_one_launch = 0;      // 1: a counterfactual call with a selected drafter runs as one launch
 float g_draw_tau = 0.f;          // chunk mass above which the draw takes its float-float path (0 = default)
 thread_local int g_last_plan[5] = {0, 0, 0, 0, 0};   // see spec_debug_last_plan
 
@@ -184,9 +185,9 @@ FFc ff_constants(float temperature) {
 // The chain and its draw for one drafter (one cluster per sequence), launched with programmatic stream
 // serialisation behind the kernel that computed the row statistics: either the segment partials of
 // stats_kernel (part, P pieces over G warps) or whole-row pairs (row_ms, from gamma_kernel).
-spec_status launch_draw(const Call& a, bool aligned, const unsigned char* draft, const float2* part,
-                        const float2* row_ms, long long P, int G, unsigned* status) {
-    const int eb = a.dtype == SPEC_BF16 ? 2 : 4;
+// The draw's parameters for one drafter (everything but the cluster size and the bulk-copy mode).
+DParams draw_params(const Call& a, const unsigned char* draft, const float2* part, const float2* row_ms,
+                    long long P, int G, unsigned* status) {
     DParams d = {};
     d.target = static_cast<const unsigned char*>(a.target);
     d.draft = draft;
@@ -211,6 +212,13 @@ spec_status launch_draw(const Call& a, bool aligned, const unsigned char* draft,
     d.diag = a.diag;
     d.gamma_star = a.gamma_star;
     d.status = status;
+    return d;
+}
+
+spec_status launch_draw(const Call& a, bool aligned, const unsigned char* draft, const float2* part,
+                        const float2* row_ms, long long P, int G, unsigned* status) {
+    const int eb = a.dtype == SPEC_BF16 ? 2 : 4;
+    DParams d = draw_params(a, draft, part, row_ms, P, G, status);
     // CTAs per sequence: the largest power of two up to D_MAX_CPS that keeps the grid within one CTA per SM
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -434,6 +442,32 @@ spec_status run_gamma(const Call& a, bool aligned) {
     cfg.blockDim = dim3(GNT, 1, 1);
     cfg.dynamicSmemBytes = G_SMEM;   // also in the unaligned mode: keeps one CTA per SM for the TMEM allocation
     cfg.stream = a.stream;
+    if (chain && aligned && g_gamma_one_launch) {
+        // gamma and the chain in one cooperative launch (every CTA resident: one per SM)
+        FuseParams f = {};
+        f.g = g;
+        const unsigned char* draft =
+            g.drafters + static_cast<size_t>(a.selected) * a.B * a.K * static_cast<size_t>(a.V) * eb;
+        f.d = draw_params(a, draft, nullptr, g.row_ms, 0, 0, g.status);
+        f.d.cps = 1;
+        f.d.tma = a.dtype == SPEC_BF16 ? 1 : 0;   // bf16 slots fit below the DrawShared block
+        f.bar = reinterpret_cast<unsigned*>(ws) + 1;
+        using FusedFn = void (*)(const FuseParams);
+        FusedFn ffn = a.dtype == SPEC_BF16 ? gamma_chain_kernel<Bf16> : gamma_chain_kernel<F32>;
+        int fcap = 0;
+        e = dyn_smem_ceiling(ffn, dev, &fcap);
+        if (e == cudaSuccess && G_SMEM > static_cast<size_t>(fcap)) e = cudaErrorInvalidValue;
+        if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "one-launch kernel attribute failed: %s", cudaGetErrorString(e));
+        cudaLaunchAttribute ca[1];
+        ca[0].id = cudaLaunchAttributeCooperative;
+        ca[0].val.cooperative = 1;
+        cfg.attrs = ca;
+        cfg.numAttrs = 1;
+        g_last_plan[3] = 5;
+        e = cudaLaunchKernelEx(&cfg, ffn, f);
+        if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "one-launch kernel launch failed: %s", cudaGetErrorString(e));
+        return SPEC_OK;
+    }
     e = cudaLaunchKernelEx(&cfg, gfn, g);
     if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "gamma kernel launch failed: %s", cudaGetErrorString(e));
     if (!chain) return SPEC_OK;
@@ -869,7 +903,7 @@ spec_status spec_read_status(const void* workspace, uint32_t* status_out, void* 
 
 spec_status spec_clear_status(void* workspace, void* stream) {
     if (!workspace) return fail(SPEC_ERR_INVALID, "workspace must not be NULL");
-    cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream));
+    cudaError_t e = cudaMemsetAsync(workspace, 0, 4 * sizeof(uint32_t), static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "status clear failed: %s", cudaGetErrorString(e));
     return SPEC_OK;
 }
@@ -889,6 +923,12 @@ int spec_debug_exp2ff(const float* d, const float* l_hi, const float* l_lo, floa
     ff_exp2_probe_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
         d, l_hi, l_lo, out, n, ff_constants(temperature));
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+int spec_debug_set_gamma_one_launch(int on) {
+    if (on != 0 && on != 1) return -1;
+    g_gamma_one_launch = on;
+    return 0;
 }
 
 int spec_debug_set_draw_tau(float tau) {

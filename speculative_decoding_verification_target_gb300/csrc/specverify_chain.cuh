@@ -388,42 +388,80 @@ __device__ __noinline__ FF piece_exact(int mode, const unsigned char* trow, cons
     return acc;
 }
 
-// One cluster of cps CTAs per sequence (CTA rank = blockIdx.x % cps). Every CTA derives the row scalars
+// The draw's shared-memory state (one CTA; a draw kernel CTA holds it statically, the one-launch
+// counterfactual kernel inside its dynamic shared memory once the gamma phase is over).
+template <class E>
+struct DrawShared {
+    using Raw = typename E::Raw;
+    float s_ht[D_MAX_K + 1], s_pd[D_MAX_K];
+    // row offsets: target rows (nm, l as a float pair), the fast h rows of the chain (l with the Cactus
+    // scale), draft rows
+    float s_nmt[D_MAX_K + 1], s_ltp[D_MAX_K + 1], s_ltp_lo[D_MAX_K + 1], s_lt[D_MAX_K];
+    float s_nmo[D_MAX_K], s_lo[D_MAX_K], s_lo_lo[D_MAX_K];
+    float s_xt[D_MAX_K], s_xd[D_MAX_K];
+    int s_tok[D_MAX_K];
+    float2 s_sc[D_MAX_K], s_g[D_MAX_K];   // Cactus, per position: precise scale s and gamma*
+    float2 s_tiles[D_MAX_PIECES];          // per piece: residual mass (float-float), gathered in CTA 0
+    float2 s_tab[33];                      // the float-float exp2 table
+    Raw s_qrt[DW][D_QCH], s_qro[DW][D_QCH];   // per warp: queue of large chunks (logits of both rows,
+    float s_qcm[DW][D_QCH];                   // fast mass, Cactus token index)
+    int s_qet[DW][D_QCH];
+    int s_pl[D_CPP], s_pn;                 // the pick: large chunks of the chosen piece,
+    float2 s_pm[D_CPP];                    // their float-float masses (by chunk)
+    float2 s_pr[D_CPP][8];                 // and element residuals (by list position)
+    float2 s_wscan[DW];                    // the pick's per-warp chunk totals
+    int s_wfirst[DW], s_wlast[DW];
+    PickPlan s_plan;
+    int s_L, s_emit;
+};
+
+// One cluster of cps CTAs per sequence. Every CTA derives the row scalars
 // and the chain itself (the same arithmetic on the same data, so the same L); the pieces of the drawn row
 // are dealt to the CTAs round robin, each piece's residual mass (its large chunks recomputed at float-float
 // precision) goes to CTA 0, and CTA 0 finds the piece holding u * Z and re-reads that one piece to find the
 // token (fast_chunk, chunk_values and elem_exact give the same values in both places).
-template <class E, bool AL>
-__global__ void __launch_bounds__(DNT, 1) draw_kernel(const __grid_constant__ DParams p) {
+// draw_body runs it for one sequence on all DNT threads of one CTA: sequence blockIdx.x / cps and rank
+// cluster_ctarank() in a draw kernel launch (LAUNCHED), else sequence b_arg as the only CTA of its cluster
+// (cps = 1). d_smem: the bulk-copy slots and their mbarriers (bulk-copy mode).
+template <class E, bool AL, bool LAUNCHED>
+__device__ __forceinline__ void draw_body(const DParams& p, DrawShared<E>& S, unsigned char* const d_smem,
+                                          const int b_arg) {
     using Raw = typename E::Raw;
-    // dynamic shared memory (bulk-copy mode): one slot per warp holding a target piece and a draft piece,
-    // then one mbarrier per warp
-    extern __shared__ __align__(128) unsigned char d_smem[];
-    __shared__ float s_ht[D_MAX_K + 1], s_pd[D_MAX_K];
-    // row offsets: target rows (nm, l as a float pair), the fast h rows of the chain (l with the Cactus
-    // scale), draft rows
-    __shared__ float s_nmt[D_MAX_K + 1], s_ltp[D_MAX_K + 1], s_ltp_lo[D_MAX_K + 1], s_lt[D_MAX_K];
-    __shared__ float s_nmo[D_MAX_K], s_lo[D_MAX_K], s_lo_lo[D_MAX_K];
-    __shared__ float s_xt[D_MAX_K], s_xd[D_MAX_K];
-    __shared__ int s_tok[D_MAX_K];
-    __shared__ float2 s_sc[D_MAX_K], s_g[D_MAX_K];   // Cactus, per position: precise scale s and gamma*
-    __shared__ float2 s_tiles[D_MAX_PIECES];          // per piece: residual mass (float-float), gathered in CTA 0
-    __shared__ float2 s_tab[33];                      // the float-float exp2 table
-    __shared__ Raw s_qrt[DW][D_QCH], s_qro[DW][D_QCH];   // per warp: queue of large chunks (logits of both rows,
-    __shared__ float s_qcm[DW][D_QCH];                   // fast mass, Cactus token index)
-    __shared__ int s_qet[DW][D_QCH];
-    __shared__ int s_pl[D_CPP], s_pn;                 // the pick: large chunks of the chosen piece,
-    __shared__ float2 s_pm[D_CPP];                    // their float-float masses (by chunk)
-    __shared__ float2 s_pr[D_CPP][8];                 // and element residuals (by list position)
-    __shared__ float2 s_wscan[DW];                    // the pick's per-warp chunk totals
-    __shared__ int s_wfirst[DW], s_wlast[DW];
-    __shared__ PickPlan s_plan;
-    __shared__ int s_L, s_emit;
+    auto& s_ht = S.s_ht;
+    auto& s_pd = S.s_pd;
+    auto& s_nmt = S.s_nmt;
+    auto& s_ltp = S.s_ltp;
+    auto& s_ltp_lo = S.s_ltp_lo;
+    auto& s_lt = S.s_lt;
+    auto& s_nmo = S.s_nmo;
+    auto& s_lo = S.s_lo;
+    auto& s_lo_lo = S.s_lo_lo;
+    auto& s_xt = S.s_xt;
+    auto& s_xd = S.s_xd;
+    auto& s_tok = S.s_tok;
+    auto& s_sc = S.s_sc;
+    auto& s_g = S.s_g;
+    auto& s_tiles = S.s_tiles;
+    auto& s_tab = S.s_tab;
+    auto& s_qrt = S.s_qrt;
+    auto& s_qro = S.s_qro;
+    auto& s_qcm = S.s_qcm;
+    auto& s_qet = S.s_qet;
+    auto& s_pl = S.s_pl;
+    auto& s_pn = S.s_pn;
+    auto& s_pm = S.s_pm;
+    auto& s_pr = S.s_pr;
+    auto& s_wscan = S.s_wscan;
+    auto& s_wfirst = S.s_wfirst;
+    auto& s_wlast = S.s_wlast;
+    auto& s_plan = S.s_plan;
+    auto& s_L = S.s_L;
+    auto& s_emit = S.s_emit;
     const float NINF = __uint_as_float(0xFF800000u);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int cps = p.cps;
-    const uint32_t rank = cluster_ctarank();
-    const int b = blockIdx.x / cps;
+    const int cps = LAUNCHED ? p.cps : 1;
+    const uint32_t rank = LAUNCHED ? cluster_ctarank() : 0u;
+    const int b = LAUNCHED ? static_cast<int>(blockIdx.x) / cps : b_arg;
     const int K = p.K, V = p.V, np = p.np;
     const float c = p.c;
     const size_t row_bytes = static_cast<size_t>(V) * E::BYTES;
@@ -814,6 +852,7 @@ __global__ void __launch_bounds__(DNT, 1) draw_kernel(const __grid_constant__ DP
     // after a failed wait a copy may still be in flight: it must land before the CTA may exit
     if (use_tma && lane == 0 && !ok_all && n_issued > 0)
         mbar_wait_bounded(fullb, static_cast<uint32_t>((n_issued - 1) & 1), p.status, STATUS_TIMEOUT, WAIT_LIMIT_NS);
+    if (use_tma && lane == 0) mbar_inval(fullb);   // the slot's memory may be reused (a next draw_body call)
     __syncwarp();
 
     // ---- outputs ----
@@ -827,6 +866,16 @@ __global__ void __launch_bounds__(DNT, 1) draw_kernel(const __grid_constant__ DP
         }
         if (lane == 0) p.accept_len[b] = L;
     }
+}
+
+// One cluster of cps CTAs per sequence (CTA rank = blockIdx.x % cps).
+template <class E, bool AL>
+__global__ void __launch_bounds__(DNT, 1) draw_kernel(const __grid_constant__ DParams p) {
+    // dynamic shared memory (bulk-copy mode): one slot per warp holding a target piece and a draft piece,
+    // then one mbarrier per warp
+    extern __shared__ __align__(128) unsigned char d_smem[];
+    __shared__ DrawShared<E> S;
+    draw_body<E, AL, true>(p, S, d_smem, 0);
 }
 
 // ------------------------------------------------------------------------------------------------

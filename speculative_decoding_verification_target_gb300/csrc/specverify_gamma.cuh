@@ -291,8 +291,10 @@ __device__ __forceinline__ void g_overlap(const typename E::Raw (&rt)[GPiece<E>:
 }
 
 // ---------------------------------------- the kernel ----------------------------------------
+// The gamma kernel's work on one CTA (all GNT threads): its run of units, then the release of its tensor
+// memory.
 template <class E>
-__global__ void __launch_bounds__(GNT, 1) gamma_kernel(const __grid_constant__ CgParams p) {
+__device__ __forceinline__ void gamma_body(const CgParams& p) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ uint32_t s_tmem;
     __shared__ float2 s_ms[4][GW];   // per unit u (mod 4): the warps' (max, sum) of its row
@@ -551,12 +553,87 @@ __global__ void __launch_bounds__(GNT, 1) gamma_kernel(const __grid_constant__ C
         for (long long q = copies - G_R > 0 ? copies - G_R : 0; q < copies; ++q)
             mbar_wait_bounded(&full[q % G_R], static_cast<uint32_t>((q / G_R) & 1), p.status, STATUS_TIMEOUT, WAIT_LIMIT_NS);
     }
+    if (p.tma && lane == 0)   // the ring's memory may be reused after this (the one-launch kernel's draw)
+        for (int q = 0; q < G_R; ++q) mbar_inval(&full[q]);
     __syncwarp();
     tmem_fence_before();
     __syncthreads();
     tmem_fence_after();
     if (warp == 0)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(G_TMEM_COLS) : "memory");
+}
+
+template <class E>
+__global__ void __launch_bounds__(GNT, 1) gamma_kernel(const __grid_constant__ CgParams p) {
+    gamma_body<E>(p);
+}
+
+// ---------------------------------------- one launch: gamma, then the chain ----------------------------------------
+// The counterfactual call with a selected drafter as a single cooperative launch: every CTA runs its gamma
+// units, a grid barrier makes every row's (max, sum) visible, and then CTA g draws sequences g, g + G, ...
+// with the draw kernel's arithmetic (one CTA per sequence), its state placed in the dynamic shared memory
+// that the gamma phase no longer uses.
+struct FuseParams {
+    CgParams g;
+    DParams d;
+    unsigned* bar;   // [0] arrivals (0 between uses), [1] generation: the grid barrier's words
+};
+
+// The DrawShared block sits at the top of the gamma kernel's dynamic shared memory, above the draw's
+// bulk-copy slots (bf16 rows) at its bottom.
+template <class E>
+__host__ __device__ constexpr size_t fused_draw_shared_off() {
+    return (G_SMEM - sizeof(DrawShared<E>)) / 128 * 128;
+}
+constexpr size_t FUSED_DRAW_RING = static_cast<size_t>(DW) * (2 * static_cast<size_t>(PE) * 2 + sizeof(uint64_t));
+static_assert(GNT == DNT, "the draw phase runs on the gamma kernel's threads");
+static_assert(FUSED_DRAW_RING <= fused_draw_shared_off<Bf16>(), "bf16 draw slots and DrawShared overlap");
+static_assert(sizeof(DrawShared<F32>) <= G_SMEM, "DrawShared does not fit the gamma kernel's shared memory");
+
+// A barrier across every CTA of a cooperative launch: thread 0 of each CTA arrives on bar[0]; the last to
+// arrive resets it and advances the generation bar[1], which the others wait for (sleeping between polls).
+// Writes before it are visible to reads after it. A wait that outlasts WAIT_LIMIT_NS sets STATUS_TIMEOUT and
+// gives up (the results are then invalid).
+__device__ __forceinline__ void grid_barrier(unsigned* bar, unsigned n, unsigned* status) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        volatile unsigned* gen = bar + 1;
+        const unsigned g0 = *gen;
+        __threadfence();
+        if (atomicAdd(bar, 1u) == n - 1) {
+            atomicExch(bar, 0u);
+            __threadfence();
+            atomicAdd(bar + 1, 1u);
+        } else {
+            const uint64_t t0 = global_timer_ns();
+            for (int it = 0; *gen == g0; ++it) {
+                __nanosleep(128);
+                if ((it & 63) == 63 && global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+                    atomicOr(status, STATUS_TIMEOUT);
+                    break;
+                }
+            }
+        }
+        __threadfence();
+    }
+    __syncthreads();
+}
+
+// The draw phase out of line, so that its registers do not crowd the gamma phase's allocation.
+template <class E>
+__device__ __noinline__ void fused_draws(const DParams& d, DrawShared<E>& S, unsigned char* smem) {
+    for (int b = static_cast<int>(blockIdx.x); b < d.B; b += static_cast<int>(gridDim.x)) {
+        draw_body<E, true, false>(d, S, smem, b);
+        __syncthreads();   // the next sequence's draw reuses the slots and the DrawShared block
+    }
+}
+
+template <class E>
+__global__ void __launch_bounds__(GNT, 1) gamma_chain_kernel(const __grid_constant__ FuseParams f) {
+    gamma_body<E>(f.g);
+    grid_barrier(f.bar, gridDim.x, f.g.status);
+    extern __shared__ __align__(128) unsigned char smem[];
+    fused_draws<E>(f.d, *reinterpret_cast<DrawShared<E>*>(smem + fused_draw_shared_off<E>()), smem);
 }
 
 // ------------------------------------------------------------------------------------------------

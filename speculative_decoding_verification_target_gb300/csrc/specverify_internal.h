@@ -20,7 +20,8 @@ int spec_debug_set_stats_grid(int ctas);
 /* The launch plan of the last call made on this thread, as five ints: 0, ring slots per warp, CTAs
  * launched, kernel (0: the statistics pass of spec_verify / spec_cactus_verify / spec_verify_static; 2: the
  * gamma kernel of spec_counterfactual_gamma, which parks rows in tensor memory; 3: the argmax pass of
- * spec_greedy_verify), pieces per row. out5 is host memory. Returns 0, or -1 for a NULL pointer. */
+ * spec_greedy_verify; 5: the one-launch gamma and chain kernel), pieces per row. out5 is host memory.
+ * Returns 0, or -1 for a NULL pointer. */
 int spec_debug_last_plan(int* out5);
 
 /* Sets the chunk mass (sum of the target and draft probabilities of an 8-logit chunk) above which the residual
@@ -28,6 +29,13 @@ int spec_debug_last_plan(int* out5);
  * and leave more elements to the float path. Process-wide and not synchronised. Returns 0, or -1 for a
  * negative or NaN value. */
 int spec_debug_set_draw_tau(float tau);
+
+/* 1: spec_counterfactual_gamma with a selected drafter (rows aligned for bulk copies) runs the gamma pass
+ * and the selected drafter's chain and draw as one cooperative launch (a grid barrier between the two, one
+ * CTA per sequence for the draw, the barrier's words in the workspace header, which spec_clear_status
+ * zeroes); 0 (the default): the gamma kernel, then the draw kernel with programmatic dependent launch.
+ * Process-wide and not synchronised. Returns 0, or -1 for another value. */
+int spec_debug_set_gamma_one_launch(int on);
 
 /* The residual draw's float-float building block on n inputs (device pointers): out[2i], out[2i + 1] = the
  * float pair of 2^((d[i]) c + l) with c = log2(e) / temperature and l = l_hi[i] + l_lo[i], evaluated as the
