@@ -235,7 +235,8 @@ spec_status spec_verify_static(const void* target_logits, const void* draft_logi
 /* Copies the workspace status word to *status_out (host), synchronising `stream`. */
 spec_status spec_read_status(const void* workspace, uint32_t* status_out, void* stream);
 
-/* Zeroes the workspace status word (asynchronous on `stream`). */
+/* Zeroes the first 16 bytes of the workspace: the status word and three words the library keeps for its own
+ * bookkeeping between calls (asynchronous on `stream`). */
 spec_status spec_clear_status(void* workspace, void* stream);
 
 /* Thread-local message describing the last non-OK status returned on this thread. */
