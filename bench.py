@@ -147,7 +147,12 @@ def max_over_ranks(pg, torch, v, device):
 # of this benchmark's own command (profiles/), keyed by a hash of the kernel sources it was taken with: when
 # the sources change the recorded number no longer applies and the JSON line reports null.
 RECORDED_TRAFFIC = {
-    "12435f7b735a104d": {"sps_llama3_b64_k5": 214668800, "hedgespec_n7_b32_k5": 372430592 + 3307264 + 16286720},
+    "891f30682ba935d7": {
+        "sps_llama3_b64_k5": 214857088,
+        "hedgespec_n7_b32_k5": 392456704,
+        "cactus_qwen_b128_m20": 1668309760,
+        "hedgespec_n21_b256_k8": 18988425216,   # captured at B = 32, scaled by 256 / 32 (grows with the sequences)
+    },
 }
 
 
@@ -579,11 +584,15 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-records", action="store_true", help="headline workload only")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="sequences per call (0: the workload's own B); smaller profiling cases of the same shapes")
     ap.add_argument("--sustain-seconds", type=float, default=0.5)
     ap.add_argument("--record-cpu-seconds", type=float, default=4.0)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w = workloads.WORKLOADS[args.workload]
+    if args.batch > 0:
+        w = w.scaled(B=args.batch)
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)
