@@ -79,6 +79,40 @@ __device__ __forceinline__ const unsigned char* f_row(const FParams& p, long lon
 
 constexpr float F_FIX = 17592186044416.f;    // 2^44: the fixed-point unit of the mass histograms
 
+// The key of a value that is one of the row's elements, taking -0 for a zero (keys order -0 below +0, float
+// comparison does not): never above the element's own key.
+template <class E>
+__device__ __forceinline__ typename FKey<E>::K key_at_most(float v) {
+    if (v == 0.f) v = -0.f;
+    if constexpr (E::BYTES == 2) return FKey<E>::of_bits(__float_as_uint(v) >> 16);
+    else return FKey<E>::of_bits(__float_as_uint(v));
+}
+
+// This thread's largest value of the row (the CTA's threads striding over 16-byte words, vec rows only): a
+// packed bf16 max per word pair for bf16 rows, -inf when the thread holds no element.
+template <class E>
+__device__ __forceinline__ float thread_max_words(const unsigned char* row, int V) {
+    const uint4* w4 = reinterpret_cast<const uint4*>(row);
+    const int n4 = static_cast<int>(static_cast<size_t>(V) * E::BYTES / 16);
+    if constexpr (E::BYTES == 2) {
+        uint32_t m2 = 0xFF80FF80u;
+#pragma unroll 4
+        for (int i = threadIdx.x; i < n4; i += FT_NT) {
+            const uint4 w = __ldg(w4 + i);
+            m2 = bf16x2_max(m2, bf16x2_max(bf16x2_max(w.x, w.y), bf16x2_max(w.z, w.w)));
+        }
+        return fmaxf(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xFFFF0000u));
+    } else {
+        float m = __uint_as_float(0xFF800000u);
+#pragma unroll 4
+        for (int i = threadIdx.x; i < n4; i += FT_NT) {
+            const float4 w = __ldg(reinterpret_cast<const float4*>(w4) + i);
+            m = fmaxf(m, fmaxf(fmaxf(w.x, w.y), fmaxf(w.z, w.w)));
+        }
+        return m;
+    }
+}
+
 // Calls f(key, valid) for every logit of a row, a CTA's threads striding over it: 16-byte words when the row
 // allows them (vec), else single elements. Every thread of a warp makes the same number of calls (valid is
 // false past the end), so f may use warp votes.
@@ -126,6 +160,8 @@ __global__ void __launch_bounds__(FT_NT) threshold_kernel(const __grid_constant_
     __shared__ unsigned s_sel, s_n;
     __shared__ unsigned long long s_above;
     __shared__ KT s_kmax[FT_W];
+    __shared__ KT s_tmax[FT_NT];                 // top-k by bound: every thread's largest key
+    __shared__ KT s_bound, s_rowmax;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const long long r = blockIdx.x;
     const int V = p.V;
@@ -213,7 +249,8 @@ __global__ void __launch_bounds__(FT_NT) threshold_kernel(const __grid_constant_
         return s_above;
     };
     // copies into the candidate list (any order: what follows only sums integers) the keys >= lo whose digits
-    // from bit `from` up equal prefix, or (ge) are at least prefix
+    // from bit `from` up equal prefix, or (ge) are at least prefix; returns how many there are (the list holds
+    // the first F_CAP)
     auto compact = [&](KT prefix, int from, KT lo, bool ge) -> int {
         if (tid == 0) s_n = 0u;
         __syncthreads();
@@ -231,7 +268,56 @@ __global__ void __launch_bounds__(FT_NT) threshold_kernel(const __grid_constant_
             }
         });
         __syncthreads();
-        const int n = static_cast<int>(min(s_n, static_cast<unsigned>(F_CAP)));
+        const int n = static_cast<int>(s_n);
+        __syncthreads();
+        return n;
+    };
+
+    // compact(0, BITS, b, false) for vec rows, a word at a time: the values of a 16-byte word are compared
+    // with b's value as floats (every key >= b passes: key order refines float order), and only a word with a
+    // passing value takes the exact key test and the list append
+    auto compact_bound = [&](KT b) -> int {
+        if (tid == 0) s_n = 0u;
+        __syncthreads();
+        const float bv = FKey<E>::value_of(b);
+        const uint4* w4 = reinterpret_cast<const uint4*>(row);
+        const int n4 = static_cast<int>(row_bytes / 16);
+        for (int i0 = 0; i0 < n4; i0 += FT_NT) {
+            const int i = i0 + tid;
+            const bool ok = i < n4;
+            const uint4 w = ok ? __ldg(w4 + i) : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+            bool any = false;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if constexpr (E::BYTES == 2)
+                    any |= (__uint_as_float(u[j] << 16) >= bv) | (__uint_as_float(u[j] & 0xFFFF0000u) >= bv);
+                else
+                    any |= __uint_as_float(u[j]) >= bv;
+            }
+            if (!__any_sync(0xffffffffu, ok && any)) continue;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                for (int h = 0; h < (E::BYTES == 2 ? 2 : 1); ++h) {
+                    const KT k = E::BYTES == 2 ? FKey<E>::of_bits(h ? (u[j] >> 16) : (u[j] & 0xFFFFu))
+                                               : FKey<E>::of_bits(u[j]);
+                    const bool in = ok && k >= b;
+                    const unsigned bal = __ballot_sync(0xffffffffu, in);
+                    if (bal) {
+                        unsigned base = 0u;
+                        if (lane == 0) base = atomicAdd(&s_n, static_cast<unsigned>(__popc(bal)));
+                        base = __shfl_sync(0xffffffffu, base, 0);
+                        if (in) {
+                            const unsigned at = base + static_cast<unsigned>(__popc(bal & ((1u << lane) - 1u)));
+                            if (at < static_cast<unsigned>(F_CAP)) cand[at] = k;
+                        }
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        const int n = static_cast<int>(s_n);
         __syncthreads();
         return n;
     };
@@ -241,6 +327,28 @@ __global__ void __launch_bounds__(FT_NT) threshold_kernel(const __grid_constant_
     bool have_max = false, filtered = false;
     int n_c = -1;                          // keys in the candidate list (-1: passes read the row)
     if (p.top_k > 0 && p.top_k < V) {
+        if (p.top_k <= FT_NT) {
+            // The threads' own largest keys are FT_NT distinct elements of the row, so the k-th largest of them
+            // is at most the row's k-th largest: every key top-k keeps is at or above it. Those keys go to the
+            // candidate list when they fit, and the descent below reads only them.
+            KT km = 0;
+            if (vec) km = key_at_most<E>(thread_max_words<E>(row, V));
+            else for_row_keys<E>(row, V, vec, [&](KT k, bool ok) { km = max(km, ok ? k : KT(0)); });
+            s_tmax[tid] = km;
+            __syncthreads();
+            int rank = 0;   // larger keys, and equal keys of lower threads
+            for (int t = 0; t < FT_NT; ++t) {
+                const KT o = s_tmax[t];
+                rank += (o > km || (o == km && t < tid)) ? 1 : 0;
+            }
+            if (rank == p.top_k - 1) s_bound = km;
+            if (rank == 0) s_rowmax = km;
+            __syncthreads();
+            kmax = s_rowmax;
+            have_max = true;
+            const int n = vec ? compact_bound(s_bound) : compact(0, BITS, s_bound, false);
+            if (n <= F_CAP) n_c = n;
+        }
         KT prefix = 0;
         unsigned long long need = static_cast<unsigned long long>(p.top_k);
         for (int shift = BITS - F_DIGIT; shift >= 0; shift -= F_DIGIT) {
@@ -253,7 +361,8 @@ __global__ void __launch_bounds__(FT_NT) threshold_kernel(const __grid_constant_
             __syncthreads();
             // every key from this prefix up: what top-k still sorts and everything it keeps
             const unsigned long long n_ge = static_cast<unsigned long long>(p.top_k) - need + cnt;
-            if (n_c < 0 && shift > 0 && n_ge <= static_cast<unsigned long long>(F_CAP)) n_c = compact(prefix, shift, 0, true);
+            if (n_c < 0 && shift > 0 && n_ge <= static_cast<unsigned long long>(F_CAP))
+                n_c = min(compact(prefix, shift, 0, true), F_CAP);
         }
         lo = prefix;
         filtered = true;
@@ -280,7 +389,7 @@ __global__ void __launch_bounds__(FT_NT) threshold_kernel(const __grid_constant_
             need -= above;
             prefix = (prefix << F_DIGIT) | static_cast<KT>(sel);
             __syncthreads();
-            if (n_c < 0 && shift > 0 && cnt <= static_cast<unsigned>(F_CAP)) n_c = compact(prefix, shift, lo, false);
+            if (n_c < 0 && shift > 0 && cnt <= static_cast<unsigned>(F_CAP)) n_c = min(compact(prefix, shift, lo, false), F_CAP);
         }
         if (!filtered || prefix > lo) lo = prefix;
         filtered = true;

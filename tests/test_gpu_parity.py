@@ -650,6 +650,7 @@ def test_normalhedge_round(N):
 @pytest.mark.parametrize("V,dtype,top_k,top_p", [
     (3000, "bf16", 50, 1.0), (3000, "bf16", 0, 0.9), (3000, "bf16", 200, 0.8), (20001, "bf16", 7, 0.95),
     (1000, "fp32", 40, 0.9), (1000, "fp32", 0, 0.5), (128256, "bf16", 1000, 0.9), (151936, "bf16", 0, 0.99),
+    (128256, "bf16", 64, 0.95), (4096, "bf16", 256, 1.0), (65536, "fp32", 256, 0.7), (2000, "bf16", 257, 1.0),
 ])
 def test_verify_filtered_small(V, dtype, top_k, top_p):
     w = small(V, B=8, K=4, dtype=dtype, T=0.9, sigma=1.0)
@@ -665,6 +666,29 @@ def test_verify_filtered_small(V, dtype, top_k, top_p):
     assert_diag(out, ref)
     assert_chain(out, ref, w.K)
     assert sv.read_status(out["workspace"]) == 0
+
+
+def test_verify_filtered_ties():
+    """Rows with many equal logits: the keys at or above top-k's bound (the k-th largest of the CTA threads'
+    own maxima) can outnumber the candidate list, and every copy of the threshold value is kept."""
+    B, K, V = 3, 2, 12000
+    gen = torch.Generator().manual_seed(3)
+    levels = torch.tensor([0.0, 1.0, 2.0, 3.5], dtype=torch.float32)
+    target = levels[torch.randint(0, 4, (B, K + 1, V), generator=gen)]
+    target[0] = 2.0                                       # one position flat: every key ties
+    draft = target[:, :K] + 0.5 * levels[torch.randint(0, 4, (B, K, V), generator=gen)]
+    tokens = torch.randint(0, V, (B, K), generator=gen, dtype=torch.int32)
+    seeds = torch.arange(B, dtype=torch.int64) + 77
+    for top_k, top_p in ((100, 1.0), (7, 0.9), (256, 0.5)):
+        for dt in (torch.bfloat16, torch.float32):
+            t, d = target.to(dt), draft.to(dt)
+            ref = oracle.verify_filtered(host(t), host(d), tokens.numpy(), seeds.numpy().astype(np.uint64), 1.0,
+                                         top_k, top_p)
+            out = sv.verify_filtered(t.cuda(), d.cuda(), tokens.cuda(), seeds.cuda(), 1.0, top_k, top_p)
+            torch.cuda.synchronize()
+            assert_diag(out, ref)
+            assert_chain(out, ref, K)
+            assert sv.read_status(out["workspace"]) == 0
 
 
 def test_verify_filtered_without_filters_is_verify():
