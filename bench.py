@@ -412,7 +412,7 @@ def run_ours(args, w):
     torch.cuda.set_device(dev)
     sv.load()
     stream = torch.cuda.current_stream(dev)
-    r = Runner(sv, torch, w, dev, rank, args.max_ring)
+    r = Runner(sv, torch, w, dev, rank, args.max_ring, filtered=args.filtered)
     kind = r.kind
     batch_bytes = r.batch_bytes
     for i in range(args.warmup):
@@ -545,10 +545,13 @@ def run_ours(args, w):
                        r.ring, r.ring * batch_bytes / 1e6),
                    "parallelism": "replicas over sequences" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": RECORDED_TRAFFIC.get(kernel_source_hash(), {}).get(w.name), "peak_kind": peak_kind,
-                     "kernel": "%s + draw_kernel: one whole %s call (both kernels), graph replay timed with CUDA "
-                               "events on the launching stream, divided by the steps" % (
-                                   "gamma_kernel" if kind == "counterfactual" else "stats_kernel", kind),
+                     "traffic": None if args.filtered else RECORDED_TRAFFIC.get(kernel_source_hash(), {}).get(w.name),
+                     "peak_kind": peak_kind,
+                     "kernel": ("threshold_kernel + mask_kernel + stats_kernel + draw_kernel: one whole filtered call"
+                                if args.filtered else
+                                "%s + draw_kernel: one whole %s call (both kernels)" % (
+                                    "gamma_kernel" if kind == "counterfactual" else "stats_kernel", kind)) +
+                               ", graph replay timed with CUDA events on the launching stream, divided by the steps",
                      "avg_call_us": avg_call_s * 1e6, "eager_call_us": eager_ms * 1e3,
                      "frac_of_8tbs_nominal": achieved / 8000.0},
         "sustained": {"ms_per_step": sus["ms_per_step"], "steps": sus["steps"], "seconds": sus["seconds"],
@@ -584,6 +587,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-records", action="store_true", help="headline workload only")
+    ap.add_argument("--filtered", action="store_true",
+                    help="time spec_verify_filtered (top_k %d, top_p %g) on the workload as the headline" % (
+                        FILTER_TOP_K, FILTER_TOP_P))
     ap.add_argument("--batch", type=int, default=0,
                     help="sequences per call (0: the workload's own B); smaller profiling cases of the same shapes")
     ap.add_argument("--sustain-seconds", type=float, default=0.5)

@@ -88,26 +88,38 @@ __device__ __forceinline__ typename FKey<E>::K key_at_most(float v) {
     else return FKey<E>::of_bits(__float_as_uint(v));
 }
 
+// One 16-byte word of a row through the read-only path with an L2 eviction policy.
+__device__ __forceinline__ uint4 ld_word(const uint4* ptr, uint64_t pol) {
+    uint4 v;
+    asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(ptr), "l"(pol));
+    return v;
+}
+
 // This thread's largest value of the row (the CTA's threads striding over 16-byte words, vec rows only): a
-// packed bf16 max per word pair for bf16 rows, -inf when the thread holds no element.
+// packed bf16 max per word pair for bf16 rows, -inf when the thread holds no element. The row is read
+// evict-last: the compaction that follows reads it again.
 template <class E>
 __device__ __forceinline__ float thread_max_words(const unsigned char* row, int V) {
     const uint4* w4 = reinterpret_cast<const uint4*>(row);
     const int n4 = static_cast<int>(static_cast<size_t>(V) * E::BYTES / 16);
+    const uint64_t pol = policy_evict_last();
     if constexpr (E::BYTES == 2) {
         uint32_t m2 = 0xFF80FF80u;
-#pragma unroll 4
+#pragma unroll 8
         for (int i = threadIdx.x; i < n4; i += FT_NT) {
-            const uint4 w = __ldg(w4 + i);
+            const uint4 w = ld_word(w4 + i, pol);
             m2 = bf16x2_max(m2, bf16x2_max(bf16x2_max(w.x, w.y), bf16x2_max(w.z, w.w)));
         }
         return fmaxf(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xFFFF0000u));
     } else {
         float m = __uint_as_float(0xFF800000u);
-#pragma unroll 4
+#pragma unroll 8
         for (int i = threadIdx.x; i < n4; i += FT_NT) {
-            const float4 w = __ldg(reinterpret_cast<const float4*>(w4) + i);
-            m = fmaxf(m, fmaxf(fmaxf(w.x, w.y), fmaxf(w.z, w.w)));
+            const uint4 w = ld_word(w4 + i, pol);
+            m = fmaxf(m, fmaxf(fmaxf(__uint_as_float(w.x), __uint_as_float(w.y)),
+                               fmaxf(__uint_as_float(w.z), __uint_as_float(w.w))));
         }
         return m;
     }
@@ -282,10 +294,20 @@ __global__ void __launch_bounds__(FT_NT) threshold_kernel(const __grid_constant_
         const float bv = FKey<E>::value_of(b);
         const uint4* w4 = reinterpret_cast<const uint4*>(row);
         const int n4 = static_cast<int>(row_bytes / 16);
-        for (int i0 = 0; i0 < n4; i0 += FT_NT) {
-            const int i = i0 + tid;
+        const uint64_t pol = policy_evict_first();   // the row's last read
+        constexpr int BATCH = 4;                       // words a thread loads before testing them
+        for (int i0 = 0; i0 < n4; i0 += BATCH * FT_NT) {
+            uint4 ws[BATCH];
+#pragma unroll
+            for (int r = 0; r < BATCH; ++r) {
+                const int i = i0 + r * FT_NT + tid;
+                ws[r] = i < n4 ? ld_word(w4 + i, pol) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int r = 0; r < BATCH; ++r) {
+            const int i = i0 + r * FT_NT + tid;
             const bool ok = i < n4;
-            const uint4 w = ok ? __ldg(w4 + i) : make_uint4(0u, 0u, 0u, 0u);
+            const uint4 w = ws[r];
             const uint32_t u[4] = {w.x, w.y, w.z, w.w};
             bool any = false;
 #pragma unroll
@@ -314,6 +336,7 @@ __global__ void __launch_bounds__(FT_NT) threshold_kernel(const __grid_constant_
                         }
                     }
                 }
+            }
             }
         }
         __syncthreads();
