@@ -147,11 +147,11 @@ def max_over_ranks(pg, torch, v, device):
 # of this benchmark's own command (profiles/), keyed by a hash of the kernel sources it was taken with: when
 # the sources change the recorded number no longer applies and the JSON line reports null.
 RECORDED_TRAFFIC = {
-    "891f30682ba935d7": {
-        "sps_llama3_b64_k5": 214857088,
-        "hedgespec_n7_b32_k5": 392456704,
-        "cactus_qwen_b128_m20": 1668309760,
-        "hedgespec_n21_b256_k8": 18988425216,   # captured at B = 32, scaled by 256 / 32 (grows with the sequences)
+    "686eac9ab016b803": {
+        "sps_llama3_b64_k5": 214698752,
+        "hedgespec_n7_b32_k5": 392502784,
+        "cactus_qwen_b128_m20": 1668214784,
+        "hedgespec_n21_b256_k8": 18995759104,   # captured at B = 32, scaled by 256 / 32 (grows with the sequences)
     },
 }
 
