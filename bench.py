@@ -264,8 +264,8 @@ class Runner:
         self.gam = torch.empty((w.N, w.B, w.K), dtype=torch.float32, device=dev) if self.kind == "counterfactual" \
             else None
         # kernels per call: the row pass (statistics or gamma kernel) and the chain-and-draw kernel; the
-        # filtered path adds its threshold and mask kernels
-        self.launches_per_call = 4 if filtered else (1 if one_launch else 2)
+        # filtered path adds its threshold kernel
+        self.launches_per_call = 3 if filtered else (1 if one_launch else 2)
 
     def entry_point(self):
         w = self.w
@@ -393,8 +393,8 @@ def record_for(args, torch, sv, w, dev, rank, stream, pg, local, filtered=False,
            "l2": "ring of %d distinct batches (%.0f MB) > 129 MB L2" % (r.ring, r.ring * r.batch_bytes / 1e6),
            "device_status": sv.read_status(r.ws) if not filtered else None}
     if filtered:
-        rec["note"] = ("bytes_per_call counts one read of every logit; the path reads the logits three times and "
-                       "writes a filtered copy once")
+        rec["note"] = ("bytes_per_call counts one read of every logit; the path reads the logits twice (the "
+                       "threshold pass, then the statistics pass that masks them as it reads)")
     if not args.no_cpu_baseline and rank == 0 and not filtered and not one_launch:
         host = {k: r.batches[0][k].to("cpu") for k in ("target", "drafters" if r.kind == "counterfactual"
                                                           else "draft", "tokens", "seeds")}
@@ -547,7 +547,7 @@ def run_ours(args, w):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": None if args.filtered else RECORDED_TRAFFIC.get(kernel_source_hash(), {}).get(w.name),
                      "peak_kind": peak_kind,
-                     "kernel": ("threshold_kernel + mask_kernel + stats_kernel + draw_kernel: one whole filtered call"
+                     "kernel": ("threshold_kernel + stats_kernel + draw_kernel (masking forms): one whole filtered call"
                                 if args.filtered else
                                 "%s + draw_kernel: one whole %s call (both kernels)" % (
                                     "gamma_kernel" if kind == "counterfactual" else "stats_kernel", kind)) +

@@ -190,8 +190,9 @@ spec_status spec_hedge_feedback_init(void* state, int N, int B, int K, int objec
 spec_status spec_hedge_feedback_push(void* state, const float* gamma, const int32_t* accept_len, int N, int B, int K,
                                      float* weights, int32_t* applied, void* stream);
 
-/* Bytes of workspace spec_verify_filtered needs: the spec_verify workspace, one float per row and a filtered
- * copy of every target and draft row (the same size as the logits). 0 for invalid sizes or dtype. */
+/* Bytes of workspace spec_verify_filtered needs: the spec_verify workspace and one float (the row's threshold)
+ * per target and draft row. No filtered copy of the logits is made: the kernels mask each logit as they read
+ * it. 0 for invalid sizes or dtype. */
 size_t spec_filter_workspace_size(int B, int K, int V, spec_dtype dtype);
 
 /* spec_verify with standardised sampling ("Speculative Decoding 为什么是 Lossless 的", §8 Q4: temperature,
@@ -203,8 +204,8 @@ size_t spec_filter_workspace_size(int B, int K, int V, spec_dtype dtype);
  * neither rule): ties at a threshold are all kept, top-k comes before top-p. Same arguments, outputs and
  * errors as spec_verify, plus top_k >= 0 and top_p in (0, 1]; the workspace must hold
  * spec_filter_workspace_size(B, K, V, dtype) bytes (its first 16 bytes zeroed once, as for spec_verify). The
- * thresholds come from radix selection with fp32 mass sums: a top-p decision within about 1e-6 of the mass
- * boundary may differ from an exact-arithmetic one. */
+ * thresholds come from radix selection on fp32 masses (summed in 2^-44 fixed point): a top-p decision within
+ * about 1e-6 of the mass boundary may differ from an exact-arithmetic one. */
 spec_status spec_verify_filtered(const void* target_logits, const void* draft_logits, spec_dtype dtype,
                                  const int32_t* draft_tokens, const uint64_t* seeds, int B, int K, int V,
                                  float temperature, int top_k, float top_p, int32_t* accept_len, int32_t* out_tokens,

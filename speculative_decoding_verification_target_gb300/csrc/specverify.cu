@@ -27,6 +27,7 @@ spec_status fail(spec_status s, const char* fmt, ...) {
 
 constexpr int MAX_K = 64;
 constexpr int MAX_V = 262144;
+static_assert(MAX_V == FB_MAX_V, "the bound kernel sizes its line keys for the largest vocabulary");
 constexpr int MAX_N = 64;
 constexpr size_t WS_HEADER = 256;          // status word + padding
 constexpr int SMEM_MAX_PER_CTA = 232448;   // opt-in maximum per CTA
@@ -58,16 +59,15 @@ WsLayout ws_layout(int B, int K, int V, int N) {
 // Workspace of spec_verify_filtered: [the verify workspace][row thresholds][filtered target rows][filtered
 // draft rows], each region 256-byte aligned.
 struct FilterLayout {
-    size_t thr_off, ta_off, tb_off, total;
+    size_t thr_off, ms_off, total;
 };
-FilterLayout filter_layout(int B, int K, int V, int eb) {
+FilterLayout filter_layout(int B, int K, int V) {
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
     FilterLayout f;
     const size_t rows = static_cast<size_t>(B) * (2 * K + 1);
     f.thr_off = up(ws_layout(B, K, V, 1).total);
-    f.ta_off = up(f.thr_off + rows * sizeof(float));
-    f.tb_off = up(f.ta_off + static_cast<size_t>(B) * (K + 1) * V * eb);
-    f.total = up(f.tb_off + static_cast<size_t>(B) * K * V * eb);
+    f.ms_off = up(f.thr_off + rows * sizeof(float));
+    f.total = up(f.ms_off + rows * sizeof(float2));
     return f;
 }
 
@@ -86,6 +86,7 @@ struct Call {
     int32_t* out_tokens;
     float* diag;
     float* gamma_star;
+    const float* thr;   // standardised sampling: per statistics row, the logits below it count as -inf (or null)
     void* workspace;
     size_t workspace_bytes;
     cudaStream_t stream;
@@ -211,6 +212,7 @@ DParams draw_params(const Call& a, const unsigned char* draft, const float2* par
     d.out_tokens = a.out_tokens;
     d.diag = a.diag;
     d.gamma_star = a.gamma_star;
+    d.thr = a.thr;
     d.status = status;
     return d;
 }
@@ -230,8 +232,11 @@ spec_status launch_draw(const Call& a, bool aligned, const unsigned char* draft,
     // (bulk-copy mode) a two-piece slot and an mbarrier per warp, when they fit
     const size_t ring_bytes = static_cast<size_t>(DW) * (2 * static_cast<size_t>(PE) * eb + sizeof(uint64_t));
     using DrawFn = void (*)(const DParams);
-    DrawFn dfn = a.dtype == SPEC_BF16 ? (aligned ? draw_kernel<Bf16, true> : draw_kernel<Bf16, false>)
-                                      : (aligned ? draw_kernel<F32, true> : draw_kernel<F32, false>);
+    DrawFn dfn;
+    if (a.thr) dfn = a.dtype == SPEC_BF16 ? (aligned ? draw_kernel<Bf16, true, true> : draw_kernel<Bf16, false, true>)
+                                          : (aligned ? draw_kernel<F32, true, true> : draw_kernel<F32, false, true>);
+    else dfn = a.dtype == SPEC_BF16 ? (aligned ? draw_kernel<Bf16, true> : draw_kernel<Bf16, false>)
+                                    : (aligned ? draw_kernel<F32, true> : draw_kernel<F32, false>);
     int dsmem_cap = 0;
     e = dyn_smem_ceiling(dfn, dev, &dsmem_cap);
     if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "draw kernel attribute failed: %s", cudaGetErrorString(e));
@@ -475,10 +480,18 @@ spec_status run_gamma(const Call& a, bool aligned) {
     return launch_draw(a, aligned, draft, nullptr, g.row_ms, 0, 0, g.status);
 }
 
-// Standardised sampling: the per-row thresholds, the filtered copies in the workspace, then the chain on them.
+// Standardised sampling: the per-row thresholds and the kept logits' (max, sum), then the draw kernel in its
+// filtering form (a logit below its row's threshold is -inf as it is read). Top-k up to FB_MAX_K on rows of
+// whole 16-byte words goes through bound_kernel, which leaves the rows it cannot settle to threshold_kernel;
+// every other filter goes through threshold_kernel alone. No filter at all is spec_verify itself.
 spec_status run_filtered(const Call& a, int top_k, float top_p) {
     const int eb = a.dtype == SPEC_BF16 ? 2 : 4;
-    const FilterLayout fl = filter_layout(a.B, a.K, a.V, eb);
+    const bool rows16 = ((reinterpret_cast<uintptr_t>(a.target) | reinterpret_cast<uintptr_t>(a.others)) & 15) == 0 &&
+                        (static_cast<size_t>(a.V) * eb) % 16 == 0;
+    const bool aligned = rows16 && a.V % CHUNK == 0;
+    const bool by_k = top_k > 0 && top_k < a.V, by_p = top_p < 1.f;
+    if (!by_k && !by_p) return run_chain(a, aligned);
+    const FilterLayout fl = filter_layout(a.B, a.K, a.V);
     unsigned char* ws = static_cast<unsigned char*>(a.workspace);
     FParams f = {};
     f.rows_a = static_cast<const unsigned char*>(a.target);
@@ -487,34 +500,42 @@ spec_status run_filtered(const Call& a, int top_k, float top_p) {
     f.rows_n = f.rows_a_n + static_cast<long long>(a.B) * a.K;
     f.V = a.V;
     f.c = static_cast<float>(1.4426950408889634 / static_cast<double>(a.temperature));
-    f.top_k = top_k;
+    f.top_k = by_k ? top_k : 0;
     f.top_p = top_p;
     f.thr = reinterpret_cast<float*>(ws + fl.thr_off);
-    f.out_a = ws + fl.ta_off;
-    f.out_b = ws + fl.tb_off;
-    f.vec = (static_cast<size_t>(a.V) * eb) % 16 == 0 && reinterpret_cast<uintptr_t>(a.target) % 16 == 0 &&
-            reinterpret_cast<uintptr_t>(a.others) % 16 == 0 && reinterpret_cast<uintptr_t>(f.out_a) % 16 == 0 &&
-            reinterpret_cast<uintptr_t>(f.out_b) % 16 == 0;
+    f.row_ms = reinterpret_cast<float2*>(ws + fl.ms_off);
+    f.vec = rows16 ? 1 : 0;
     using ThrFn = void (*)(const FParams);
     ThrFn tfn = a.dtype == SPEC_BF16 ? threshold_kernel<Bf16> : threshold_kernel<F32>;
-    int dev = 0, tcap = 0;
+    int dev = 0, tcap = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess) e = dyn_smem_ceiling(tfn, dev, &tcap);
     if (e == cudaSuccess && F_SMEM > static_cast<size_t>(tcap)) e = cudaErrorInvalidValue;
     if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "threshold kernel attribute failed: %s", cudaGetErrorString(e));
-    tfn<<<static_cast<unsigned>(f.rows_n), FT_NT, F_SMEM, a.stream>>>(f);
+    const bool bound = by_k && top_k <= FB_MAX_K && rows16;
+    unsigned grid = static_cast<unsigned>(f.rows_n);
+    if (bound) {
+        if (a.dtype == SPEC_BF16) bound_kernel<Bf16><<<static_cast<unsigned>(f.rows_n), FB_NT, 0, a.stream>>>(f);
+        else bound_kernel<F32><<<static_cast<unsigned>(f.rows_n), FB_NT, 0, a.stream>>>(f);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "bound kernel launch failed: %s", cudaGetErrorString(e));
+        // the rows it left: CTAs striding over the rows, one wave of them
+        f.flagged_only = 1;
+        grid = static_cast<unsigned>(std::min<long long>(f.rows_n, 2LL * sms));
+    }
+    tfn<<<grid, FT_NT, F_SMEM, a.stream>>>(f);
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "threshold kernel launch failed: %s", cudaGetErrorString(e));
-    // the filtered copies: one CTA per row
-    if (a.dtype == SPEC_BF16) mask_kernel<Bf16><<<static_cast<unsigned>(f.rows_n), 256, 0, a.stream>>>(f);
-    else mask_kernel<F32><<<static_cast<unsigned>(f.rows_n), 256, 0, a.stream>>>(f);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "mask kernel launch failed: %s", cudaGetErrorString(e));
+    g_last_plan[0] = 0;
+    g_last_plan[1] = 0;
+    g_last_plan[2] = static_cast<int>(grid);
+    g_last_plan[3] = bound ? 6 : 7;
+    g_last_plan[4] = (a.V + PE - 1) / PE;
     Call c = a;
-    c.target = f.out_a;
-    c.others = f.out_b;
-    const bool aligned = (static_cast<size_t>(a.V) * eb) % 16 == 0 && a.V % CHUNK == 0;
-    return run_chain(c, aligned);
+    c.thr = f.thr;
+    return launch_draw(c, aligned, static_cast<const unsigned char*>(a.others), nullptr, f.row_ms, 0, 0,
+                       reinterpret_cast<unsigned*>(ws));
 }
 
 spec_status run(const Call& a) {
@@ -797,7 +818,7 @@ spec_status spec_hedge_feedback_push(void* state, const float* gamma, const int3
 
 size_t spec_filter_workspace_size(int B, int K, int V, spec_dtype dtype) {
     if (B < 0 || K < 0 || V < 1 || (dtype != SPEC_BF16 && dtype != SPEC_FP32)) return 0;
-    return filter_layout(B, K, V, dtype == SPEC_BF16 ? 2 : 4).total;
+    return filter_layout(B, K, V).total;
 }
 
 spec_status spec_verify_filtered(const void* target_logits, const void* draft_logits, spec_dtype dtype,

@@ -277,6 +277,7 @@ struct DParams {
     int32_t* out_tokens;           // [B, K+1]
     float* diag;                   // [B, K, 4] or null
     float* gamma_star;             // [B, K] or null (Cactus)
+    const float* thr;              // FILT: per statistics row, the logits below it count as -inf
     unsigned* status;
 };
 
@@ -357,12 +358,20 @@ __device__ __noinline__ FF flush_chunks(int mode, const typename E::Raw* qrt, co
     return acc;
 }
 
+// A chunk as the filter leaves it (FILT: logits below t are -inf), else as loaded.
+template <class E, bool FILT>
+__device__ __forceinline__ typename E::Raw filt(const typename E::Raw& r, float t) {
+    if constexpr (FILT) return E::mask(r, t);
+    else return r;
+}
+
 // Every large chunk of piece pc (more than a queue holds), read again from memory: its float-float mass minus
-// the fast one, eight lanes to a chunk (warp-collective; returns this lane's share).
-template <class E, bool AL>
+// the fast one, eight lanes to a chunk (warp-collective; returns this lane's share). FILT: logits below tt
+// (target row) and to (the other row) count as -inf.
+template <class E, bool AL, bool FILT>
 __device__ __noinline__ FF piece_exact(int mode, const unsigned char* trow, const unsigned char* orow, int pc, int V,
                                        float c, const PairOff po, const PairOffX px, const FFc& k, const float2* tab,
-                                       int tok, float hpatch, FF g, int lane) {
+                                       int tok, float hpatch, FF g, int lane, float tt, float to) {
     FF acc = {0.f, 0.f};
     const int e = lane & 7;
     for (int base = 0; base < PE / CHUNK; base += 4) {
@@ -371,8 +380,8 @@ __device__ __noinline__ FF piece_exact(int mode, const unsigned char* trow, cons
         float cm = 0.f;
         bool big = false;
         if (e0 < V) {
-            const typename E::Raw rt = E::template gload<AL>(trow, e0, V);
-            const typename E::Raw ro = mode == 1 ? E::template gload<AL>(orow, e0, V) : rt;
+            const typename E::Raw rt = filt<E, FILT>(E::template gload<AL>(trow, e0, V), tt);
+            const typename E::Raw ro = mode == 1 ? filt<E, FILT>(E::template gload<AL>(orow, e0, V), to) : rt;
             const int et = (tok >= e0 && tok < e0 + CHUNK) ? tok - e0 : -1;
             float ovl;
             cm = fast_chunk<E>(mode, rt, ro, c, po, et, hpatch, ovl);
@@ -422,8 +431,9 @@ struct DrawShared {
 // token (fast_chunk, chunk_values and elem_exact give the same values in both places).
 // draw_body runs it for one sequence on all DNT threads of one CTA: sequence blockIdx.x / cps and rank
 // cluster_ctarank() in a draw kernel launch (LAUNCHED), else sequence b_arg as the only CTA of its cluster
-// (cps = 1). d_smem: the bulk-copy slots and their mbarriers (bulk-copy mode).
-template <class E, bool AL, bool LAUNCHED>
+// (cps = 1). d_smem: the bulk-copy slots and their mbarriers (bulk-copy mode). FILT: the logits of each row
+// below its threshold p.thr[row] count as -inf (standardised sampling), wherever the draw reads them.
+template <class E, bool AL, bool LAUNCHED, bool FILT = false>
 __device__ __forceinline__ void draw_body(const DParams& p, DrawShared<E>& S, unsigned char* const d_smem,
                                           const int b_arg) {
     using Raw = typename E::Raw;
@@ -505,7 +515,8 @@ __device__ __forceinline__ void draw_body(const DParams& p, DrawShared<E>& S, un
         const bool tgt = q <= K;
         const int j = tgt ? q : q - K - 1;
         const long long r = tgt ? static_cast<long long>(b) * (K + 1) + j : p.rows_a_n + static_cast<long long>(b) * K + j;
-        const float x = j < K ? (tgt ? s_xt[j] : s_xd[j]) : NINF;
+        float x = j < K ? (tgt ? s_xt[j] : s_xd[j]) : NINF;
+        if constexpr (FILT) x = mask1(x, p.thr[r]);   // thresholds come from the grid before: read after its wait
         const MaxSum ms = d_row_stats(p, sp, r, c, lane);
         if (lane == 0) {
             const RowOff o = row_off(ms);
@@ -515,6 +526,9 @@ __device__ __forceinline__ void draw_body(const DParams& p, DrawShared<E>& S, un
             if (ms.s > 0.f) {
                 const FF l2 = ff_log2(FF{ms.s, 0.f}, p.k);
                 ll = __fsub_rn(__fsub_rn(-l2.hi, o.l), l2.lo);
+            }
+            if constexpr (FILT) {
+                if (j < K) (tgt ? s_xt[j] : s_xd[j]) = x;
             }
             if (tgt) {
                 s_nmt[j] = o.nm;
@@ -599,6 +613,11 @@ __device__ __forceinline__ void draw_body(const DParams& p, DrawShared<E>& S, un
         const int tok = cact ? s_tok[j] : -1;
         const FF gx = cact ? FF{s_g[j].x, s_g[j].y} : FF{0.f, 0.f};
         const float hpatch = gx.hi;
+        float tt = 0.f, to = 0.f;   // the rows' filter thresholds
+        if constexpr (FILT) {
+            tt = p.thr[static_cast<size_t>(b) * (K + 1) + j];
+            to = mode == 1 ? p.thr[p.rows_a_n + static_cast<long long>(b) * K + j] : tt;
+        }
         // bulk copy of piece pc of both rows (the target alone for a bonus row) into this warp's slot
         auto issue = [&](int pc) {
             if (lane == 0 && ok_all) {
@@ -624,7 +643,15 @@ __device__ __forceinline__ void draw_body(const DParams& p, DrawShared<E>& S, un
                 const int nch = (min(PE, V - pc * PE) + CHUNK - 1) / CHUNK;
                 piece_load<E>(slot, nch, lane, rt);
                 if (mode == 1) piece_load<E>(slot + PIECE_BYTES, nch, lane, ro);
-                else {
+                if constexpr (FILT) {
+#pragma unroll
+                    for (int q = 0; q < PCH; ++q) rt[q] = E::mask(rt[q], tt);
+                    if (mode == 1) {
+#pragma unroll
+                        for (int q = 0; q < PCH; ++q) ro[q] = E::mask(ro[q], to);
+                    }
+                }
+                if (mode != 1) {
 #pragma unroll
                     for (int q = 0; q < PCH; ++q) ro[q] = rt[q];
                 }
@@ -635,8 +662,8 @@ __device__ __forceinline__ void draw_body(const DParams& p, DrawShared<E>& S, un
 #pragma unroll
                 for (int q = 0; q < PCH; ++q) {
                     const int e0 = pc * PE + (lane + 32 * q) * CHUNK;
-                    rt[q] = E::template gload<AL>(trow, e0, V);
-                    ro[q] = mode == 1 ? E::template gload<AL>(orow, e0, V) : rt[q];
+                    rt[q] = filt<E, FILT>(E::template gload<AL>(trow, e0, V), tt);
+                    ro[q] = mode == 1 ? filt<E, FILT>(E::template gload<AL>(orow, e0, V), to) : rt[q];
                 }
             }
             FF loc = {0.f, 0.f};
@@ -663,7 +690,8 @@ __device__ __forceinline__ void draw_body(const DParams& p, DrawShared<E>& S, un
                 }
             }
             if (nq > D_QCH)   // a flat row: every large chunk of the piece again, from memory
-                loc = ff_add(loc, piece_exact<E, AL>(mode, trow, orow, pc, V, c, po, px, p.k, s_tab, tok, hpatch, gx, lane));
+                loc = ff_add(loc, piece_exact<E, AL, FILT>(mode, trow, orow, pc, V, c, po, px, p.k, s_tab, tok, hpatch,
+                                                                 gx, lane, tt, to));
             else if (nq)
                 loc = ff_add(loc, flush_chunks<E>(mode, s_qrt[warp], s_qro[warp], s_qcm[warp], s_qet[warp], nq, px, p.k,
                                                   s_tab, gx, lane));
@@ -700,13 +728,13 @@ __device__ __forceinline__ void draw_body(const DParams& p, DrawShared<E>& S, un
                         const int tk = s_tok[j];
                         double all = 0.0;
                         for (int e0 = lane * CHUNK; e0 < V; e0 += 32 * CHUNK) {
-                            const Raw rt = E::template gload<AL>(trow, e0, V);
+                            const Raw rt = filt<E, FILT>(E::template gload<AL>(trow, e0, V), tt);
                             float2 unused = make_float2(0.f, 0.f);
                             const int et = (tk >= e0 && tk < e0 + CHUNK) ? tk - e0 : -1;
                             all += static_cast<double>(chunk_mass_patched<E>(2, rt, rt, c, po, et, ht, unused));
                         }
                         const double tpd = static_cast<double>(u) * warp_sum(all);
-                        emitted = scan_pick<E, AL>(c, trow, trow, 2, 0, V, po, tk, ht, tpd, 0.0, lane);
+                        emitted = scan_pick<E, AL, FILT>(c, trow, trow, 2, 0, V, po, tk, ht, tpd, 0.0, lane, tt, tt);
                         plan.ft = -2;
                     } else {
                         const FF tp = ff_mulf(Z, u);
@@ -767,8 +795,8 @@ __device__ __forceinline__ void draw_body(const DParams& p, DrawShared<E>& S, un
                 if (threadIdx.x == 0) s_pn = 0;
                 __syncthreads();
                 if (ch < nch) {
-                    rt = E::template gload<AL>(trow, e0, V);
-                    ro = mode == 1 ? E::template gload<AL>(orow, e0, V) : rt;
+                    rt = filt<E, FILT>(E::template gload<AL>(trow, e0, V), tt);
+                    ro = mode == 1 ? filt<E, FILT>(E::template gload<AL>(orow, e0, V), to) : rt;
                     float ovl, unused = 0.f;
                     const float cm = fast_chunk<E>(mode, rt, ro, c, po, et, hpatch, ovl);
                     chunk_values<E>(mode, rt, ro, c, po, et, hpatch, v, unused);
@@ -786,8 +814,8 @@ __device__ __forceinline__ void draw_body(const DParams& p, DrawShared<E>& S, un
                         if (li < npl) {
                             const int cj = s_pl[li];
                             const int c0 = ft * PE + cj * CHUNK;
-                            const Raw xt = E::template gload<AL>(trow, c0, V);
-                            const Raw xd = mode == 1 ? E::template gload<AL>(orow, c0, V) : xt;
+                            const Raw xt = filt<E, FILT>(E::template gload<AL>(trow, c0, V), tt);
+                            const Raw xd = mode == 1 ? filt<E, FILT>(E::template gload<AL>(orow, c0, V), to) : xt;
                             const float2 xt2 = E::pair(xt, e >> 1), xd2 = E::pair(xd, e >> 1);
                             const int cet = (tok >= c0 && tok < c0 + CHUNK) ? tok - c0 : -1;
                             r = elem_exact(mode, (e & 1) ? xt2.y : xt2.x, (e & 1) ? xd2.y : xd2.x, px, p.k, s_tab, e == cet, gx);
@@ -869,13 +897,13 @@ __device__ __forceinline__ void draw_body(const DParams& p, DrawShared<E>& S, un
 }
 
 // One cluster of cps CTAs per sequence (CTA rank = blockIdx.x % cps).
-template <class E, bool AL>
+template <class E, bool AL, bool FILT = false>
 __global__ void __launch_bounds__(DNT, 1) draw_kernel(const __grid_constant__ DParams p) {
     // dynamic shared memory (bulk-copy mode): one slot per warp holding a target piece and a draft piece,
     // then one mbarrier per warp
     extern __shared__ __align__(128) unsigned char d_smem[];
     __shared__ DrawShared<E> S;
-    draw_body<E, AL, true>(p, S, d_smem, 0);
+    draw_body<E, AL, true, FILT>(p, S, d_smem, 0);
 }
 
 // ------------------------------------------------------------------------------------------------

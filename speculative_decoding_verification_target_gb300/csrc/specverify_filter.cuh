@@ -9,8 +9,8 @@
 //     top_p of the kept total. Ties at a threshold are all kept (the kept set depends on values only). Once
 //     the elements still in play fit in shared memory (at most F_CAP keys), one more pass over the row copies
 //     them there and the remaining passes read only them;
-//   - mask_kernel: writes the filtered rows (kept logits unchanged, the others -inf) into the caller's
-//     workspace, and the chain kernels run on them.
+//   - the statistics and draw kernels then read the caller's rows as they are and replace every logit below
+//     its row's threshold by -inf as it arrives in registers (their FILT form), so no filtered copy is made.
 // The histograms of a pass are integer sums, so they do not depend on the order of the additions: counts, and
 // masses in 64-bit fixed point (2^-44 units; a mass 2^((x - M) c) is at most 1 and a row holds at most 2^18
 // logits, so a bin cannot overflow). Each thread adds into its own column of the shared-memory histograms (no
@@ -66,9 +66,9 @@ struct FParams {
     float c;                       // log2(e) / temperature
     int top_k;                     // 0 or V: none
     float top_p;                   // >= 1: none
-    float* thr;                    // [rows_n] threshold value (-inf: nothing filtered)
-    unsigned char* out_a;          // filtered copies, same layout as rows_a / rows_b
-    unsigned char* out_b;
+    float* thr;                    // [rows_n] threshold value (-inf: nothing filtered; NaN: left to threshold_kernel)
+    float2* row_ms;                // [rows_n] (max, sum of 2^((x - max) c)) over the logits the filter keeps
+    int flagged_only;              // threshold_kernel: only the rows whose threshold is NaN (else every row)
     int vec;                       // every row starts on 16 bytes and holds whole 16-byte words
 };
 
@@ -159,8 +159,25 @@ __device__ __forceinline__ void for_row_keys(const unsigned char* row, int V, bo
     }
 }
 
+// Sum of one float per thread in a fixed order (warp trees, then the warps in order): the same bits on every
+// run. Every thread of the CTA calls it; thread 0 gets the sum.
+template <int NT>
+__device__ __forceinline__ float cta_sum_fixed(float v, float* s_red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xffffffffu, v, o);
+    if (lane == 0) s_red[warp] = v;
+    __syncthreads();
+    float t = 0.f;
+    if (threadIdx.x == 0)
+        for (int w = 0; w < NT / 32; ++w) t += s_red[w];
+    __syncthreads();
+    return t;
+}
+
+// The threshold and the kept logits' (max, sum) of row r (all FT_NT threads of the CTA).
 template <class E>
-__global__ void __launch_bounds__(FT_NT) threshold_kernel(const __grid_constant__ FParams p) {
+__device__ __forceinline__ void threshold_row(const FParams& p, const long long r) {
     using KT = typename FKey<E>::K;
     constexpr int BITS = FKey<E>::BITS;
     extern __shared__ __align__(16) unsigned char f_smem[];
@@ -174,8 +191,8 @@ __global__ void __launch_bounds__(FT_NT) threshold_kernel(const __grid_constant_
     __shared__ KT s_kmax[FT_W];
     __shared__ KT s_tmax[FT_NT];                 // top-k by bound: every thread's largest key
     __shared__ KT s_bound, s_rowmax;
+    __shared__ float s_red[FT_W];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const long long r = blockIdx.x;
     const int V = p.V;
     const bool vec = p.vec != 0;
     const size_t row_bytes = static_cast<size_t>(V) * E::BYTES;
@@ -417,53 +434,316 @@ __global__ void __launch_bounds__(FT_NT) threshold_kernel(const __grid_constant_
         if (!filtered || prefix > lo) lo = prefix;
         filtered = true;
     }
-    if (tid == 0) p.thr[r] = filtered ? FKey<E>::value_of(lo) : NINF;
+    if (!have_max) {
+        KT km = 0;
+        for_row_keys<E>(row, V, vec, [&](KT k, bool ok) { km = max(km, ok ? k : KT(0)); });
+        kmax = cta_kmax(km);
+    }
+    // the kept logits (every value at or above the threshold, the row's largest among them): their (max, sum)
+    // for the draw, which masks by the same float comparison
+    const float th = filtered ? FKey<E>::value_of(lo) : NINF;
+    const float M = FKey<E>::value_of(kmax);
+    float sacc = 0.f;
+    for_row_keys<E>(row, V, vec, [&](KT k, bool ok) {
+        const float x = FKey<E>::value_of(k);
+        if (ok && x >= th) sacc += ex2((x - M) * p.c);
+    });
+    const float ssum = cta_sum_fixed<FT_NT>(sacc, s_red);
+    if (tid == 0) {
+        p.thr[r] = th;
+        p.row_ms[r] = make_float2(M, ssum);
+    }
 }
 
-// The filtered copies, one CTA per row: logits at or above the row's threshold, -inf elsewhere (16-byte words
-// when every row allows them).
+// One CTA per row (flagged_only: the CTAs stride over the rows and take those left with a NaN threshold).
 template <class E>
-__global__ void __launch_bounds__(256) mask_kernel(const __grid_constant__ FParams p) {
+__global__ void __launch_bounds__(FT_NT) threshold_kernel(const __grid_constant__ FParams p) {
+    for (long long r = blockIdx.x; r < p.rows_n; r += gridDim.x) {
+        if (p.flagged_only && !isnan(p.thr[r])) continue;
+        threshold_row<E>(p, r);
+        __syncthreads();
+    }
+}
+
+// ------------------------------------------------------------------------------------------------
+// top-k through line maxima (rows of whole 16-byte words, 0 < top_k <= FB_MAX_K < V)
+// ------------------------------------------------------------------------------------------------
+// A line is 8 words (128 bytes) of a row. The lines' maxima are maxima of disjoint sets, so the k-th
+// largest of them is at most the row's k-th largest logit: every logit top-k keeps lies in a line whose
+// maximum reaches it. One CTA per row:
+//   1. reads the row once (evict-last), keeping each line's maximum as a 16-bit key in shared memory (the
+//      upper half of the key for fp32, which rounds it down and keeps the bound valid);
+//   2. selects the k-th largest line key by two 8-bit radix passes over shared memory (the bound);
+//   3. re-reads only the lines whose maximum reaches the bound (mostly from L2) and lists their logits at or
+//      above it: at least k of them, all that top-k can keep;
+//   4. sorts the list (bitonic, descending keys): the k-th key is the top-k threshold; top-p scans the kept
+//      keys' fixed-point masses from the top (the same masses and the same rule as threshold_kernel, so the
+//      same threshold);
+//   5. writes the threshold and the kept logits' (max, sum).
+// A row whose list would pass F_CAP keys gets a NaN threshold and is left to threshold_kernel.
+constexpr int FB_NT = 256;
+constexpr int FB_W = FB_NT / 32;
+constexpr int FB_MAX_K = F_CAP / 4;
+constexpr int FB_MAX_V = 262144;                 // the library's largest vocabulary
+constexpr int FB_LINE_WORDS = 8;
+constexpr int FB_U = 8;                          // words a thread has in flight in the first read
+
+// a 16-byte word of -inf logits, and the largest value of a word
+template <class E>
+__device__ __forceinline__ uint4 f_ninf_word() {
+    const uint32_t x = E::BYTES == 2 ? 0xFF80FF80u : 0xFF800000u;
+    return make_uint4(x, x, x, x);
+}
+template <class E>
+__device__ __forceinline__ float f_word_max(const uint4& w) {
+    if constexpr (E::BYTES == 2) {
+        const uint32_t m2 = bf16x2_max(bf16x2_max(w.x, w.y), bf16x2_max(w.z, w.w));
+        return fmaxf(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xFFFF0000u));
+    } else {
+        return fmaxf(fmaxf(__uint_as_float(w.x), __uint_as_float(w.y)), fmaxf(__uint_as_float(w.z), __uint_as_float(w.w)));
+    }
+}
+
+// a line's maximum value as a 16-bit key that is never above the key of the logit it came from
+template <class E>
+__device__ __forceinline__ uint32_t line_key16(float v) {
+    const uint32_t k = key_at_most<E>(v);
+    return E::BYTES == 2 ? k : (k >> 16);
+}
+
+template <class E>
+__global__ void __launch_bounds__(FB_NT, 4) bound_kernel(const __grid_constant__ FParams p) {
+    using KT = typename FKey<E>::K;
+    static_assert(FB_MAX_V * E::BYTES / (16 * FB_LINE_WORDS) * 2 <= F_CAP * 4, "line keys fit the list's space");
+    static_assert(F_CAP * 2 <= FB_W * 256 * 4, "line list fits the histograms' space");
+    __shared__ __align__(16) uint32_t s_a[F_CAP];         // line keys (uint16), then the candidate keys
+    __shared__ __align__(16) uint32_t s_b[FB_W * 256];    // per-warp 8-bit histograms, then the line list (uint16)
+    __shared__ unsigned s_wt[FB_W];
+    __shared__ unsigned long long s_wm[FB_W];
+    __shared__ float s_red[FB_W];
+    __shared__ unsigned s_n, s_sel, s_above, s_nk, s_first;
+    uint16_t* const lkey = reinterpret_cast<uint16_t*>(s_a);
+    uint16_t* const lines = reinterpret_cast<uint16_t*>(s_b);
+    KT* const cand = s_a;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const long long r = blockIdx.x;
-    const size_t V = static_cast<size_t>(p.V);
-    const size_t row_bytes = V * E::BYTES;
-    const float t = p.thr[r];
-    const unsigned char* src = f_row(p, r, row_bytes);
-    unsigned char* dst = r < p.rows_a_n ? p.out_a + static_cast<size_t>(r) * row_bytes
-                                        : p.out_b + static_cast<size_t>(r - p.rows_a_n) * row_bytes;
-    auto keep16 = [&](uint32_t b) -> uint32_t {   // a bf16 in the low half of b
-        return __uint_as_float(b << 16) >= t ? b : 0xFF80u;
-    };
-    auto keep32 = [&](uint32_t b) -> uint32_t { return __uint_as_float(b) >= t ? b : 0xFF800000u; };
-    if (p.vec) {
-        const uint4* s4 = reinterpret_cast<const uint4*>(src);
-        uint4* d4 = reinterpret_cast<uint4*>(dst);
-        const size_t n4 = row_bytes / 16;
-#pragma unroll 4
-        for (size_t i = threadIdx.x; i < n4; i += blockDim.x) {
-            uint4 w = __ldg(s4 + i);
-            if constexpr (E::BYTES == 2) {
-                w.x = keep16(w.x & 0xFFFFu) | (keep16(w.x >> 16) << 16);
-                w.y = keep16(w.y & 0xFFFFu) | (keep16(w.y >> 16) << 16);
-                w.z = keep16(w.z & 0xFFFFu) | (keep16(w.z >> 16) << 16);
-                w.w = keep16(w.w & 0xFFFFu) | (keep16(w.w >> 16) << 16);
-            } else {
-                w.x = keep32(w.x);
-                w.y = keep32(w.y);
-                w.z = keep32(w.z);
-                w.w = keep32(w.w);
+    const int V = p.V, k = p.top_k;
+    const size_t row_bytes = static_cast<size_t>(V) * E::BYTES;
+    const uint4* const w4 = reinterpret_cast<const uint4*>(f_row(p, r, row_bytes));
+    const int n4 = static_cast<int>(row_bytes / 16);
+    const int n_lines = (n4 + FB_LINE_WORDS - 1) / FB_LINE_WORDS;
+
+    // ---- 1. line maxima: the eight lanes of a line each take one word ----
+    {
+        const uint64_t pol = policy_evict_last();
+        const int n_it = (n4 + FB_NT - 1) / FB_NT;
+        for (int it0 = 0; it0 < n_it; it0 += FB_U) {
+            uint4 w[FB_U];
+#pragma unroll
+            for (int u = 0; u < FB_U; ++u) {
+                const int i = (it0 + u) * FB_NT + tid;
+                w[u] = i < n4 ? ld_word(w4 + i, pol) : f_ninf_word<E>();
             }
-            d4[i] = w;
+#pragma unroll
+            for (int u = 0; u < FB_U; ++u) {
+                if (it0 + u >= n_it) break;
+                float m = f_word_max<E>(w[u]);
+#pragma unroll
+                for (int o = 1; o < FB_LINE_WORDS; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                const int line = (it0 + u) * (FB_NT / FB_LINE_WORDS) + tid / FB_LINE_WORDS;
+                if ((lane & (FB_LINE_WORDS - 1)) == 0 && line < n_lines) lkey[line] = static_cast<uint16_t>(line_key16<E>(m));
+            }
         }
+    }
+    __syncthreads();
+
+    // ---- 2. the k-th largest line key (every key when there are fewer than k lines) ----
+    // one 8-bit digit: among the keys whose high byte is `hi` (hi < 0: all), the bin where the count from the
+    // top first reaches need; leaves the bin and the count above it in s_sel / s_above
+    auto select_byte = [&](int shift, int hi, unsigned need) {
+        for (int i = tid; i < FB_W * 256; i += FB_NT) s_b[i] = 0u;
+        __syncthreads();
+        uint32_t* const h = s_b + warp * 256;
+        for (int l = tid; l < n_lines; l += FB_NT) {
+            const uint32_t key = lkey[l];
+            if (hi < 0 || static_cast<int>(key >> 8) == hi) atomicAdd(&h[(key >> shift) & 255u], 1u);
+        }
+        __syncthreads();
+        const int bin = 255 - tid;   // thread t holds bin 255 - t: the scan runs from the top bin down
+        unsigned c = 0u;
+#pragma unroll
+        for (int w2 = 0; w2 < FB_W; ++w2) c += s_b[w2 * 256 + bin];
+        unsigned incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (lane == 31) s_wt[warp] = incl;
+        __syncthreads();
+        for (int w2 = 0; w2 < warp; ++w2) incl += s_wt[w2];
+        if (incl >= need && incl - c < need) {
+            s_sel = static_cast<unsigned>(bin);
+            s_above = incl - c;
+        }
+        __syncthreads();
+    };
+    uint32_t bound16 = 0u;
+    if (n_lines >= k) {
+        select_byte(8, -1, static_cast<unsigned>(k));
+        const unsigned hi = s_sel, above = s_above;
+        select_byte(0, static_cast<int>(hi), static_cast<unsigned>(k) - above);
+        bound16 = (hi << 8) | s_sel;
+    }
+    // as a key of the row's type; a bound whose value is zero becomes the key of -0, so that every logit the
+    // draw's float comparison keeps (-0 >= +0) is listed
+    const KT bound = key_at_most<E>(FKey<E>::value_of(E::BYTES == 2 ? static_cast<KT>(bound16) : static_cast<KT>(bound16 << 16)));
+    const uint32_t bound_line = E::BYTES == 2 ? bound : (bound >> 16);   // a line holding such a logit reaches it
+
+    // ---- 3. the lines that reach the bound, then their logits at or above it ----
+    if (tid == 0) s_n = 0u;
+    __syncthreads();
+    for (int l0 = 0; l0 < n_lines; l0 += FB_NT) {
+        const int l = l0 + tid;
+        const bool in = l < n_lines && lkey[l] >= bound_line;
+        const unsigned bal = __ballot_sync(0xffffffffu, in);
+        if (bal) {
+            unsigned base = 0u;
+            if (lane == 0) base = atomicAdd(&s_n, static_cast<unsigned>(__popc(bal)));
+            base = __shfl_sync(0xffffffffu, base, 0);
+            const unsigned at = base + static_cast<unsigned>(__popc(bal & ((1u << lane) - 1u)));
+            if (in && at < static_cast<unsigned>(F_CAP)) lines[at] = static_cast<uint16_t>(l);
+        }
+    }
+    __syncthreads();
+    const unsigned nl = s_n;   // each listed line holds a logit at or above the bound
+    __syncthreads();
+    if (nl <= static_cast<unsigned>(F_CAP)) {
+        if (tid == 0) s_n = 0u;
+        __syncthreads();
+        const uint64_t pol = policy_evict_first();   // the row's last read
+        const int g = tid / FB_LINE_WORDS, sub = tid % FB_LINE_WORDS;
+        constexpr int GPB = FB_NT / FB_LINE_WORDS;   // lines a CTA reads per step
+        constexpr int UG = 4;
+        for (int base = 0; base < static_cast<int>(nl); base += GPB * UG) {
+            uint4 w[UG];
+            bool ok[UG];
+#pragma unroll
+            for (int u = 0; u < UG; ++u) {
+                const int li = base + u * GPB + g;
+                const int wi = li < static_cast<int>(nl) ? static_cast<int>(lines[li]) * FB_LINE_WORDS + sub : n4;
+                ok[u] = wi < n4;
+                w[u] = ok[u] ? ld_word(w4 + wi, pol) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < UG; ++u) {
+                const uint32_t uu[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                    for (int h = 0; h < (E::BYTES == 2 ? 2 : 1); ++h) {
+                        const KT key = E::BYTES == 2 ? FKey<E>::of_bits(h ? (uu[j] >> 16) : (uu[j] & 0xFFFFu))
+                                                     : FKey<E>::of_bits(uu[j]);
+                        const bool in = ok[u] && key >= bound;
+                        const unsigned bal = __ballot_sync(0xffffffffu, in);
+                        if (bal) {
+                            unsigned b0 = 0u;
+                            if (lane == 0) b0 = atomicAdd(&s_n, static_cast<unsigned>(__popc(bal)));
+                            b0 = __shfl_sync(0xffffffffu, b0, 0);
+                            const unsigned at = b0 + static_cast<unsigned>(__popc(bal & ((1u << lane) - 1u)));
+                            if (in && at < static_cast<unsigned>(F_CAP)) cand[at] = key;
+                        }
+                    }
+                }
+            }
+        }
+        __syncthreads();
+    }
+    const unsigned n = nl <= static_cast<unsigned>(F_CAP) ? s_n : 0xFFFFFFFFu;
+    if (n > static_cast<unsigned>(F_CAP) || n < static_cast<unsigned>(k)) {   // too many: threshold_kernel takes the row
+        if (tid == 0) p.thr[r] = __uint_as_float(0x7FC00000u);
         return;
     }
-    for (size_t e = threadIdx.x; e < V; e += blockDim.x) {
-        if constexpr (E::BYTES == 2) {
-            const uint16_t b = reinterpret_cast<const uint16_t*>(src)[e];
-            reinterpret_cast<uint16_t*>(dst)[e] = static_cast<uint16_t>(keep16(b));
-        } else {
-            reinterpret_cast<uint32_t*>(dst)[e] = keep32(reinterpret_cast<const uint32_t*>(src)[e]);
+
+    // ---- 4. sort the list, descending keys (bitonic over the next power of two, padded with key 0) ----
+    int P = 1;
+    while (P < static_cast<int>(n)) P <<= 1;
+    for (int i = static_cast<int>(n) + tid; i < P; i += FB_NT) cand[i] = 0u;
+    __syncthreads();
+    for (int size = 2; size <= P; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int q = tid; q < P / 2; q += FB_NT) {
+                const int i = 2 * q - (q & (stride - 1));
+                const KT a = cand[i], b = cand[i + stride];
+                if ((i & size) == 0 ? a < b : a > b) {
+                    cand[i] = b;
+                    cand[i + stride] = a;
+                }
+            }
+            __syncthreads();
         }
+    }
+    // keys at or above cand[t - 1] (ties with it included): nk of them
+    auto count_ge = [&](KT t) -> unsigned {
+        if (tid == 0) s_nk = 0u;
+        __syncthreads();
+        for (int i = tid; i < static_cast<int>(n); i += FB_NT)
+            if (cand[i] >= t && (i + 1 == static_cast<int>(n) || cand[i + 1] < t)) s_nk = static_cast<unsigned>(i + 1);
+        __syncthreads();
+        return s_nk;
+    };
+    KT lo = cand[k - 1];
+    const float M = FKey<E>::value_of(cand[0]);
+    if (p.top_p > 0.f && p.top_p < 1.f) {
+        const unsigned nk = count_ge(lo);
+        // each thread a run of the sorted keys: its fixed-point masses, then an exclusive scan across the CTA
+        const int per = (static_cast<int>(nk) + FB_NT - 1) / FB_NT;
+        const int i0 = min(static_cast<int>(nk), tid * per), i1 = min(static_cast<int>(nk), i0 + per);
+        auto mass = [&](int i) -> unsigned long long {
+            return __float2ull_rz(ex2((FKey<E>::value_of(cand[i]) - M) * p.c) * F_FIX);
+        };
+        unsigned long long loc = 0ull;
+        for (int i = i0; i < i1; ++i) loc += mass(i);
+        unsigned long long incl = loc;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (lane == 31) s_wm[warp] = incl;
+        if (tid == 0) s_first = 0xFFFFFFFFu;
+        __syncthreads();
+        unsigned long long before = 0ull, total = 0ull;
+        for (int w2 = 0; w2 < FB_W; ++w2) {
+            if (w2 < warp) before += s_wm[w2];
+            total += s_wm[w2];
+        }
+        // top_p of the total, rounded up: the smallest fixed-point mass that reaches it
+        const unsigned long long need =
+            static_cast<unsigned long long>(ceil(static_cast<double>(p.top_p) * static_cast<double>(total)));
+        unsigned long long run = before + incl - loc;
+        for (int i = i0; i < i1; ++i) {
+            run += mass(i);
+            if (run >= need) {
+                atomicMin(&s_first, static_cast<unsigned>(i));
+                break;
+            }
+        }
+        __syncthreads();
+        lo = cand[s_first];
+    }
+
+    // ---- 5. threshold, and the kept logits' (max, sum) by the draw's float comparison ----
+    const float th = FKey<E>::value_of(lo);
+    float sacc = 0.f;
+    for (int i = tid; i < static_cast<int>(n); i += FB_NT) {
+        const float x = FKey<E>::value_of(cand[i]);
+        if (x >= th) sacc += ex2((x - M) * p.c);
+    }
+    const float ssum = cta_sum_fixed<FB_NT>(sacc, s_red);
+    if (tid == 0) {
+        p.thr[r] = th;
+        p.row_ms[r] = make_float2(M, ssum);
     }
 }
 

@@ -20,7 +20,9 @@ int spec_debug_set_stats_grid(int ctas);
 /* The launch plan of the last call made on this thread, as five ints: 0, ring slots per warp, CTAs
  * launched, kernel (0: the statistics pass of spec_verify / spec_cactus_verify / spec_verify_static; 2: the
  * gamma kernel of spec_counterfactual_gamma, which parks rows in tensor memory; 3: the argmax pass of
- * spec_greedy_verify; 5: the one-launch gamma and chain kernel), pieces per row. out5 is host memory.
+ * spec_greedy_verify; 5: the one-launch gamma and chain kernel; 6: spec_verify_filtered through the
+ * line-maxima bound kernel, then the radix threshold kernel on the rows it left; 7: spec_verify_filtered
+ * through the radix threshold kernel alone), pieces per row. out5 is host memory.
  * Returns 0, or -1 for a NULL pointer. */
 int spec_debug_last_plan(int* out5);
 

@@ -61,6 +61,15 @@ struct Bf16 {
     __device__ static float at(const unsigned char* slot, int e) {
         return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(slot)[e]) << 16);
     }
+    // a chunk with every logit below t replaced by -inf (standardised sampling's filter)
+    __device__ static Raw mask(const Raw& r, float t) {
+        auto m = [t](uint32_t w) -> uint32_t {
+            const uint32_t lo = __uint_as_float(w << 16) >= t ? (w & 0xFFFFu) : 0xFF80u;
+            const uint32_t hi = __uint_as_float(w & 0xFFFF0000u) >= t ? (w & 0xFFFF0000u) : 0xFF800000u;
+            return lo | hi;
+        };
+        return make_uint4(m(r.x), m(r.y), m(r.z), m(r.w));
+    }
     // element-wise staging for rows that are not 16-byte aligned (pads the last chunk with -inf)
     __device__ static void copy_slice(unsigned char* slot, const unsigned char* src, int n_el, int lane) {
         const uint16_t* s = reinterpret_cast<const uint16_t*>(src);
@@ -129,6 +138,14 @@ struct F32 {
     }
     __device__ static float max_fin(Max m) { return m; }
     __device__ static float at(const unsigned char* slot, int e) { return reinterpret_cast<const float*>(slot)[e]; }
+    // a chunk with every logit below t replaced by -inf (standardised sampling's filter)
+    __device__ static Raw mask(const Raw& r, float t) {
+        auto m = [t](float x) { return x >= t ? x : __uint_as_float(0xFF800000u); };
+        Raw o;
+        o.a = make_float4(m(r.a.x), m(r.a.y), m(r.a.z), m(r.a.w));
+        o.b = make_float4(m(r.b.x), m(r.b.y), m(r.b.z), m(r.b.w));
+        return o;
+    }
     __device__ static void copy_slice(unsigned char* slot, const unsigned char* src, int n_el, int lane) {
         const uint32_t* s = reinterpret_cast<const uint32_t*>(src);
         uint32_t* d = reinterpret_cast<uint32_t*>(slot);
@@ -244,6 +261,9 @@ __device__ __noinline__ void cactus_scalars_kl(float q, float delta, float& gsta
     log2s = log2f(s);
     scale = s;
 }
+
+// A logit kept by the filter (t = -inf keeps every finite or infinite logit), else -inf.
+__device__ __forceinline__ float mask1(float x, float t) { return x >= t ? x : __uint_as_float(0xFF800000u); }
 
 // ------------------------------------------------------------------------------------------------
 // per-chunk arithmetic
@@ -546,9 +566,11 @@ __device__ __forceinline__ void piece_stats(const typename E::Raw (&r)[PCH], flo
 // ------------------------------------------------------------------------------------------------
 // inverse CDF
 // ------------------------------------------------------------------------------------------------
-template <class E, bool AL>
+// FILT: logits of the target row below tt, and of the other row below to, count as -inf.
+template <class E, bool AL, bool FILT = false>
 __device__ __noinline__ int scan_pick(float c, const unsigned char* trow, const unsigned char* orow, int mode, int e_begin,
-                         int e_end, PairOff o, int tok, float ht, double tp, double before, int lane) {
+                         int e_end, PairOff o, int tok, float ht, double tp, double before, int lane, float tt = 0.f,
+                         float to = 0.f) {
     using Raw = typename E::Raw;
     int last_pos = -1;
     for (int base = e_begin; base < e_end; base += 32 * CHUNK) {
@@ -558,8 +580,12 @@ __device__ __noinline__ int scan_pick(float c, const unsigned char* trow, const 
 #pragma unroll
         for (int q = 0; q < 8; ++q) v[q] = 0.f;
         if (e0 < e_end) {
-            const Raw rt = E::template gload<AL>(trow, e0, e_end);
-            const Raw ro = mode == 1 ? E::template gload<AL>(orow, e0, e_end) : rt;
+            Raw rt = E::template gload<AL>(trow, e0, e_end);
+            Raw ro = mode == 1 ? E::template gload<AL>(orow, e0, e_end) : rt;
+            if constexpr (FILT) {
+                rt = E::mask(rt, tt);
+                ro = E::mask(ro, mode == 1 ? to : tt);
+            }
             const int et = (tok >= e0 && tok < e0 + CHUNK) ? tok - e0 : -1;
             float ovl = 0.f;
             chunk_values<E>(mode, rt, ro, c, o, et, ht, v, ovl);

@@ -660,6 +660,10 @@ def test_verify_filtered_small(V, dtype, top_k, top_p):
     g = to_device(inp)
     out = sv.verify_filtered(g["target"], g["draft"], g["tokens"], g["seeds"], w.temperature, top_k, top_p)
     torch.cuda.synchronize()
+    # top-k up to 1024 on rows of whole 16-byte words takes the line-maxima bound kernel (6), the rest the
+    # radix threshold kernel alone (7)
+    eb = 2 if dtype == "bf16" else 4
+    assert sv.last_plan()["kernel"] == (6 if 0 < top_k <= 1024 and top_k < V and (V * eb) % 16 == 0 else 7)
     # A top-p threshold can land one value off the oracle's when the mass boundary falls within fp32
     # resolution of a partial sum; that moves p(t), Z and the CDF by about one element's mass, which the
     # bar's tolerance and near-tie rules cover.
@@ -689,6 +693,31 @@ def test_verify_filtered_ties():
             assert_diag(out, ref)
             assert_chain(out, ref, K)
             assert sv.read_status(out["workspace"]) == 0
+
+
+@pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16])
+def test_verify_filtered_signed_zeros(dt):
+    """Thresholds at zero on rows full of +0 and -0: the keys order -0 below +0, the kept set and the row
+    normalisers take both (a float comparison), as the oracle's values do."""
+    B, K, V = 4, 3, 2000
+    gen = torch.Generator().manual_seed(11)
+    levels = torch.tensor([-1.0, -0.0, 0.0, 0.5], dtype=torch.float32)
+    target = levels[torch.randint(0, 4, (B, K + 1, V), generator=gen)]
+    target[:, :, ::97] = 2.0
+    draft = levels[torch.randint(0, 4, (B, K, V), generator=gen)]
+    tokens = torch.randint(0, V, (B, K), generator=gen, dtype=torch.int32)
+    seeds = torch.arange(B, dtype=torch.int64) + 5
+    n_pos = int((target[0, 0] > 0).sum())
+    for top_k, top_p in ((n_pos + 10, 1.0), (n_pos + 10, 0.97), (900, 0.999)):
+        t, d = target.to(dt), draft.to(dt)
+        ref = oracle.verify_filtered(host(t), host(d), tokens.numpy(), seeds.numpy().astype(np.uint64), 0.8,
+                                     top_k, top_p)
+        out = sv.verify_filtered(t.cuda(), d.cuda(), tokens.cuda(), seeds.cuda(), 0.8, top_k, top_p)
+        torch.cuda.synchronize()
+        assert sv.last_plan()["kernel"] == 6
+        assert_diag(out, ref)
+        assert_chain(out, ref, K)
+        assert sv.read_status(out["workspace"]) == 0
 
 
 def test_verify_filtered_without_filters_is_verify():
