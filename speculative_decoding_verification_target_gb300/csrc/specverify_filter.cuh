@@ -476,7 +476,8 @@ __global__ void __launch_bounds__(FT_NT) threshold_kernel(const __grid_constant_
 //   2. selects the k-th largest line key by two 8-bit radix passes over shared memory (the bound);
 //   3. re-reads only the lines whose maximum reaches the bound (mostly from L2) and lists their logits at or
 //      above it: at least k of them, all that top-k can keep;
-//   4. sorts the list (bitonic, descending keys): the k-th key is the top-k threshold; top-p scans the kept
+//   4. sorts the list (descending keys; by rank up to 512 keys, else bitonic): the k-th key is the top-k
+//      threshold; top-p scans the kept
 //      keys' fixed-point masses from the top (the same masses and the same rule as threshold_kernel, so the
 //      same threshold);
 //   5. writes the threshold and the kept logits' (max, sum).
@@ -635,23 +636,30 @@ __global__ void __launch_bounds__(FB_NT, 4) bound_kernel(const __grid_constant__
                 ok[u] = wi < n4;
                 w[u] = ok[u] ? ld_word(w4 + wi, pol) : make_uint4(0u, 0u, 0u, 0u);
             }
+            const float bv = bound == 0u ? __uint_as_float(0xFF800000u) : FKey<E>::value_of(bound);   // 0: all
 #pragma unroll
             for (int u = 0; u < UG; ++u) {
                 const uint32_t uu[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+                // a word whose values all lie below the bound's (as floats: key order refines float order)
+                // holds no key at or above it
+                bool any = false;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    if constexpr (E::BYTES == 2)
+                        any |= (__uint_as_float(uu[j] << 16) >= bv) | (__uint_as_float(uu[j] & 0xFFFF0000u) >= bv);
+                    else
+                        any |= __uint_as_float(uu[j]) >= bv;
+                }
+                if (!(ok[u] && any)) continue;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
 #pragma unroll
                     for (int h = 0; h < (E::BYTES == 2 ? 2 : 1); ++h) {
                         const KT key = E::BYTES == 2 ? FKey<E>::of_bits(h ? (uu[j] >> 16) : (uu[j] & 0xFFFFu))
                                                      : FKey<E>::of_bits(uu[j]);
-                        const bool in = ok[u] && key >= bound;
-                        const unsigned bal = __ballot_sync(0xffffffffu, in);
-                        if (bal) {
-                            unsigned b0 = 0u;
-                            if (lane == 0) b0 = atomicAdd(&s_n, static_cast<unsigned>(__popc(bal)));
-                            b0 = __shfl_sync(0xffffffffu, b0, 0);
-                            const unsigned at = b0 + static_cast<unsigned>(__popc(bal & ((1u << lane) - 1u)));
-                            if (in && at < static_cast<unsigned>(F_CAP)) cand[at] = key;
+                        if (key >= bound) {
+                            const unsigned at = atomicAdd(&s_n, 1u);
+                            if (at < static_cast<unsigned>(F_CAP)) cand[at] = key;
                         }
                     }
                 }
@@ -665,22 +673,45 @@ __global__ void __launch_bounds__(FB_NT, 4) bound_kernel(const __grid_constant__
         return;
     }
 
-    // ---- 4. sort the list, descending keys (bitonic over the next power of two, padded with key 0) ----
-    int P = 1;
-    while (P < static_cast<int>(n)) P <<= 1;
-    for (int i = static_cast<int>(n) + tid; i < P; i += FB_NT) cand[i] = 0u;
-    __syncthreads();
-    for (int size = 2; size <= P; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int q = tid; q < P / 2; q += FB_NT) {
-                const int i = 2 * q - (q & (stride - 1));
-                const KT a = cand[i], b = cand[i + stride];
-                if ((i & size) == 0 ? a < b : a > b) {
-                    cand[i] = b;
-                    cand[i + stride] = a;
+    // ---- 4. sort the list, descending keys ----
+    if (n <= static_cast<unsigned>(2 * FB_NT)) {
+        // by rank (the larger keys, and the equal keys listed before): two keys a thread
+        KT mine[2];
+        int rank[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int i = tid + q * FB_NT;
+            mine[q] = i < static_cast<int>(n) ? cand[i] : KT(0);
+            rank[q] = 0;
+        }
+        for (int jj = 0; jj < static_cast<int>(n); ++jj) {
+            const KT o = cand[jj];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) rank[q] += (o > mine[q] || (o == mine[q] && jj < tid + q * FB_NT)) ? 1 : 0;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+            if (tid + q * FB_NT < static_cast<int>(n)) cand[rank[q]] = mine[q];
+        __syncthreads();
+    } else {
+        // bitonic over the next power of two, padded with key 0
+        int P = 1;
+        while (P < static_cast<int>(n)) P <<= 1;
+        for (int i = static_cast<int>(n) + tid; i < P; i += FB_NT) cand[i] = 0u;
+        __syncthreads();
+        for (int size = 2; size <= P; size <<= 1) {
+            for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                for (int q = tid; q < P / 2; q += FB_NT) {
+                    const int i = 2 * q - (q & (stride - 1));
+                    const KT a = cand[i], b = cand[i + stride];
+                    if ((i & size) == 0 ? a < b : a > b) {
+                        cand[i] = b;
+                        cand[i + stride] = a;
+                    }
                 }
+                __syncthreads();
             }
-            __syncthreads();
         }
     }
     // keys at or above cand[t - 1] (ties with it included): nk of them
