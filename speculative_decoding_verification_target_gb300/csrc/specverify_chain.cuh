@@ -672,8 +672,15 @@ __device__ __forceinline__ void draw_body(const DParams& p, DrawShared<E>& S, un
             for (int q = 0; q < PCH; ++q) {
                 const int e0 = pc * PE + (lane + 32 * q) * CHUNK;
                 const int et = (tok >= e0 && tok < e0 + CHUNK) ? tok - e0 : -1;
-                float ovl;
-                const float cm = fast_chunk<E>(mode, rt[q], ro[q], c, po, et, hpatch, ovl);
+                float ovl, cm;
+                // filtered rows: where every target logit is -inf, h and so the residual and the overlap are 0
+                // (most chunks of a top-k row): the warp skips the arithmetic when all its chunks are such
+                if (!FILT || __any_sync(0xffffffffu, E::any_kept(rt[q]) || et >= 0)) {
+                    cm = fast_chunk<E>(mode, rt[q], ro[q], c, po, et, hpatch, ovl);
+                } else {
+                    cm = 0.f;
+                    ovl = 0.f;
+                }
                 loc = ff_addf(loc, cm);
                 // a large chunk (or the Cactus token's) joins the queue: its float-float mass will replace cm
                 const bool big = cm + ovl > p.k.tau || et >= 0;
@@ -789,6 +796,10 @@ __device__ __forceinline__ void draw_body(const DParams& p, DrawShared<E>& S, un
                 const int e0 = ft * PE + ch * CHUNK;
                 const int et = (tok >= e0 && tok < e0 + CHUNK) ? tok - e0 : -1;
                 float v[8];   // the chunk's fast residual per element
+                if constexpr (FILT) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) v[q] = 0.f;
+                }
                 FF m = {0.f, 0.f};
                 bool big = false;
                 Raw rt = E::ninf(), ro = E::ninf();
@@ -797,12 +808,14 @@ __device__ __forceinline__ void draw_body(const DParams& p, DrawShared<E>& S, un
                 if (ch < nch) {
                     rt = filt<E, FILT>(E::template gload<AL>(trow, e0, V), tt);
                     ro = mode == 1 ? filt<E, FILT>(E::template gload<AL>(orow, e0, V), to) : rt;
-                    float ovl, unused = 0.f;
-                    const float cm = fast_chunk<E>(mode, rt, ro, c, po, et, hpatch, ovl);
-                    chunk_values<E>(mode, rt, ro, c, po, et, hpatch, v, unused);
-                    m = FF{cm, 0.f};
-                    big = cm + ovl > p.k.tau || et >= 0;
-                    if (big) s_pl[atomicAdd(&s_pn, 1)] = ch;
+                    if (!FILT || E::any_kept(rt) || et >= 0) {   // (else the chunk's residual is 0: v stays 0)
+                        float ovl, unused = 0.f;
+                        const float cm = fast_chunk<E>(mode, rt, ro, c, po, et, hpatch, ovl);
+                        chunk_values<E>(mode, rt, ro, c, po, et, hpatch, v, unused);
+                        m = FF{cm, 0.f};
+                        big = cm + ovl > p.k.tau || et >= 0;
+                        if (big) s_pl[atomicAdd(&s_pn, 1)] = ch;
+                    }
                 }
                 __syncthreads();
                 // the piece's large chunks at float-float precision, eight threads to a chunk

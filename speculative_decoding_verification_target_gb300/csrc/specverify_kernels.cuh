@@ -61,6 +61,11 @@ struct Bf16 {
     __device__ static float at(const unsigned char* slot, int e) {
         return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(slot)[e]) << 16);
     }
+    // whether a chunk holds a logit other than -inf
+    __device__ static bool any_kept(const Raw& r) {
+        const uint32_t ni = 0xFF80FF80u;
+        return (r.x != ni) | (r.y != ni) | (r.z != ni) | (r.w != ni);
+    }
     // a chunk with every logit below t replaced by -inf (standardised sampling's filter)
     __device__ static Raw mask(const Raw& r, float t) {
         auto m = [t](uint32_t w) -> uint32_t {
@@ -138,6 +143,11 @@ struct F32 {
     }
     __device__ static float max_fin(Max m) { return m; }
     __device__ static float at(const unsigned char* slot, int e) { return reinterpret_cast<const float*>(slot)[e]; }
+    __device__ static bool any_kept(const Raw& r) {
+        const float ni = __uint_as_float(0xFF800000u);
+        return (r.a.x != ni) | (r.a.y != ni) | (r.a.z != ni) | (r.a.w != ni) | (r.b.x != ni) | (r.b.y != ni) |
+               (r.b.z != ni) | (r.b.w != ni);
+    }
     // a chunk with every logit below t replaced by -inf (standardised sampling's filter)
     __device__ static Raw mask(const Raw& r, float t) {
         auto m = [t](float x) { return x >= t ? x : __uint_as_float(0xFF800000u); };
