@@ -147,11 +147,12 @@ def max_over_ranks(pg, torch, v, device):
 # of this benchmark's own command (profiles/), keyed by a hash of the kernel sources it was taken with: when
 # the sources change the recorded number no longer applies and the JSON line reports null.
 RECORDED_TRAFFIC = {
-    "686eac9ab016b803": {
-        "sps_llama3_b64_k5": 214698752,
-        "hedgespec_n7_b32_k5": 392502784,
-        "cactus_qwen_b128_m20": 1668214784,
-        "hedgespec_n21_b256_k8": 18995759104,   # captured at B = 32, scaled by 256 / 32 (grows with the sequences)
+    "c305865b3d847593": {
+        "sps_llama3_b64_k5": 214816384,
+        "hedgespec_n7_b32_k5": 392684288,
+        "cactus_qwen_b128_m20": 1668357120,
+        "hedgespec_n21_b256_k8": 19008962560,   # captured at B = 32, scaled by 256 / 32 (grows with the sequences)
+        "sps_llama3_b64_k5+top_k64_top_p0.95": 220032512,   # bound, threshold and draw kernels of a filtered call
     },
 }
 
@@ -387,14 +388,14 @@ def record_for(args, torch, sv, w, dev, rank, stream, pg, local, filtered=False,
            "value": w.positions / call_s, "unit": UNIT, "steps": steps, "avg_call_us": call_s * 1e6,
            "bytes_per_call": r.batch_bytes, "achieved_gbs": achieved, "peak_gbs": peak, "peak_kind": peak_kind,
            "frac": achieved / peak,
-           "traffic": None if (filtered or one_launch) else RECORDED_TRAFFIC.get(kernel_source_hash(), {}).get(w.name),
+           "traffic": None if one_launch else RECORDED_TRAFFIC.get(kernel_source_hash(), {}).get(name),
            "sustained_call_us": sus["ms_per_step"] * 1e3, "sustained_calls": sus["steps"],
            "clocks": merge_clocks(c1, c2),
            "l2": "ring of %d distinct batches (%.0f MB) > 129 MB L2" % (r.ring, r.ring * r.batch_bytes / 1e6),
            "device_status": sv.read_status(r.ws) if not filtered else None}
     if filtered:
-        rec["note"] = ("bytes_per_call counts one read of every logit; the path reads the logits twice (the "
-                       "threshold pass, then the statistics pass that masks them as it reads)")
+        rec["note"] = ("bytes_per_call counts one read of every logit; the bound kernel reads every logit once "
+                       "and re-reads the lines that reach its bound, and the draw re-reads one row pair per sequence")
     if not args.no_cpu_baseline and rank == 0 and not filtered and not one_launch:
         host = {k: r.batches[0][k].to("cpu") for k in ("target", "drafters" if r.kind == "counterfactual"
                                                           else "draft", "tokens", "seeds")}
@@ -545,9 +546,10 @@ def run_ours(args, w):
                        r.ring, r.ring * batch_bytes / 1e6),
                    "parallelism": "replicas over sequences" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None if args.filtered else RECORDED_TRAFFIC.get(kernel_source_hash(), {}).get(w.name),
+                     "traffic": RECORDED_TRAFFIC.get(kernel_source_hash(), {}).get(
+                         w.name + ("+top_k%d_top_p%g" % (FILTER_TOP_K, FILTER_TOP_P) if args.filtered else "")),
                      "peak_kind": peak_kind,
-                     "kernel": ("threshold_kernel + stats_kernel + draw_kernel (masking forms): one whole filtered call"
+                     "kernel": ("bound_kernel + threshold_kernel + draw_kernel (masking form): one whole filtered call"
                                 if args.filtered else
                                 "%s + draw_kernel: one whole %s call (both kernels)" % (
                                     "gamma_kernel" if kind == "counterfactual" else "stats_kernel", kind)) +
