@@ -204,8 +204,9 @@ size_t spec_filter_workspace_size(int B, int K, int V, spec_dtype dtype);
  * neither rule): ties at a threshold are all kept, top-k comes before top-p. Same arguments, outputs and
  * errors as spec_verify, plus top_k >= 0 and top_p in (0, 1]; the workspace must hold
  * spec_filter_workspace_size(B, K, V, dtype) bytes (its first 16 bytes zeroed once, as for spec_verify). The
- * thresholds come from radix selection on fp32 masses (summed in 2^-44 fixed point): a top-p decision within
- * about 1e-6 of the mass boundary may differ from an exact-arithmetic one. */
+ * thresholds come from an exact selection on order-preserving integer keys of the logits; top-p sums fp32
+ * masses in 2^-44 fixed point, so a top-p decision within about 1e-6 of the mass boundary may differ from
+ * an exact-arithmetic one. */
 spec_status spec_verify_filtered(const void* target_logits, const void* draft_logits, spec_dtype dtype,
                                  const int32_t* draft_tokens, const uint64_t* seeds, int B, int K, int V,
                                  float temperature, int top_k, float top_p, int32_t* accept_len, int32_t* out_tokens,

@@ -161,3 +161,33 @@ def test_no_cpu_fallback(lib, tmp_path):
             sv.load()
     finally:
         sv._build.LIB, sv._lib = saved_path, saved_lib
+
+
+def test_filter_workspace_size(lib):
+    """spec_verify_filtered's workspace: spec_verify's, then one float threshold and one float pair (the kept
+    logits' max and sum) per target and draft row, each region on 256 bytes. No copy of the logits."""
+    import speculative_decoding_verification_target_gb300 as sv
+    up = lambda x: (x + 255) // 256 * 256
+    for B, K, V in ((64, 5, 128256), (4, 3, 1000), (1, 64, 262144), (3, 1, 7)):
+        rows = B * (2 * K + 1)
+        thr = up(sv.workspace_size(B, K, V, 1))
+        ms = up(thr + 4 * rows)
+        for dt in (0, 1):
+            assert lib.spec_filter_workspace_size(B, K, V, dt) == up(ms + 8 * rows)
+        if V >= 100000:   # well under 1% of the bf16 logits it filters
+            assert lib.spec_filter_workspace_size(B, K, V, 0) < 2 * V * rows // 100
+    assert lib.spec_filter_workspace_size(4, 3, 0, 0) == 0
+    assert lib.spec_filter_workspace_size(4, 3, 1000, 7) == 0
+    assert lib.spec_filter_workspace_size(-1, 3, 1000, 0) == 0
+
+
+@pytest.mark.parametrize("top_k,top_p,wsb,code", [
+    (-1, 1.0, 1 << 20, 1), (5, 0.0, 1 << 20, 1), (5, 1.5, 1 << 20, 1), (5, float("nan"), 1 << 20, 1),
+    (5, 0.9, 64, 1),
+])
+def test_filtered_host_validation(lib, top_k, top_p, wsb, code):
+    P = ctypes.c_void_p
+    r = lib.spec_verify_filtered(P(1 << 20), P(1 << 21), 0, P(1 << 22), P(1 << 23), 2, 3, 1000, ctypes.c_float(1.0),
+                                 top_k, ctypes.c_float(top_p), P(1 << 24), P(1 << 25), None, P(1 << 26), wsb, None)
+    assert r == code
+    assert lib.spec_last_error()
