@@ -147,7 +147,7 @@ def max_over_ranks(pg, torch, v, device):
 # of this benchmark's own command (profiles/), keyed by a hash of the kernel sources it was taken with: when
 # the sources change the recorded number no longer applies and the JSON line reports null.
 RECORDED_TRAFFIC = {
-    "c305865b3d847593": {
+    "66d5e36fcf3ae607": {
         "sps_llama3_b64_k5": 214816384,
         "hedgespec_n7_b32_k5": 392684288,
         "cactus_qwen_b128_m20": 1668357120,
@@ -158,13 +158,19 @@ RECORDED_TRAFFIC = {
 
 
 def kernel_source_hash():
+    """Hash of the kernel sources' code: comments and blank lines are stripped first, so a comment edit keeps
+    the traffic records taken on the same code, and any change to the code drops them."""
     import glob
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in sorted(glob.glob(os.path.join(ROOT, "speculative_decoding_verification_target_gb300", "csrc", "*.cu*"))):
         h.update(os.path.basename(f).encode())
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        with open(f, encoding="utf-8") as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update("\n".join(line.rstrip() for line in text.splitlines() if line.strip()).encode())
     return h.hexdigest()[:16]
 
 

@@ -1,19 +1,23 @@
 // Standardised sampling ("Speculative Decoding 为什么是 Lossless 的 — 详细证明教程", §8 Q4: temperature,
 // top-k and top-p are folded into p and q, the same transforms for the target and the draft row, before the
 // ratio is taken). Every such filter keeps the logits at or above a per-row threshold, so the filtered
-// verification is the ordinary one on rows whose other logits are -inf:
-//   - threshold_kernel: one CTA per row finds the threshold by radix selection on order-preserving integer
-//     keys of the logits, 4 bits a pass from the top (4 passes for bf16, 8 for fp32). Top-k (0 < k < V)
-//     descends by counts to the k-th largest value; top-p (0 < top_p < 1), on what top-k kept, descends by
-//     the mass sum_x 2^((x - M) c) to the value at which the mass from the largest logit down first reaches
-//     top_p of the kept total. Ties at a threshold are all kept (the kept set depends on values only). Once
-//     the elements still in play fit in shared memory (at most F_CAP keys), one more pass over the row copies
-//     them there and the remaining passes read only them;
-//   - the statistics and draw kernels then read the caller's rows as they are and replace every logit below
-//     its row's threshold by -inf as it arrives in registers (their FILT form), so no filtered copy is made.
-// The histograms of a pass are integer sums, so they do not depend on the order of the additions: counts, and
-// masses in 64-bit fixed point (2^-44 units; a mass 2^((x - M) c) is at most 1 and a row holds at most 2^18
-// logits, so a bin cannot overflow). Each thread adds into its own column of the shared-memory histograms (no
+// verification is the ordinary one on rows whose other logits are -inf. Two kernels write each row's
+// threshold and the kept logits' (max, sum of 2^((x - max) c)), which the draw takes as its row normalisers:
+//   - bound_kernel (top-k up to FB_MAX_K on rows of whole 16-byte words): a bound from the row's line maxima,
+//     the candidates at or above it, sorted (its own comment below);
+//   - threshold_kernel (every other filter, and the rows bound_kernel leaves): radix selection on
+//     order-preserving integer keys of the logits, 4 bits a pass from the top (4 passes for bf16, 8 for
+//     fp32). Top-k (0 < k < V) descends by counts to the k-th largest value; top-p (0 < top_p < 1), on what
+//     top-k kept, descends by the mass sum_x 2^((x - M) c) to the value at which the mass from the largest
+//     logit down first reaches top_p of the kept total. Once the elements still in play fit in shared memory
+//     (at most F_CAP keys), one more pass over the row copies them there and the remaining passes read only
+//     them.
+// Ties at a threshold are all kept (the kept set depends on values only). The draw kernel then reads the
+// caller's rows as they are and replaces every logit below its row's threshold by -inf as it arrives in
+// registers (its FILT form): no filtered copy is made and no statistics pass runs.
+// The masses are integer sums, so they do not depend on the order of the additions: masses in 64-bit fixed
+// point (2^-44 units; a mass 2^((x - M) c) is at most 1 and a row holds at most 2^18 logits, so a sum cannot
+// overflow). In threshold_kernel each thread adds into its own column of the shared-memory histograms (no
 // atomics, no contention however the keys cluster) and the columns are summed after the pass.
 #pragma once
 #include "specverify_kernels.cuh"
