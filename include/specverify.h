@@ -190,9 +190,10 @@ spec_status spec_hedge_feedback_init(void* state, int N, int B, int K, int objec
 spec_status spec_hedge_feedback_push(void* state, const float* gamma, const int32_t* accept_len, int N, int B, int K,
                                      float* weights, int32_t* applied, void* stream);
 
-/* Bytes of workspace spec_verify_filtered needs: the spec_verify workspace and one float (the row's threshold)
- * per target and draft row. No filtered copy of the logits is made: the kernels mask each logit as they read
- * it. 0 for invalid sizes or dtype. */
+/* Bytes of workspace spec_verify_filtered needs: the spec_verify workspace; per target and draft row its
+ * threshold and the kept logits' (max, sum); per target row a list of up to 1024 kept logits (index and
+ * value) for the draw. No filtered copy of the logits is made: the kernels mask each logit as they read it.
+ * 0 for invalid sizes or dtype. */
 size_t spec_filter_workspace_size(int B, int K, int V, spec_dtype dtype);
 
 /* spec_verify with standardised sampling ("Speculative Decoding 为什么是 Lossless 的", §8 Q4: temperature,

@@ -58,16 +58,21 @@ WsLayout ws_layout(int B, int K, int V, int N) {
 
 // Workspace of spec_verify_filtered: [the verify workspace][row thresholds][filtered target rows][filtered
 // draft rows], each region 256-byte aligned.
+// spec_verify's workspace, then per row a threshold and the kept logits' (max, sum), then per target row the
+// count, element indices and values of its kept logits when they are few (D_LIST_CAP at most).
 struct FilterLayout {
-    size_t thr_off, ms_off, total;
+    size_t thr_off, ms_off, ln_off, li_off, lx_off, total;
 };
 FilterLayout filter_layout(int B, int K, int V) {
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
     FilterLayout f;
-    const size_t rows = static_cast<size_t>(B) * (2 * K + 1);
+    const size_t rows = static_cast<size_t>(B) * (2 * K + 1), rows_a = static_cast<size_t>(B) * (K + 1);
     f.thr_off = up(ws_layout(B, K, V, 1).total);
     f.ms_off = up(f.thr_off + rows * sizeof(float));
-    f.total = up(f.ms_off + rows * sizeof(float2));
+    f.ln_off = up(f.ms_off + rows * sizeof(float2));
+    f.li_off = up(f.ln_off + rows_a * sizeof(int));
+    f.lx_off = up(f.li_off + rows_a * D_LIST_CAP * sizeof(int));
+    f.total = up(f.lx_off + rows_a * D_LIST_CAP * sizeof(float));
     return f;
 }
 
@@ -87,6 +92,9 @@ struct Call {
     float* diag;
     float* gamma_star;
     const float* thr;   // standardised sampling: per statistics row, the logits below it count as -inf (or null)
+    const int* list_n;  // standardised sampling: the target rows' kept logits listed for the draw
+    const int* list_idx;
+    const float* list_x;
     void* workspace;
     size_t workspace_bytes;
     cudaStream_t stream;
@@ -213,6 +221,10 @@ DParams draw_params(const Call& a, const unsigned char* draft, const float2* par
     d.diag = a.diag;
     d.gamma_star = a.gamma_star;
     d.thr = a.thr;
+    d.list_n = a.list_n;
+    d.list_idx = a.list_idx;
+    d.list_x = a.list_x;
+    d.list_cap = D_LIST_CAP;
     d.status = status;
     return d;
 }
@@ -504,6 +516,10 @@ spec_status run_filtered(const Call& a, int top_k, float top_p) {
     f.top_p = top_p;
     f.thr = reinterpret_cast<float*>(ws + fl.thr_off);
     f.row_ms = reinterpret_cast<float2*>(ws + fl.ms_off);
+    f.list_n = reinterpret_cast<int*>(ws + fl.ln_off);
+    f.list_idx = reinterpret_cast<int*>(ws + fl.li_off);
+    f.list_x = reinterpret_cast<float*>(ws + fl.lx_off);
+    f.list_cap = D_LIST_CAP;
     f.vec = rows16 ? 1 : 0;
     using ThrFn = void (*)(const FParams);
     ThrFn tfn = a.dtype == SPEC_BF16 ? threshold_kernel<Bf16> : threshold_kernel<F32>;
@@ -534,6 +550,9 @@ spec_status run_filtered(const Call& a, int top_k, float top_p) {
     g_last_plan[4] = (a.V + PE - 1) / PE;
     Call c = a;
     c.thr = f.thr;
+    c.list_n = f.list_n;
+    c.list_idx = f.list_idx;
+    c.list_x = f.list_x;
     return launch_draw(c, aligned, static_cast<const unsigned char*>(a.others), nullptr, f.row_ms, 0, 0,
                        reinterpret_cast<unsigned*>(ws));
 }

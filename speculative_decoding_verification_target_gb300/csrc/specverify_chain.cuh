@@ -38,6 +38,7 @@ constexpr int S_MAX_CTAS = 1024;        // grid cap (partials are sized for S_MA
 constexpr int DW = 16;                  // warps per CTA of the draw kernel
 constexpr int DNT = DW * 32;
 constexpr int D_MAX_K = 64;             // positions per sequence
+constexpr int D_LIST_CAP = 2 * DNT;     // kept logits of a listed row (standardised sampling): two a thread
 constexpr int D_MAX_PIECES = 128;       // pieces per row (V <= 262144)
 
 // The equal split of P pieces over G warps: warp g takes base + (g < rem) pieces from g * base + min(g, rem).
@@ -278,6 +279,10 @@ struct DParams {
     float* diag;                   // [B, K, 4] or null
     float* gamma_star;             // [B, K] or null (Cactus)
     const float* thr;              // FILT: per statistics row, the logits below it count as -inf
+    const int* list_n;             // FILT: per target row, its kept logits listed (-1: none, read the row)
+    const int* list_idx;           // FILT: [B (K+1), list_cap] their element indices, ascending
+    const float* list_x;           // FILT: [B (K+1), list_cap] their values
+    int list_cap;
     unsigned* status;
 };
 
@@ -423,6 +428,88 @@ struct DrawShared {
     PickPlan s_plan;
     int s_L, s_emit;
 };
+
+// One position's pass from its target row's kept logits alone (standardised sampling, when the threshold
+// kernel listed them): h is 0 off that list, and so is the residual. The masses of the ln entries in
+// vocabulary order at float-float precision (the draft logit at each entry's index read and masked), Z, and
+// at the drawn position the pick by the full-row pass's rule: the first element of positive mass whose
+// running mass exceeds u Z, else the last element of positive mass. All DNT threads of the cluster's CTA 0;
+// thread t takes entries 2t and 2t + 1. Returns the drawn token (-1 off the drawn position).
+template <class E>
+__device__ __noinline__ int list_pass(const DParams& p, DrawShared<E>& S, int mode, int j, int L, int b, int ln,
+                                      const unsigned char* orow, const PairOffX px, float to, uint64_t seed) {
+    static_assert(2 * DNT >= D_LIST_CAP, "two entries a thread");
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const size_t base = (static_cast<size_t>(b) * (p.K + 1) + j) * static_cast<size_t>(p.list_cap);
+    const int* const idx = p.list_idx + base;
+    const float* const xs = p.list_x + base;
+    const FF zero = {0.f, 0.f};
+    // entry e's residual (m = 1) or target probability (m = 2)
+    auto value = [&](int e, int m) -> FF {
+        if (e >= ln) return zero;
+        const float xt = xs[e];
+        const float xd = m == 1 ? mask1(E::at(orow, idx[e]), to) : xt;
+        return elem_exact(m, xt, xd, px, p.k, S.s_tab, false, zero);
+    };
+    // the mass before this thread's entries and the total, in entry order (fixed association)
+    auto scan = [&](FF r0, FF r1, FF& before, FF& total) {
+        const FF incl = warp_incl_scan_ff(ff_add(r0, r1), lane);
+        if (lane == 31) S.s_wscan[warp] = make_float2(incl.hi, incl.lo);
+        __syncthreads();
+        FF start = zero;
+        total = zero;
+        for (int w = 0; w < DW; ++w) {
+            const FF t = FF{S.s_wscan[w].x, S.s_wscan[w].y};
+            if (w < warp) start = ff_add(start, t);
+            total = ff_add(total, t);
+        }
+        FF excl = ff_shfl_up(incl, 1);
+        if (lane == 0) excl = zero;
+        before = ff_add(start, excl);
+        __syncthreads();   // s_wscan may be written again
+    };
+    FF r0 = value(2 * tid, mode), r1 = value(2 * tid + 1, mode);
+    FF before, Z;
+    scan(r0, r1, before, Z);
+    if (p.diag && j < p.K && tid == 0) p.diag[(static_cast<size_t>(b) * p.K + j) * 4 + 2] = Z.hi + Z.lo;
+    if (j != L) return -1;
+    const float u = philox_uniform(seed, static_cast<uint32_t>(b), static_cast<uint32_t>(L), 1u);
+    if (mode == 1 && !(Z.hi > 0.f)) {   // the residual rounded to zero mass: draw from h over the row instead
+        r0 = value(2 * tid, 2);
+        r1 = value(2 * tid + 1, 2);
+        scan(r0, r1, before, Z);
+    }
+    const FF tp = ff_mulf(Z, u);
+    int first = 0x7fffffff, last = -1;
+    FF a = ff_add(before, r0);
+    if (r0.hi > 0.f) {
+        last = 2 * tid;
+        if (ff_gt(a, tp)) first = 2 * tid;
+    }
+    a = ff_add(a, r1);
+    if (r1.hi > 0.f) {
+        last = 2 * tid + 1;
+        if (first == 0x7fffffff && ff_gt(a, tp)) first = 2 * tid + 1;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        first = min(first, __shfl_xor_sync(0xffffffffu, first, o));
+        last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+    }
+    if (lane == 0) {
+        S.s_wfirst[warp] = first;
+        S.s_wlast[warp] = last;
+    }
+    __syncthreads();
+    int f = 0x7fffffff, l = -1;
+    for (int w = 0; w < DW; ++w) {
+        f = min(f, S.s_wfirst[w]);
+        l = max(l, S.s_wlast[w]);
+    }
+    __syncthreads();
+    const int chosen = f != 0x7fffffff ? f : l;
+    return chosen >= 0 ? idx[chosen] : -1;
+}
 
 // One cluster of cps CTAs per sequence. Every CTA derives the row scalars
 // and the chain itself (the same arithmetic on the same data, so the same L); the pieces of the drawn row
@@ -617,6 +704,18 @@ __device__ __forceinline__ void draw_body(const DParams& p, DrawShared<E>& S, un
         if constexpr (FILT) {
             tt = p.thr[static_cast<size_t>(b) * (K + 1) + j];
             to = mode == 1 ? p.thr[p.rows_a_n + static_cast<long long>(b) * K + j] : tt;
+        }
+        if constexpr (FILT) {
+            // a listed target row: CTA 0 works from the list, and no CTA reads the rows
+            const int ln = p.list_n[static_cast<size_t>(b) * (K + 1) + j];
+            if (ln >= 0) {
+                if (rank == 0 && !idle) {
+                    const int e = list_pass<E>(p, S, mode, j, L, b, ln, orow, px, to, seed);
+                    if (j == L) emitted = e;
+                }
+                if (it + 1 < n_pass) cluster_sync_all();
+                continue;
+            }
         }
         // bulk copy of piece pc of both rows (the target alone for a bonus row) into this warp's slot
         auto issue = [&](int pc) {

@@ -73,6 +73,10 @@ struct FParams {
     float* thr;                    // [rows_n] threshold value (-inf: nothing filtered; NaN: left to threshold_kernel)
     float2* row_ms;                // [rows_n] (max, sum of 2^((x - max) c)) over the logits the filter keeps
     int flagged_only;              // threshold_kernel: only the rows whose threshold is NaN (else every row)
+    int* list_n;                   // [rows_a_n] kept logits of a target row listed for the draw (-1: none)
+    int* list_idx;                 // [rows_a_n, list_cap] their element indices, ascending
+    float* list_x;                 // [rows_a_n, list_cap] their values
+    int list_cap;
     int vec;                       // every row starts on 16 bytes and holds whole 16-byte words
 };
 
@@ -456,6 +460,7 @@ __device__ __forceinline__ void threshold_row(const FParams& p, const long long 
     if (tid == 0) {
         p.thr[r] = th;
         p.row_ms[r] = make_float2(M, ssum);
+        if (r < p.rows_a_n) p.list_n[r] = -1;   // the draw reads this row whole
     }
 }
 
@@ -517,11 +522,12 @@ __device__ __forceinline__ uint32_t line_key16(float v) {
 }
 
 template <class E>
-__global__ void __launch_bounds__(FB_NT, 4) bound_kernel(const __grid_constant__ FParams p) {
+__global__ void __launch_bounds__(FB_NT, 5) bound_kernel(const __grid_constant__ FParams p) {
     using KT = typename FKey<E>::K;
-    static_assert(FB_MAX_V * E::BYTES / (16 * FB_LINE_WORDS) * 2 <= F_CAP * 4, "line keys fit the list's space");
+    static_assert(FB_MAX_V * E::BYTES / (16 * FB_LINE_WORDS) * 2 <= F_CAP * 8, "line keys fit the list's space");
     static_assert(F_CAP * 2 <= FB_W * 256 * 4, "line list fits the histograms' space");
-    __shared__ __align__(16) uint32_t s_a[F_CAP];         // line keys (uint16), then the candidate keys
+    __shared__ __align__(16) unsigned long long s_a[F_CAP];   // line keys (uint16), then the candidates:
+                                                              // key << 32 | element index
     __shared__ __align__(16) uint32_t s_b[FB_W * 256];    // per-warp 8-bit histograms, then the line list (uint16)
     __shared__ unsigned s_wt[FB_W];
     __shared__ unsigned long long s_wm[FB_W];
@@ -529,7 +535,8 @@ __global__ void __launch_bounds__(FB_NT, 4) bound_kernel(const __grid_constant__
     __shared__ unsigned s_n, s_sel, s_above, s_nk, s_first;
     uint16_t* const lkey = reinterpret_cast<uint16_t*>(s_a);
     uint16_t* const lines = reinterpret_cast<uint16_t*>(s_b);
-    KT* const cand = s_a;
+    unsigned long long* const cand = s_a;
+    auto key_of = [&](int i) -> KT { return static_cast<KT>(cand[i] >> 32); };
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const long long r = blockIdx.x;
     const int V = p.V, k = p.top_k;
@@ -663,7 +670,10 @@ __global__ void __launch_bounds__(FB_NT, 4) bound_kernel(const __grid_constant__
                                                      : FKey<E>::of_bits(uu[j]);
                         if (key >= bound) {
                             const unsigned at = atomicAdd(&s_n, 1u);
-                            if (at < static_cast<unsigned>(F_CAP)) cand[at] = key;
+                            const int wi = static_cast<int>(lines[base + u * GPB + g]) * FB_LINE_WORDS + sub;
+                            const unsigned e = static_cast<unsigned>(wi * (16 / E::BYTES) + j * (E::BYTES == 2 ? 2 : 1) + h);
+                            if (at < static_cast<unsigned>(F_CAP))
+                                cand[at] = (static_cast<unsigned long long>(key) << 32) | e;
                         }
                     }
                 }
@@ -673,25 +683,28 @@ __global__ void __launch_bounds__(FB_NT, 4) bound_kernel(const __grid_constant__
     }
     const unsigned n = nl <= static_cast<unsigned>(F_CAP) ? s_n : 0xFFFFFFFFu;
     if (n > static_cast<unsigned>(F_CAP) || n < static_cast<unsigned>(k)) {   // too many: threshold_kernel takes the row
-        if (tid == 0) p.thr[r] = __uint_as_float(0x7FC00000u);
+        if (tid == 0) {
+            p.thr[r] = __uint_as_float(0x7FC00000u);
+            if (r < p.rows_a_n) p.list_n[r] = -1;
+        }
         return;
     }
 
-    // ---- 4. sort the list, descending keys ----
+    // ---- 4. sort the list, descending keys (then descending element index: the entries are distinct) ----
     if (n <= static_cast<unsigned>(2 * FB_NT)) {
-        // by rank (the larger keys, and the equal keys listed before): two keys a thread
-        KT mine[2];
+        // by rank (the larger entries): two entries a thread
+        unsigned long long mine[2];
         int rank[2];
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
             const int i = tid + q * FB_NT;
-            mine[q] = i < static_cast<int>(n) ? cand[i] : KT(0);
+            mine[q] = i < static_cast<int>(n) ? cand[i] : 0ull;
             rank[q] = 0;
         }
         for (int jj = 0; jj < static_cast<int>(n); ++jj) {
-            const KT o = cand[jj];
+            const unsigned long long o = cand[jj];
 #pragma unroll
-            for (int q = 0; q < 2; ++q) rank[q] += (o > mine[q] || (o == mine[q] && jj < tid + q * FB_NT)) ? 1 : 0;
+            for (int q = 0; q < 2; ++q) rank[q] += o > mine[q] ? 1 : 0;
         }
         __syncthreads();
 #pragma unroll
@@ -702,13 +715,13 @@ __global__ void __launch_bounds__(FB_NT, 4) bound_kernel(const __grid_constant__
         // bitonic over the next power of two, padded with key 0
         int P = 1;
         while (P < static_cast<int>(n)) P <<= 1;
-        for (int i = static_cast<int>(n) + tid; i < P; i += FB_NT) cand[i] = 0u;
+        for (int i = static_cast<int>(n) + tid; i < P; i += FB_NT) cand[i] = 0ull;
         __syncthreads();
         for (int size = 2; size <= P; size <<= 1) {
             for (int stride = size >> 1; stride > 0; stride >>= 1) {
                 for (int q = tid; q < P / 2; q += FB_NT) {
                     const int i = 2 * q - (q & (stride - 1));
-                    const KT a = cand[i], b = cand[i + stride];
+                    const unsigned long long a = cand[i], b = cand[i + stride];
                     if ((i & size) == 0 ? a < b : a > b) {
                         cand[i] = b;
                         cand[i + stride] = a;
@@ -723,19 +736,19 @@ __global__ void __launch_bounds__(FB_NT, 4) bound_kernel(const __grid_constant__
         if (tid == 0) s_nk = 0u;
         __syncthreads();
         for (int i = tid; i < static_cast<int>(n); i += FB_NT)
-            if (cand[i] >= t && (i + 1 == static_cast<int>(n) || cand[i + 1] < t)) s_nk = static_cast<unsigned>(i + 1);
+            if (key_of(i) >= t && (i + 1 == static_cast<int>(n) || key_of(i + 1) < t)) s_nk = static_cast<unsigned>(i + 1);
         __syncthreads();
         return s_nk;
     };
-    KT lo = cand[k - 1];
-    const float M = FKey<E>::value_of(cand[0]);
+    KT lo = key_of(k - 1);
+    const float M = FKey<E>::value_of(key_of(0));
     if (p.top_p > 0.f && p.top_p < 1.f) {
         const unsigned nk = count_ge(lo);
         // each thread a run of the sorted keys: its fixed-point masses, then an exclusive scan across the CTA
         const int per = (static_cast<int>(nk) + FB_NT - 1) / FB_NT;
         const int i0 = min(static_cast<int>(nk), tid * per), i1 = min(static_cast<int>(nk), i0 + per);
         auto mass = [&](int i) -> unsigned long long {
-            return __float2ull_rz(ex2((FKey<E>::value_of(cand[i]) - M) * p.c) * F_FIX);
+            return __float2ull_rz(ex2((FKey<E>::value_of(key_of(i)) - M) * p.c) * F_FIX);
         };
         unsigned long long loc = 0ull;
         for (int i = i0; i < i1; ++i) loc += mass(i);
@@ -765,20 +778,42 @@ __global__ void __launch_bounds__(FB_NT, 4) bound_kernel(const __grid_constant__
             }
         }
         __syncthreads();
-        lo = cand[s_first];
+        lo = key_of(s_first);
     }
 
     // ---- 5. threshold, and the kept logits' (max, sum) by the draw's float comparison ----
     const float th = FKey<E>::value_of(lo);
     float sacc = 0.f;
+    if (tid == 0) s_nk = 0u;
+    __syncthreads();
     for (int i = tid; i < static_cast<int>(n); i += FB_NT) {
-        const float x = FKey<E>::value_of(cand[i]);
-        if (x >= th) sacc += ex2((x - M) * p.c);
+        const float x = FKey<E>::value_of(key_of(i));
+        if (x >= th) {
+            sacc += ex2((x - M) * p.c);
+            // the values fall along the list, so the kept logits are its first nkeep entries
+            if (i + 1 == static_cast<int>(n) || FKey<E>::value_of(key_of(i + 1)) < th) s_nk = static_cast<unsigned>(i + 1);
+        }
     }
-    const float ssum = cta_sum_fixed<FB_NT>(sacc, s_red);
+    const float ssum = cta_sum_fixed<FB_NT>(sacc, s_red);   // (its barriers also publish s_nk)
+    const int nkeep = static_cast<int>(s_nk);
     if (tid == 0) {
         p.thr[r] = th;
         p.row_ms[r] = make_float2(M, ssum);
+    }
+    // ---- 6. a target row's kept logits for the draw, in vocabulary order (each entry's rank among the kept
+    // element indices, which are distinct) ----
+    if (r < p.rows_a_n) {
+        if (nkeep <= p.list_cap) {
+            const size_t base = static_cast<size_t>(r) * p.list_cap;
+            for (int i = tid; i < nkeep; i += FB_NT) {
+                const unsigned e = static_cast<unsigned>(cand[i]);
+                int at = 0;
+                for (int jj = 0; jj < nkeep; ++jj) at += static_cast<unsigned>(cand[jj]) < e ? 1 : 0;
+                p.list_idx[base + at] = static_cast<int>(e);
+                p.list_x[base + at] = FKey<E>::value_of(key_of(i));
+            }
+        }
+        if (tid == 0) p.list_n[r] = nkeep <= p.list_cap ? nkeep : -1;
     }
 }
 

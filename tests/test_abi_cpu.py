@@ -165,17 +165,21 @@ def test_no_cpu_fallback(lib, tmp_path):
 
 def test_filter_workspace_size(lib):
     """spec_verify_filtered's workspace: spec_verify's, then one float threshold and one float pair (the kept
-    logits' max and sum) per target and draft row, each region on 256 bytes. No copy of the logits."""
+    logits' max and sum) per target and draft row, then per target row a count and up to 1024 kept logits
+    (index and value) for the draw, each region on 256 bytes. No copy of the logits."""
     import speculative_decoding_verification_target_gb300 as sv
     up = lambda x: (x + 255) // 256 * 256
     for B, K, V in ((64, 5, 128256), (4, 3, 1000), (1, 64, 262144), (3, 1, 7)):
-        rows = B * (2 * K + 1)
+        rows, rows_a = B * (2 * K + 1), B * (K + 1)
         thr = up(sv.workspace_size(B, K, V, 1))
         ms = up(thr + 4 * rows)
+        ln = up(ms + 8 * rows)
+        li = up(ln + 4 * rows_a)
+        lx = up(li + 4 * 1024 * rows_a)
         for dt in (0, 1):
-            assert lib.spec_filter_workspace_size(B, K, V, dt) == up(ms + 8 * rows)
-        if V >= 100000:   # well under 1% of the bf16 logits it filters
-            assert lib.spec_filter_workspace_size(B, K, V, 0) < 2 * V * rows // 100
+            assert lib.spec_filter_workspace_size(B, K, V, dt) == up(lx + 4 * 1024 * rows_a)
+        if V >= 100000:   # a few percent of the bf16 logits it filters
+            assert lib.spec_filter_workspace_size(B, K, V, 0) < 2 * V * rows // 20
     assert lib.spec_filter_workspace_size(4, 3, 0, 0) == 0
     assert lib.spec_filter_workspace_size(4, 3, 1000, 7) == 0
     assert lib.spec_filter_workspace_size(-1, 3, 1000, 0) == 0
