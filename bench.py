@@ -147,12 +147,12 @@ def max_over_ranks(pg, torch, v, device):
 # of this benchmark's own command (profiles/), keyed by a hash of the kernel sources it was taken with: when
 # the sources change the recorded number no longer applies and the JSON line reports null.
 RECORDED_TRAFFIC = {
-    "66d5e36fcf3ae607": {
-        "sps_llama3_b64_k5": 214816384,
-        "hedgespec_n7_b32_k5": 392684288,
-        "cactus_qwen_b128_m20": 1668357120,
-        "hedgespec_n21_b256_k8": 19008962560,   # captured at B = 32, scaled by 256 / 32 (grows with the sequences)
-        "sps_llama3_b64_k5+top_k64_top_p0.95": 220032512,   # bound, threshold and draw kernels of a filtered call
+    "4863ee80b57ac867": {
+        "sps_llama3_b64_k5": 214574208,
+        "hedgespec_n7_b32_k5": 392328960,
+        "cactus_qwen_b128_m20": 1668288512,
+        "hedgespec_n21_b256_k8": 19003412480,   # captured at B = 32, scaled by 256 / 32 (grows with the sequences)
+        "sps_llama3_b64_k5+top_k64_top_p0.95": 187456256,   # bound, threshold and draw kernels of a filtered call
     },
 }
 
@@ -401,7 +401,8 @@ def record_for(args, torch, sv, w, dev, rank, stream, pg, local, filtered=False,
            "device_status": sv.read_status(r.ws) if not filtered else None}
     if filtered:
         rec["note"] = ("bytes_per_call counts one read of every logit; the bound kernel reads every logit once "
-                       "and re-reads the lines that reach its bound, and the draw re-reads one row pair per sequence")
+                       "and re-reads the lines that reach its bound, and the draw reads the draft logits at the "
+                       "listed indices (a row pair per sequence only for rows with no list)")
     if not args.no_cpu_baseline and rank == 0 and not filtered and not one_launch:
         host = {k: r.batches[0][k].to("cpu") for k in ("target", "drafters" if r.kind == "counterfactual"
                                                           else "draft", "tokens", "seeds")}
