@@ -720,6 +720,25 @@ def test_verify_filtered_signed_zeros(dt):
         assert sv.read_status(out["workspace"]) == 0
 
 
+def test_verify_filtered_lean_launch():
+    """The launch the benchmark times (no diag, so only the drawn position's pass, from the kept lists) on
+    config 2's row shapes against the oracle, and the same tokens as the call with diag."""
+    w = small(128256, B=8, K=5, T=1.0, sigma=1.5)
+    inp = workloads.make(w)
+    ref = oracle.verify_filtered(host(inp["target"]), host(inp["draft"]), inp["tokens"].numpy(),
+                                 inp["seeds"].numpy().astype(np.uint64), w.temperature, 64, 0.95)
+    g = to_device(inp)
+    lean = sv.verify_filtered(g["target"], g["draft"], g["tokens"], g["seeds"], w.temperature, 64, 0.95,
+                              want_diag=False)
+    full = sv.verify_filtered(g["target"], g["draft"], g["tokens"], g["seeds"], w.temperature, 64, 0.95)
+    torch.cuda.synchronize()
+    assert sv.last_plan()["kernel"] == 6
+    assert_chain(lean, ref, w.K)
+    assert torch.equal(lean["accept_len"], full["accept_len"])
+    assert torch.equal(lean["out_tokens"], full["out_tokens"])
+    assert sv.read_status(lean["workspace"]) == 0
+
+
 def test_verify_filtered_without_filters_is_verify():
     w = small(50000, B=6, K=4)
     g = to_device(workloads.make(w))
