@@ -494,8 +494,9 @@ spec_status run_gamma(const Call& a, bool aligned) {
 
 // Standardised sampling: the per-row thresholds and the kept logits' (max, sum), then the draw kernel in its
 // filtering form (a logit below its row's threshold is -inf as it is read). Top-k up to FB_MAX_K on rows of
-// whole 16-byte words goes through bound_kernel, which leaves the rows it cannot settle to threshold_kernel;
-// every other filter goes through threshold_kernel alone. No filter at all is spec_verify itself.
+// whole 16-byte words goes through bound_kernel, which leaves the rows it cannot settle to threshold_kernel
+// and lists each settled target row's kept logits (up to D_LIST_CAP) for the draw; every other filter goes
+// through threshold_kernel alone, and the draw reads those rows whole. No filter at all is spec_verify itself.
 spec_status run_filtered(const Call& a, int top_k, float top_p) {
     const int eb = a.dtype == SPEC_BF16 ? 2 : 4;
     const bool rows16 = ((reinterpret_cast<uintptr_t>(a.target) | reinterpret_cast<uintptr_t>(a.others)) & 15) == 0 &&

@@ -519,7 +519,9 @@ __device__ __noinline__ int list_pass(const DParams& p, DrawShared<E>& S, int mo
 // draw_body runs it for one sequence on all DNT threads of one CTA: sequence blockIdx.x / cps and rank
 // cluster_ctarank() in a draw kernel launch (LAUNCHED), else sequence b_arg as the only CTA of its cluster
 // (cps = 1). d_smem: the bulk-copy slots and their mbarriers (bulk-copy mode). FILT: the logits of each row
-// below its threshold p.thr[row] count as -inf (standardised sampling), wherever the draw reads them.
+// below its threshold p.thr[row] count as -inf (standardised sampling), wherever the draw reads them; a
+// position whose target row's kept logits the threshold kernels listed (p.list_n >= 0) is drawn from that
+// list by list_pass, and no CTA reads its rows.
 template <class E, bool AL, bool LAUNCHED, bool FILT = false>
 __device__ __forceinline__ void draw_body(const DParams& p, DrawShared<E>& S, unsigned char* const d_smem,
                                           const int b_arg) {
